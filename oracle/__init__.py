@@ -1,0 +1,19 @@
+"""CPU oracle for the local MoE forward chain. Test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it and it
+never calls the CUDA library.
+"""
+from .moe_oracle import (  # noqa: F401
+    DispatchResult,
+    RouteResult,
+    combine,
+    dispatch,
+    experts_forward_dispatched,
+    forward,
+    forward_tokens,
+    route,
+    round_to_dtype,
+    silu,
+    widen,
+)

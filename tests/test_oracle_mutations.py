@@ -1,0 +1,113 @@
+"""Plant a plausible mistake in the CPU oracle (never in the CUDA path) and check
+that at least one pin of ``test_oracle_pins`` catches it."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle
+from tests.test_oracle_pins import PINS
+
+_route = moe_oracle.route
+_dispatch = moe_oracle.dispatch
+_combine = moe_oracle.combine
+_rows = moe_oracle._swiglu_rows
+
+
+def _route_ignoring_renormalize(logits, top_k, renormalize, out_dtype=None):
+    return _route(logits, top_k, False, out_dtype)
+
+
+def _route_ties_to_higher_id(logits, top_k, renormalize, out_dtype=None):
+    rt = _route(torch.flip(logits, dims=[1]), top_k, renormalize, out_dtype)
+    E = logits.shape[1]
+    rt.indices = (E - 1 - rt.indices.astype(np.int64)).astype(np.uint32)
+    return rt
+
+
+def _route_ascending_slots(logits, top_k, renormalize, out_dtype=None):
+    rt = _route(logits, top_k, renormalize, out_dtype)
+    rt.indices = rt.indices[:, ::-1].copy()
+    rt.weights32 = rt.weights32[:, ::-1].copy()
+    rt.weights = rt.weights[:, ::-1].copy()
+    rt.weights64 = rt.weights64[:, ::-1].copy()
+    return rt
+
+
+def _route_uniform_fallback(logits, top_k, renormalize, out_dtype=None):
+    rt = _route(logits, top_k, renormalize, out_dtype)
+    E = logits.shape[1]
+    for arr in (rt.weights32, rt.weights, rt.weights64):
+        arr[rt.bad] = 1.0 / (top_k if renormalize else E)
+    return rt
+
+
+def _dispatch_descending(indices, E):
+    d = _dispatch(indices, E)
+    for e in range(E):
+        lo, hi = int(d.offsets[e]), int(d.offsets[e + 1])
+        d.row_src[lo:hi] = d.row_src[lo:hi][::-1].copy()
+    d.inv[d.row_src] = np.arange(len(d.row_src), dtype=np.uint32)
+    return d
+
+
+def _dispatch_inclusive_offsets(indices, E):
+    d = _dispatch(indices, E)
+    d.offsets = np.concatenate([d.offsets[1:], d.offsets[-1:]])
+    return d
+
+
+def _combine_unweighted(y, inv, weights, T, top_k):
+    return _combine(y, inv, np.where(np.isnan(weights), np.nan, 1.0), T, top_k)
+
+
+def _combine_with_row_src(y, inv, weights, T, top_k):
+    order = np.argsort(np.asarray(inv, dtype=np.int64))
+    return _combine(y, order.astype(np.uint32), weights, T, top_k)
+
+
+def _rows_swap_gate_up(x, gate, up, down):
+    return _rows(x, up, gate, down)
+
+
+def _rows_drop_up(x, gate, up, down):
+    g = x @ gate.T
+    return moe_oracle.silu(g) @ down.T
+
+
+def _silu_wrong_sign(g):
+    return g / (1.0 + np.exp(g))
+
+
+def _forward_expert0_down(x, logits, gate, up, down, top_k, renormalize):
+    down0 = down[0:1].expand_as(down) if isinstance(down, torch.Tensor) else np.broadcast_to(down[0:1], down.shape)
+    return moe_oracle.__dict__["_forward_orig"](x, logits, gate, up, down0, top_k, renormalize)
+
+
+MUTATIONS = {
+    "no_renormalize": ("route", _route_ignoring_renormalize),
+    "ties_to_higher_id": ("route", _route_ties_to_higher_id),
+    "ascending_slot_order": ("route", _route_ascending_slots),
+    "uniform_fallback_on_nonfinite": ("route", _route_uniform_fallback),
+    "dispatch_descending_within_expert": ("dispatch", _dispatch_descending),
+    "dispatch_inclusive_offsets": ("dispatch", _dispatch_inclusive_offsets),
+    "combine_ignores_weights": ("combine", _combine_unweighted),
+    "combine_indexes_with_row_src": ("combine", _combine_with_row_src),
+    "swap_gate_and_up": ("_swiglu_rows", _rows_swap_gate_up),
+    "drop_up_projection": ("_swiglu_rows", _rows_drop_up),
+    "silu_wrong_sign": ("silu", _silu_wrong_sign),
+    "every_expert_uses_down_of_expert_0": ("forward", _forward_expert0_down),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setitem(moe_oracle.__dict__, "_forward_orig", moe_oracle.forward)
+    monkeypatch.setattr(moe_oracle, attr, fn)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(moe_oracle)
+        except Exception as exc:  # an assertion or a shape error both count
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin catches the planted mistake {name!r}"

@@ -1,0 +1,238 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) local Mixture-of-Experts forward chain.
+ *
+ * The chain (ruDNN user guide, section 3 "MoE workflow"):
+ *
+ *     logits [T,E] -> softmax/top-k routing -> compact per-expert dispatch
+ *                  -> SwiGLU experts -> routing-weighted combine -> out [T,H]
+ *
+ * Conventions shared by every entry point
+ *   - All pointers named "device" are CUDA device pointers on the current
+ *     device; the caller allocates and owns every buffer, including the
+ *     workspaces. The library allocates no device memory on any call below.
+ *   - Tensors are dense and row-major (C order) with the shapes given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call only enqueues work on that stream and returns; no
+ *     call waits for the device. Results are ready when the stream is.
+ *   - Every argument check runs on the host before anything is launched; a
+ *     failed check returns its status and enqueues nothing. MOE_ERR_CUDA
+ *     means a launch was rejected by the CUDA runtime (the message is in
+ *     moe_last_error()).
+ *   - Dtypes: MOE_F32, MOE_F16, MOE_BF16 (non-quantised floats, ruDNN user
+ *     guide section 4). Arithmetic: routing in FP32; expert projections
+ *     accumulate in FP32 (tensor cores for F16/BF16, FP32 FMA for F32, never
+ *     TF32); combine accumulates in FP32.
+ *   - Indices are uint32 (ruDNN user guide section 4: "indices use U32").
+ *   - Thread safety: calls on different streams may run concurrently when
+ *     their buffers do not overlap. A moe_experts handle is read-only after
+ *     creation and may be shared.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MOE_F32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype;
+
+/* Status codes: the C counterpart of MoeError (ruDNN user guide section 3:
+ * "computation entry points return Result with MoeError for invalid shapes,
+ * dtypes, or other arguments"). */
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,          /* a required pointer is NULL                          */
+  MOE_ERR_SHAPE = 2,         /* a size is out of range or sizes disagree             */
+  MOE_ERR_DTYPE = 3,         /* unknown dtype, or dtypes that must agree do not      */
+  MOE_ERR_TOP_K = 4,         /* top_k outside 1 <= top_k <= E (section 4)            */
+  MOE_ERR_ALIGNMENT = 5,     /* a pointer or row pitch is not 16-byte aligned        */
+  MOE_ERR_WORKSPACE = 6,     /* workspace pointer NULL or smaller than required      */
+  MOE_ERR_UNSUPPORTED = 7,   /* a valid request this build does not implement        */
+  MOE_ERR_CUDA = 8,          /* the CUDA runtime rejected a launch or query          */
+  MOE_ERR_DEVICE_CHECK = 9   /* a device-side wait ran out of time (see moe_device_status) */
+} moe_status;
+
+/* Opaque expert-weight handle (SwiGluExperts::new, ruDNN user guide section 3). */
+typedef struct moe_experts moe_experts;
+
+/* Human-readable name of a status code; never NULL. */
+const char* moe_status_string(int status);
+
+/* Detail of the last failed call on this host thread (empty if none). */
+const char* moe_last_error(void);
+
+/* ABI version of this library (major * 10000 + minor * 100 + patch). */
+int moe_version(void);
+
+/*
+ * moe_route - softmax/top-k routing (RoutingPlan, ruDNN user guide section 4
+ * "Routing contract"; restated in the Japanese guide section 4 and the
+ * ruDNN 0.1.5 User Guide section 4).
+ *
+ *   logits        device, [T, E] in `dtype`.
+ *   T, E          1 <= E <= 1024, T >= 0 (T = 0 enqueues nothing).
+ *   top_k         1 <= top_k <= E, else MOE_ERR_TOP_K.
+ *   renormalize   nonzero: divide the selected weights by their sum.
+ *   indices       device, [T, top_k] uint32 out: selected experts, slot 0 the
+ *                 largest logit, ties to the lower expert id.
+ *   weights       device, [T, top_k] out in `dtype`: FP32 softmax over all E
+ *                 experts, gathered, optionally renormalized, then rounded to
+ *                 `dtype` (round to nearest even).
+ *   weights_fp32  device, [T, top_k] float out before that rounding, or NULL.
+ *
+ * A row holding a NaN or +inf, or only -inf, gets NaN weights (no uniform
+ * fallback) and indices 0..top_k-1. Selection compares the logits
+ * themselves (softmax is strictly increasing, so this is "softmax then
+ * top-k" without ties added by exp rounding).
+ */
+moe_status moe_route(const void* logits, moe_dtype dtype, int64_t T, int64_t E, int32_t top_k,
+                     int32_t renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                     void* stream);
+
+/*
+ * moe_dispatch - compact per-expert token layout with no capacity dropping
+ * (RoutingPlan::dispatch; ruDNN user guide section 5 "Expert weights and
+ * dispatch": tokens are never dropped, a saved mapping restores token order).
+ *
+ *   indices       device, [T, top_k] uint32 (from moe_route or the caller).
+ *   x             device, [T, H] in `dtype`, or NULL to skip x_dispatched.
+ *   counts        device, [E] uint32 out: rows per expert.
+ *   offsets       device, [E + 1] uint32 out: exclusive prefix of counts.
+ *   row_src       device, [T * top_k] uint32 out: dispatched row r holds slot
+ *                 row_src[r] = t * top_k + j.
+ *   inv           device, [T * top_k] uint32 out: slot t * top_k + j sits in
+ *                 dispatched row inv[t * top_k + j].
+ *   x_dispatched  device, [T * top_k, H] out (row r = x[row_src[r] / top_k]),
+ *                 or NULL. Needs x.
+ *   workspace     device scratch of moe_dispatch_workspace_size(T, E, top_k)
+ *                 bytes (256-byte aligned); contents need not be initialised.
+ *
+ * Order within an expert is ascending t * top_k + j, so the maps are the
+ * same on every run (the pages leave that order free). An index >= E is not
+ * dispatched: its inv entry is 0xFFFFFFFF, counts exclude it, and
+ * moe_combine writes a NaN row for that token. No out-of-range access, no
+ * host synchronisation.
+ */
+size_t moe_dispatch_workspace_size(int64_t T, int64_t E, int32_t top_k);
+moe_status moe_dispatch(const uint32_t* indices, int64_t T, int64_t E, int32_t top_k,
+                        const void* x, moe_dtype dtype, int64_t H, uint32_t* counts,
+                        uint32_t* offsets, uint32_t* row_src, uint32_t* inv, void* x_dispatched,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_experts_create - validate and wrap bias-free SwiGLU expert weights
+ * (SwiGluExperts::new; ruDNN user guide section 5: gate and up [E, I, H],
+ * down [E, H, I], one float dtype, one device).
+ *
+ *   gate, up      device, [E, I, H] in `dtype`.
+ *   down          device, [E, H, I] in `dtype`.
+ *   E, H, I       1 <= E <= 1024; H, I >= 1. F16/BF16 need H and I to be
+ *                 multiples of 8 (16-byte row pitch), else MOE_ERR_ALIGNMENT.
+ *   out           receives the handle.
+ *
+ * The handle records the pointers (the caller keeps the weights alive and
+ * unchanged while it is in use) and the prebuilt TMA descriptors. It is
+ * reusable across batches and read-only; free it with moe_experts_destroy.
+ * Device is the current device at creation.
+ */
+moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dtype,
+                              int64_t E, int64_t H, int64_t I, moe_experts** out);
+void moe_experts_destroy(moe_experts* experts);
+
+/*
+ * moe_experts_forward_dispatched - SwiGLU experts on dispatched rows
+ * (SwiGluExperts::forward_dispatched; "tiny-llm deep dive 5: ops.rs",
+ * section on SiLU: FFN(x) = W_down (SiLU(W_gate x) * W_up x)).
+ *
+ *   x_dispatched  device, [rows, H] in the experts' dtype (from moe_dispatch).
+ *   offsets       device, [E + 1] uint32 (from moe_dispatch); expert e owns
+ *                 rows offsets[e] .. offsets[e+1]-1; offsets[E] must equal
+ *                 rows. The host never reads the counts.
+ *   rows          T * top_k.
+ *   y_dispatched  device, [rows, H] out in the experts' dtype:
+ *                 y = W_down[e] h, h = SiLU(W_gate[e] x) * (W_up[e] x), FP32
+ *                 accumulation, h rounded to the dtype before the down
+ *                 projection.
+ *   workspace     device scratch of
+ *                 moe_experts_forward_dispatched_workspace_size(experts, rows)
+ *                 bytes (holds h).
+ */
+size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* experts, int64_t rows);
+moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void* x_dispatched,
+                                          const uint32_t* offsets, int64_t rows,
+                                          void* y_dispatched, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
+ * moe_combine - restore token order and take the routing-weighted sum
+ * (DispatchedTokens::combine; ruDNN user guide section 6: combine uses the
+ * dispatch mapping to restore token order and merges the expert outputs with
+ * the routing weights).
+ *
+ *   y_dispatched  device, [T * top_k, H] in `dtype`.
+ *   inv           device, [T * top_k] uint32 (from moe_dispatch).
+ *   weights       device, [T, top_k] in `weights_dtype` (from moe_route).
+ *   out           device, [T, H] out in `dtype`:
+ *                 out[t] = sum over j = 0..top_k-1, in that order, of
+ *                 w[t, j] * y[inv[t * top_k + j]], FP32 accumulation, then
+ *                 rounded to `dtype`. Deterministic: no atomics.
+ */
+moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                       const void* weights, moe_dtype weights_dtype, int64_t T, int32_t top_k,
+                       int64_t H, void* out, void* stream);
+
+/*
+ * moe_forward - the whole local chain in one call (SwiGluExperts::forward;
+ * ruDNN user guide section 6): route, dispatch, SwiGLU experts, combine.
+ *
+ *   experts       handle from moe_experts_create (its dtype is x's and out's).
+ *   x             device, [T, H] in the experts' dtype.
+ *   logits        device, [T, E] in `logits_dtype` (E from the handle).
+ *   top_k, renormalize   as in moe_route.
+ *   out           device, [T, H] out in the experts' dtype.
+ *   indices_opt   device [T, top_k] uint32 out, or NULL (kept in workspace).
+ *   weights_opt   device [T, top_k] out in `logits_dtype`, or NULL.
+ *   workspace     device scratch of moe_forward_workspace_size(experts, T,
+ *                 top_k) bytes, 256-byte aligned, uninitialised is fine.
+ *
+ * Same numerics as calling moe_route, moe_dispatch,
+ * moe_experts_forward_dispatched and moe_combine in turn: the outputs are
+ * bit-identical to that sequence.
+ */
+size_t moe_forward_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k);
+moe_status moe_forward(const moe_experts* experts, const void* x, const void* logits,
+                       moe_dtype logits_dtype, int64_t T, int32_t top_k, int32_t renormalize,
+                       void* out, uint32_t* indices_opt, void* weights_opt, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * moe_device_status - read (and clear, if `clear` is nonzero) the device
+ * status word. The expert GEMM kernels bound every pipeline wait (about one
+ * second); a wait that runs out stops its kernel's remaining work, lets the
+ * copies and MMAs already issued finish, frees its tensor memory, returns,
+ * and records a code here instead of hanging the GPU. Codes (first one
+ * wins): 0x11 producer waiting for a free stage, 0x12 MMA waiting for a
+ * loaded stage, 0x13 MMA waiting for a drained accumulator, 0x14 epilogue
+ * waiting for a finished accumulator, 0x15 / 0x16 teardown drains, 0x100
+ * moe_selftest_bounded_wait. Synchronises the current device; *code = 0 when
+ * no wait has timed out.
+ */
+moe_status moe_device_status(uint32_t* code, int32_t clear);
+
+/*
+ * moe_selftest_bounded_wait - launch one thread that waits on an mbarrier
+ * nothing ever arrives on, with a limit of `limit_us` microseconds
+ * (1 .. 10^7). The wait gives up, records 0x100 in the device status word
+ * and the kernel returns; the CUDA context stays usable. Exercises the same
+ * bounded-wait routine the expert GEMMs use.
+ */
+moe_status moe_selftest_bounded_wait(uint32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,246 @@
+"""Python binding of the GB300 local MoE forward chain.
+
+Thin ctypes layer over the C ABI in ``include/moe.h`` (``libmoe_gb300.so``,
+built in-tree by ``_build.build``). The functions carry the C names and only
+marshal arguments: PyTorch supplies device memory and the current stream;
+every step of the chain runs in the library's CUDA kernels. There is no
+fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from collections import namedtuple
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libmoe_gb300.so"
+
+MOE_F32, MOE_F16, MOE_BF16 = 0, 1, 2
+_DTYPE = {torch.float32: MOE_F32, torch.float16: MOE_F16, torch.bfloat16: MOE_BF16}
+
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_DTYPE", 4: "MOE_ERR_TOP_K",
+    5: "MOE_ERR_ALIGNMENT", 6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_UNSUPPORTED", 8: "MOE_ERR_CUDA",
+    9: "MOE_ERR_DEVICE_CHECK",
+}
+
+# Every entry point declared in include/moe.h: name -> (restype, argtypes).
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_version": (ctypes.c_int, []),
+    "moe_route": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _I32, _P, _P, _P, _P]),
+    "moe_dispatch_workspace_size": (_SZ, [_I64, _I64, _I32]),
+    "moe_dispatch": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, ctypes.c_int, _I64, _P, _P, _P, _P, _P,
+                                    _P, _SZ, _P]),
+    "moe_experts_create": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
+                                          ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_experts_destroy": (None, [_P]),
+    "moe_experts_forward_dispatched_workspace_size": (_SZ, [_P, _I64]),
+    "moe_experts_forward_dispatched": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
+    "moe_combine": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _I64, _I32, _I64, _P, _P]),
+    "moe_forward_workspace_size": (_SZ, [_P, _I64, _I32]),
+    "moe_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32]),
+    "moe_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _P]),
+}
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    """A nonzero moe_status from the library (the MoeError of the pages)."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, f"status {status}")
+        super().__init__(f"{self.name}: {message}")
+
+
+def load_library(path: str | Path | None = None):
+    """Load libmoe_gb300.so (once) and declare every entry point. Raises if it
+    is missing: there is no CPU or eager fallback."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path is not None else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() "
+                           "(nvcc, sm_103a); there is no fallback path")
+    lib = ctypes.CDLL(str(p))
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise MoeError(status, load_library().moe_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_tensor(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE:
+        raise MoeError(3, f"unsupported dtype {t.dtype}")
+    return _DTYPE[t.dtype]
+
+
+def _workspace(nbytes: int, device, ws: torch.Tensor | None) -> torch.Tensor:
+    if ws is not None:
+        return ws
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def moe_route(logits: torch.Tensor, top_k: int, renormalize: bool, *, indices=None, weights=None,
+              weights_fp32=False, stream=None):
+    """RoutingPlan: returns (indices [T,k] uint32 as int32 view, weights [T,k] in
+    the logits dtype[, FP32 weights before the cast])."""
+    lib = load_library()
+    _dev_tensor(logits, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    if indices is None:
+        indices = torch.empty(T, top_k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(T, top_k, dtype=logits.dtype, device=dev)
+    w32 = torch.empty(T, top_k, dtype=torch.float32, device=dev) if weights_fp32 is True else (
+        weights_fp32 if isinstance(weights_fp32, torch.Tensor) else None)
+    _check(lib.moe_route(_ptr(logits), _dt(logits), T, E, top_k, int(bool(renormalize)), _ptr(indices),
+                         _ptr(weights), _ptr(w32), _stream(stream)))
+    return (indices, weights, w32) if w32 is not None else (indices, weights)
+
+
+DispatchedTokens = namedtuple("DispatchedTokens", "counts offsets row_src inv x_dispatched")
+
+
+def moe_dispatch(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None = None,
+                 workspace=None, stream=None) -> DispatchedTokens:
+    """RoutingPlan::dispatch: per-expert counts/offsets, row_src, inv and (if x
+    is given) x_dispatched [T*k, H]."""
+    lib = load_library()
+    _dev_tensor(indices, "indices")
+    T, k = indices.shape
+    dev = indices.device
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    row_src = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    xd = None
+    H, xdt = 0, MOE_F32
+    if x is not None:
+        _dev_tensor(x, "x")
+        H, xdt = x.shape[1], _dt(x)
+        xd = torch.empty(T * k, H, dtype=x.dtype, device=dev)
+    need = lib.moe_dispatch_workspace_size(T, num_experts, k)
+    ws = _workspace(need, dev, workspace)
+    _check(lib.moe_dispatch(_ptr(indices), T, num_experts, k, _ptr(x), xdt, H, _ptr(counts),
+                            _ptr(offsets), _ptr(row_src), _ptr(inv), _ptr(xd), _ptr(ws),
+                            ws.numel(), _stream(stream)))
+    return DispatchedTokens(counts, offsets, row_src, inv, xd)
+
+
+class Experts:
+    """SwiGluExperts: a handle over gate/up [E,I,H] and down [E,H,I] (kept alive here)."""
+
+    def __init__(self, gate: torch.Tensor, up: torch.Tensor, down: torch.Tensor):
+        lib = load_library()
+        for name, t in (("gate", gate), ("up", up), ("down", down)):
+            _dev_tensor(t, name)
+        E, I, H = gate.shape
+        self.gate, self.up, self.down = gate, up, down
+        self.E, self.H, self.I = E, H, I
+        self.dtype = gate.dtype
+        handle = ctypes.c_void_p()
+        _check(lib.moe_experts_create(_ptr(gate), _ptr(up), _ptr(down), _dt(gate), E, H, I,
+                                      ctypes.byref(handle)))
+        self.handle = handle
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.moe_experts_destroy(self.handle)
+            self.handle = None
+
+
+def moe_experts_create(gate, up, down) -> Experts:
+    return Experts(gate, up, down)
+
+
+def moe_experts_forward_dispatched(experts: Experts, x_dispatched: torch.Tensor,
+                                   offsets: torch.Tensor, out=None, workspace=None, stream=None):
+    """SwiGluExperts::forward_dispatched: y_dispatched [rows, H] in the experts' dtype."""
+    lib = load_library()
+    _dev_tensor(x_dispatched, "x_dispatched")
+    rows = x_dispatched.shape[0]
+    y = out if out is not None else torch.empty(rows, experts.H, dtype=experts.dtype,
+                                                device=x_dispatched.device)
+    need = lib.moe_experts_forward_dispatched_workspace_size(experts.handle, rows)
+    ws = _workspace(need, x_dispatched.device, workspace)
+    _check(lib.moe_experts_forward_dispatched(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows,
+                                              _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def moe_combine(y_dispatched: torch.Tensor, inv: torch.Tensor, weights: torch.Tensor, out=None,
+                stream=None):
+    """DispatchedTokens::combine: out [T, H] in y's dtype."""
+    lib = load_library()
+    _dev_tensor(y_dispatched, "y_dispatched")
+    T, k = weights.shape
+    H = y_dispatched.shape[1]
+    o = out if out is not None else torch.empty(T, H, dtype=y_dispatched.dtype, device=y_dispatched.device)
+    _check(lib.moe_combine(_ptr(y_dispatched), _dt(y_dispatched), _ptr(inv), _ptr(weights), _dt(weights),
+                           T, k, H, _ptr(o), _stream(stream)))
+    return o
+
+
+def moe_forward_workspace_size(experts: Experts, T: int, top_k: int) -> int:
+    return int(load_library().moe_forward_workspace_size(experts.handle, T, top_k))
+
+
+def moe_forward(experts: Experts, x: torch.Tensor, logits: torch.Tensor, top_k: int,
+                renormalize: bool, *, out=None, indices=None, weights=None, workspace=None,
+                stream=None):
+    """SwiGluExperts::forward: the whole chain, out [T, H]."""
+    lib = load_library()
+    _dev_tensor(x, "x")
+    _dev_tensor(logits, "logits")
+    T = x.shape[0]
+    o = out if out is not None else torch.empty(T, experts.H, dtype=experts.dtype, device=x.device)
+    ws = _workspace(lib.moe_forward_workspace_size(experts.handle, T, top_k), x.device, workspace)
+    _check(lib.moe_forward(experts.handle, _ptr(x), _ptr(logits), _dt(logits), T, top_k,
+                           int(bool(renormalize)), _ptr(o), _ptr(indices), _ptr(weights), _ptr(ws),
+                           ws.numel(), _stream(stream)))
+    return o
+
+
+def moe_device_status(clear: bool = True) -> int:
+    code = ctypes.c_uint32(0)
+    _check(load_library().moe_device_status(ctypes.byref(code), int(clear)))
+    return code.value
+
+
+def moe_selftest_bounded_wait(limit_us: int, stream=None):
+    _check(load_library().moe_selftest_bounded_wait(limit_us, _stream(stream)))

@@ -1,0 +1,340 @@
+// C ABI of the local MoE forward chain: argument checks on the host, then
+// kernel launches on the caller's stream. See include/moe.h for the contract
+// of every entry point. No entry point allocates device memory or waits for
+// the device (moe_device_status excepted, which exists to read a result).
+#include <stdio.h>
+
+#include <limits>
+#include <string>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+using moe::align_up;
+using moe::dtype_size;
+using moe::dtype_valid;
+
+struct moe_experts {
+  int device;
+  int num_sms;
+  moe_dtype dtype;
+  int64_t E, H, I;
+  const void* gate;
+  const void* up;
+  const void* down;
+  moe::TcWeights tc;  // TMA descriptors of gate/up/down (F16/BF16 only)
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const std::string& why) {
+  g_last_error = why;
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t err, const char* where, const char* why = nullptr) {
+  std::string msg = std::string(where) + ": " + cudaGetErrorString(err);
+  if (why != nullptr) msg += std::string(" (") + why + ")";
+  return fail(MOE_ERR_CUDA, msg);
+}
+
+moe_status ok() {
+  g_last_error.clear();
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+bool aligned256(const void* p) { return reinterpret_cast<uintptr_t>(p) % 256 == 0; }
+
+// Flat slot numbers t*k+j and dispatched row numbers are uint32 and
+// 0xFFFFFFFF marks an undispatched slot, so T*k must stay below it.
+bool slots_fit(int64_t T, int64_t k) {
+  return T >= 0 && k >= 1 && T <= (int64_t{0xFFFFFFFE} / k);
+}
+
+moe_status check_route_args(const void* logits, int dtype, int64_t T, int64_t E, int64_t top_k,
+                            const void* indices, const void* weights) {
+  if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  if (top_k < 1 || top_k > E) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= E");
+  if (T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && (logits == nullptr || indices == nullptr || weights == nullptr))
+    return fail(MOE_ERR_NULL, "logits, indices and weights must be non-NULL");
+  return MOE_OK;
+}
+
+struct ForwardLayout {
+  size_t indices, weights, counts, offsets, row_src, inv, scratch, xd, h, yd, total;
+};
+
+ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(top_k);
+  const size_t es = dtype_size(ex->dtype);
+  ForwardLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return at;
+  };
+  L.indices = take(n * 4);
+  L.weights = take(n * 4);  // room for any logits dtype
+  L.counts = take(static_cast<size_t>(ex->E) * 4);
+  L.offsets = take(static_cast<size_t>(ex->E + 1) * 4);
+  L.row_src = take(n * 4);
+  L.inv = take(n * 4);
+  L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
+  L.xd = take(n * static_cast<size_t>(ex->H) * es);
+  L.h = take(n * static_cast<size_t>(ex->I) * es);
+  L.yd = take(n * static_cast<size_t>(ex->H) * es);
+  L.total = off;
+  return L;
+}
+
+moe_status check_current_device(const moe_experts* ex) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev != ex->device)
+    return fail(MOE_ERR_UNSUPPORTED, "the current device is not the device the experts were created on");
+  return MOE_OK;
+}
+
+moe_status run_experts(const moe_experts* ex, const void* xd, const uint32_t* offsets, int64_t rows,
+                       void* h, void* y, cudaStream_t s) {
+  cudaError_t err;
+  const char* why = nullptr;
+  if (ex->dtype == MOE_F32) {
+    err = moe::launch_experts_simt_f32(static_cast<const float*>(xd), offsets, static_cast<int>(ex->E),
+                                       rows, static_cast<const float*>(ex->gate),
+                                       static_cast<const float*>(ex->up),
+                                       static_cast<const float*>(ex->down), ex->H, ex->I,
+                                       static_cast<float*>(h), static_cast<float*>(y), s);
+  } else {
+    err = moe::launch_experts_tc(ex->tc, ex->dtype, xd, offsets, static_cast<int>(ex->E), rows,
+                                 ex->H, ex->I, h, y, ex->num_sms, s, &why);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "expert GEMM launch", why);
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_NULL: return "MOE_ERR_NULL";
+    case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE";
+    case MOE_ERR_DTYPE: return "MOE_ERR_DTYPE";
+    case MOE_ERR_TOP_K: return "MOE_ERR_TOP_K";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+int moe_version(void) { return 10000; }
+
+moe_status moe_route(const void* logits, moe_dtype dtype, int64_t T, int64_t E, int32_t top_k,
+                     int32_t renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                     void* stream) {
+  moe_status st = check_route_args(logits, dtype, T, E, top_k, indices, weights);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_route(logits, dtype, T, static_cast<int>(E), top_k, renormalize != 0,
+                                      indices, weights, weights_fp32, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_route launch");
+  return ok();
+}
+
+size_t moe_dispatch_workspace_size(int64_t T, int64_t E, int32_t top_k) {
+  if (T < 0 || E < 1 || top_k < 1) return 0;
+  return moe::dispatch_scratch_bytes(T, E, top_k);
+}
+
+moe_status moe_dispatch(const uint32_t* indices, int64_t T, int64_t E, int32_t top_k,
+                        const void* x, moe_dtype dtype, int64_t H, uint32_t* counts,
+                        uint32_t* offsets, uint32_t* row_src, uint32_t* inv, void* x_dispatched,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  if (top_k < 1 || top_k > E) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= E");
+  if (T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (counts == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "counts and offsets must be non-NULL");
+  if (T > 0 && (indices == nullptr || row_src == nullptr || inv == nullptr))
+    return fail(MOE_ERR_NULL, "indices, row_src and inv must be non-NULL");
+  if (x_dispatched != nullptr) {
+    if (x == nullptr) return fail(MOE_ERR_NULL, "x_dispatched needs x");
+    if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+    if (H < 1) return fail(MOE_ERR_SHAPE, "H must be >= 1");
+  }
+  const size_t need = moe::dispatch_scratch_bytes(T, E, top_k);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_dispatch_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  cudaError_t err = moe::launch_dispatch(indices, T, static_cast<int>(E), top_k, x, dtype, H, counts,
+                                         offsets, row_src, inv, x_dispatched, workspace,
+                                         static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch launch");
+  return ok();
+}
+
+moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dtype,
+                              int64_t E, int64_t H, int64_t I, moe_experts** out) {
+  if (out == nullptr) return fail(MOE_ERR_NULL, "out must be non-NULL");
+  *out = nullptr;
+  if (gate == nullptr || up == nullptr || down == nullptr)
+    return fail(MOE_ERR_NULL, "gate, up and down must be non-NULL");
+  if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "expert dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  if (H < 1 || I < 1 || H > (int64_t{1} << 30) || I > (int64_t{1} << 30))
+    return fail(MOE_ERR_SHAPE, "H and I must be in 1 .. 2^30");
+  if (dtype != MOE_F32) {
+    if (H % 8 != 0 || I % 8 != 0)
+      return fail(MOE_ERR_ALIGNMENT, "F16/BF16 experts need H and I to be multiples of 8 (16-byte rows)");
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(down))
+      return fail(MOE_ERR_ALIGNMENT, "expert weights must be 16-byte aligned");
+  }
+  moe_experts* ex = new moe_experts{};
+  ex->dtype = dtype;
+  ex->E = E;
+  ex->H = H;
+  ex->I = I;
+  ex->gate = gate;
+  ex->up = up;
+  ex->down = down;
+  cudaError_t err = cudaGetDevice(&ex->device);
+  if (err == cudaSuccess)
+    err = cudaDeviceGetAttribute(&ex->num_sms, cudaDevAttrMultiProcessorCount, ex->device);
+  if (err != cudaSuccess) {
+    delete ex;
+    return cuda_fail(err, "moe_experts_create device query");
+  }
+  if (dtype != MOE_F32) {
+    const char* why = nullptr;
+    if (!moe::tc_encode_weights(gate, up, down, dtype, E, H, I, &ex->tc, &why)) {
+      delete ex;
+      return fail(MOE_ERR_CUDA, why ? why : "tensor map encoding failed");
+    }
+  }
+  *out = ex;
+  return ok();
+}
+
+void moe_experts_destroy(moe_experts* experts) { delete experts; }
+
+size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* ex, int64_t rows) {
+  if (ex == nullptr || rows < 0) return 0;
+  return align_up(static_cast<size_t>(rows) * static_cast<size_t>(ex->I) * dtype_size(ex->dtype) + 1, 256);
+}
+
+moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_dispatched,
+                                          const uint32_t* offsets, int64_t rows,
+                                          void* y_dispatched, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  if (ex == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "experts and offsets must be non-NULL");
+  if (rows < 0 || rows >= int64_t{0xFFFFFFFF}) return fail(MOE_ERR_SHAPE, "rows must be in 0 .. 2^32-2");
+  if (rows > 0 && (x_dispatched == nullptr || y_dispatched == nullptr))
+    return fail(MOE_ERR_NULL, "x_dispatched and y_dispatched must be non-NULL");
+  const size_t need = moe_experts_forward_dispatched_workspace_size(ex, rows);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_experts_forward_dispatched_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (ex->dtype != MOE_F32 && (!aligned16(x_dispatched) || !aligned16(y_dispatched)))
+    return fail(MOE_ERR_ALIGNMENT, "x_dispatched and y_dispatched must be 16-byte aligned");
+  moe_status st = check_current_device(ex);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return ok();
+  st = run_experts(ex, x_dispatched, offsets, rows, workspace, y_dispatched,
+                   static_cast<cudaStream_t>(stream));
+  if (st != MOE_OK) return st;
+  return ok();
+}
+
+moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                       const void* weights, moe_dtype weights_dtype, int64_t T, int32_t top_k,
+                       int64_t H, void* out, void* stream) {
+  if (!dtype_valid(dtype) || !dtype_valid(weights_dtype))
+    return fail(MOE_ERR_DTYPE, "dtypes must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (top_k < 1) return fail(MOE_ERR_TOP_K, "top_k must be >= 1");
+  if (T < 0 || !slots_fit(T, top_k) || H < 1) return fail(MOE_ERR_SHAPE, "need T >= 0, H >= 1, T*top_k < 2^32-1");
+  if (T > 0 && (y_dispatched == nullptr || inv == nullptr || weights == nullptr || out == nullptr))
+    return fail(MOE_ERR_NULL, "y_dispatched, inv, weights and out must be non-NULL");
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_combine(y_dispatched, dtype, inv, weights, weights_dtype, T, top_k, H,
+                                        out, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_combine launch");
+  return ok();
+}
+
+size_t moe_forward_workspace_size(const moe_experts* ex, int64_t T, int32_t top_k) {
+  if (ex == nullptr || T < 0 || top_k < 1 || !slots_fit(T, top_k)) return 0;
+  return forward_layout(ex, T, top_k).total;
+}
+
+moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
+                       moe_dtype logits_dtype, int64_t T, int32_t top_k, int32_t renormalize,
+                       void* out, uint32_t* indices_opt, void* weights_opt, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (ex == nullptr) return fail(MOE_ERR_NULL, "experts must be non-NULL");
+  moe_status st = check_route_args(logits, logits_dtype, T, ex->E, top_k, logits, logits);
+  if (st != MOE_OK) return st;
+  if (T > 0 && (x == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "x and out must be non-NULL");
+  const ForwardLayout L = forward_layout(ex, T, top_k);
+  if (workspace == nullptr || workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_forward_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  st = check_current_device(ex);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* indices = indices_opt ? indices_opt : reinterpret_cast<uint32_t*>(ws + L.indices);
+  void* weights = weights_opt ? weights_opt : static_cast<void*>(ws + L.weights);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(ws + L.counts);
+  uint32_t* offsets = reinterpret_cast<uint32_t*>(ws + L.offsets);
+  uint32_t* row_src = reinterpret_cast<uint32_t*>(ws + L.row_src);
+  uint32_t* inv = reinterpret_cast<uint32_t*>(ws + L.inv);
+  void* xd = ws + L.xd;
+  void* h = ws + L.h;
+  void* yd = ws + L.yd;
+  const int64_t rows = T * top_k;
+
+  cudaError_t err = moe::launch_route(logits, logits_dtype, T, static_cast<int>(ex->E), top_k,
+                                      renormalize != 0, indices, weights, nullptr, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward route launch");
+  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, x, ex->dtype, ex->H, counts,
+                             offsets, row_src, inv, xd, ws + L.scratch, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward dispatch launch");
+  st = run_experts(ex, xd, offsets, rows, h, yd, s);
+  if (st != MOE_OK) return st;
+  err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward combine launch");
+  return ok();
+}
+
+moe_status moe_device_status(uint32_t* code, int32_t clear) {
+  if (code == nullptr) return fail(MOE_ERR_NULL, "code must be non-NULL");
+  cudaError_t err = moe::read_device_status(code, clear != 0);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_device_status");
+  return ok();
+}
+
+moe_status moe_selftest_bounded_wait(uint32_t limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u)
+    return fail(MOE_ERR_SHAPE, "limit_us must be in 1 .. 10^7");
+  cudaError_t err = moe::launch_bounded_wait_selftest(limit_us, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_selftest_bounded_wait launch");
+  return ok();
+}
+
+}  // extern "C"

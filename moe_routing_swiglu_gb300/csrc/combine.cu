@@ -1,0 +1,128 @@
+// K5: weighted combine back to token order (ruDNN user guide, section 6:
+// combine restores token order through the dispatch mapping and merges the
+// expert outputs with the routing weights).
+//
+// out[t, :] = sum_{j=0..k-1} w[t, j] * y[inv[t*k + j], :], accumulated in FP32
+// in slot order j = 0, 1, ..., k-1, then rounded to the output dtype. One
+// block per token (grid-stride); each thread owns 16-byte vectors of the row.
+// No atomics, so the result does not depend on scheduling. A slot whose inv
+// entry is INVALID_ROW (an index >= E at dispatch), or any entry >= T*k,
+// makes its token's row NaN instead of reading out of range.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<__half> { static constexpr int N = 8; };
+template <> struct Vec<__nv_bfloat16> { static constexpr int N = 8; };
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec<T>::N]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+  for (int i = 0; i < Vec<T>::N; ++i) v[i] = to_f32(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(T* p, const float (&v)[Vec<T>::N]) {
+  uint4 raw;
+  T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+  for (int i = 0; i < Vec<T>::N; ++i) e[i] = from_f32<T>(v[i]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+
+template <typename T, typename TW, bool VEC>
+__global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
+                                                      const uint32_t* __restrict__ inv,
+                                                      const TW* __restrict__ w, int64_t T_tokens,
+                                                      int k, int64_t H, uint32_t rows,
+                                                      T* __restrict__ out) {
+  constexpr int NV = VEC ? Vec<T>::N : 1;
+  const float qnan = __int_as_float(0x7FC00000);
+  for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * NV; c < H; c += static_cast<int64_t>(blockDim.x) * NV) {
+      float acc[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const float wj = to_f32(w[t * k + j]);
+        const uint32_t r = inv[t * k + j];
+        if (r >= rows) {  // INVALID_ROW, or a map entry out of range
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = qnan;
+          continue;
+        }
+        const T* src = y + static_cast<int64_t>(r) * H + c;
+        if constexpr (VEC) {
+          float v[NV];
+          load_vec<T>(src, v);
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+        } else {
+          acc[0] = fmaf(wj, to_f32(src[0]), acc[0]);
+        }
+      }
+      T* dst = out + t * H + c;
+      if constexpr (VEC) {
+        store_vec<T>(dst, acc);
+      } else {
+        dst[0] = from_f32<T>(acc[0]);
+      }
+    }
+  }
+}
+
+template <typename T, typename TW>
+cudaError_t launch_combine_t(const void* y, const uint32_t* inv, const void* w, int64_t T_tokens,
+                             int k, int64_t H, void* out, cudaStream_t stream) {
+  const int blocks = static_cast<int>(T_tokens < 65536 ? T_tokens : 65536);
+  const bool vec = (H * static_cast<int64_t>(sizeof(T))) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(out) % 16 == 0;
+  int threads = 256;
+  const int64_t per_thread = vec ? Vec<T>::N : 1;
+  while (threads > 32 && static_cast<int64_t>(threads / 2) * per_thread >= H) threads /= 2;
+  if (vec) {
+    combine_kernel<T, TW, true><<<blocks, threads, 0, stream>>>(
+        static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
+        static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
+  } else {
+    combine_kernel<T, TW, false><<<blocks, threads, 0, stream>>>(
+        static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
+        static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine_w(const void* y, const uint32_t* inv, const void* w, moe_dtype wdt,
+                             int64_t T_tokens, int k, int64_t H, void* out, cudaStream_t stream) {
+  switch (wdt) {
+    case MOE_F32: return launch_combine_t<T, float>(y, inv, w, T_tokens, k, H, out, stream);
+    case MOE_F16: return launch_combine_t<T, __half>(y, inv, w, T_tokens, k, H, out, stream);
+    default: return launch_combine_t<T, __nv_bfloat16>(y, inv, w, T_tokens, k, H, out, stream);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                           const void* weights, moe_dtype weights_dtype, int64_t T, int top_k,
+                           int64_t H, void* out, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  switch (dtype) {
+    case MOE_F32:
+      return launch_combine_w<float>(y_dispatched, inv, weights, weights_dtype, T, top_k, H, out, stream);
+    case MOE_F16:
+      return launch_combine_w<__half>(y_dispatched, inv, weights, weights_dtype, T, top_k, H, out, stream);
+    default:
+      return launch_combine_w<__nv_bfloat16>(y_dispatched, inv, weights, weights_dtype, T, top_k, H, out, stream);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,52 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units. Every launcher only enqueues work on `stream`; argument
+// checks have already been done by the caller.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- K1 routing (route.cu)
+constexpr int ROUTE_MAX_E = 1024;
+cudaError_t launch_route(const void* logits, moe_dtype dtype, int64_t T, int E, int top_k,
+                         bool renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                         cudaStream_t stream);
+
+// ---- K2 dispatch (dispatch.cu)
+constexpr int DISPATCH_CHUNK = 2048;  // flat slots per counting/scatter block
+size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k);
+cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
+                            moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                            uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
+                            cudaStream_t stream);
+
+// ---- K5 combine (combine.cu)
+cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                           const void* weights, moe_dtype weights_dtype, int64_t T, int top_k,
+                           int64_t H, void* out, cudaStream_t stream);
+
+// ---- K7 FP32 experts on CUDA cores (experts_simt.cu)
+cudaError_t launch_experts_simt_f32(const float* x_dispatched, const uint32_t* offsets, int E,
+                                    int64_t rows, const float* gate, const float* up,
+                                    const float* down, int64_t H, int64_t I, float* h, float* y,
+                                    cudaStream_t stream);
+
+// ---- K3/K4 F16/BF16 experts on tcgen05 tensor cores (experts_tc.cu)
+struct TcWeights {
+  CUtensorMap gate, up, down;  // 3-D maps over [E, rows, K] with 64 x 128 x 1 boxes
+};
+bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,
+                       int64_t E, int64_t H, int64_t I, TcWeights* out, const char** why);
+cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, const void* x_dispatched,
+                              const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
+                              void* h, void* y, int num_sms, cudaStream_t stream, const char** why);
+cudaError_t read_device_status(uint32_t* code, bool clear);
+cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,139 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+declared in include/moe.h, and rejects bad arguments on the host before any
+CUDA call (these checks run on the CPU)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import moe_routing_swiglu_gb300 as moe
+from moe_routing_swiglu_gb300 import _build
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "moe.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_chain():
+    names = declared_functions()
+    for required in ("moe_route", "moe_dispatch", "moe_experts_create", "moe_experts_forward_dispatched",
+                     "moe_combine", "moe_forward"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(moe.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS_NAMES.items():
+        assert lib.moe_status_string(code).decode() == name
+    assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"
+    assert lib.moe_version() == 10000
+
+
+P = ctypes.c_void_p
+FAKE = P(0x100000)  # never dereferenced: every case below fails a host check first
+
+
+def _route(lib, logits=FAKE, dtype=2, T=4, E=8, k=2, idx=FAKE, w=FAKE):
+    return lib.moe_route(logits, dtype, T, E, k, 1, idx, w, None, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(w=None), 1),
+    (dict(dtype=7), 3), (dict(dtype=-1), 3),
+    (dict(k=0), 4), (dict(k=9), 4), (dict(k=-3), 4),
+    (dict(E=0, k=1), 2), (dict(E=1025, k=1), 2), (dict(T=-1), 2),
+    (dict(T=1 << 31, k=2), 2),
+])
+def test_route_rejects_bad_arguments(lib, kwargs, status):
+    assert _route(lib, **kwargs) == status
+    assert lib.moe_last_error().decode() != ""
+
+
+def test_route_with_no_tokens_is_a_no_op(lib):
+    assert _route(lib, logits=None, idx=None, w=None, T=0) == 0
+
+
+def _dispatch(lib, idx=FAKE, T=4, E=8, k=2, x=None, H=0, counts=FAKE, offsets=FAKE, row_src=FAKE,
+              inv=FAKE, xd=None, ws=P(0x200000), ws_bytes=1 << 20, dtype=2):
+    return lib.moe_dispatch(idx, T, E, k, x, dtype, H, counts, offsets, row_src, inv, xd, ws,
+                            ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(idx=None), 1), (dict(counts=None), 1), (dict(inv=None), 1), (dict(row_src=None), 1),
+    (dict(xd=FAKE), 1),                                   # x_dispatched without x
+    (dict(xd=FAKE, x=FAKE, H=16, dtype=5), 3),
+    (dict(xd=FAKE, x=FAKE, H=0), 2),
+    (dict(k=0), 4), (dict(k=9), 4), (dict(E=0, k=1), 2),
+    (dict(ws=None), 6), (dict(ws_bytes=0), 6),
+    (dict(ws=P(0x200010)), 5),                           # workspace not 256-byte aligned
+])
+def test_dispatch_rejects_bad_arguments(lib, kwargs, status):
+    assert _dispatch(lib, **kwargs) == status
+
+
+def test_dispatch_workspace_size(lib):
+    assert lib.moe_dispatch_workspace_size(4096, 128, 8) >= 16 * 128 * 4
+    assert lib.moe_dispatch_workspace_size(-1, 8, 2) == 0
+    assert lib.moe_dispatch_workspace_size(0, 8, 2) % 256 == 0
+
+
+def _create(lib, gate=FAKE, up=FAKE, down=FAKE, dtype=2, E=8, H=64, I=128, out=True):
+    h = ctypes.c_void_p()
+    return lib.moe_experts_create(gate, up, down, dtype, E, H, I, ctypes.byref(h) if out else None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(gate=None), 1), (dict(up=None), 1), (dict(down=None), 1), (dict(out=False), 1),
+    (dict(dtype=3), 3), (dict(E=0), 2), (dict(E=2000), 2), (dict(H=0), 2), (dict(I=-4), 2),
+    (dict(H=20), 5), (dict(I=100), 5),             # 16-bit rows must be 16-byte multiples
+    (dict(gate=P(0x100008)), 5),                       # misaligned weights
+])
+def test_experts_create_rejects_bad_arguments(lib, kwargs, status):
+    assert _create(lib, **kwargs) == status
+
+
+def test_null_handles_are_rejected(lib):
+    assert lib.moe_forward(None, FAKE, FAKE, 2, 4, 2, 1, FAKE, None, None, FAKE, 1 << 20, None) == 1
+    assert lib.moe_experts_forward_dispatched(None, FAKE, FAKE, 4, FAKE, FAKE, 1 << 20, None) == 1
+    assert lib.moe_forward_workspace_size(None, 4, 2) == 0
+    assert lib.moe_experts_forward_dispatched_workspace_size(None, 4) == 0
+    lib.moe_experts_destroy(None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(y=None), 1), (dict(dtype=9), 3), (dict(wdt=9), 3), (dict(k=0), 4), (dict(H=0), 2),
+])
+def test_combine_rejects_bad_arguments(lib, kwargs, status):
+    a = dict(y=FAKE, dtype=2, inv=FAKE, w=FAKE, wdt=2, T=4, k=2, H=64, out=FAKE)
+    a.update(kwargs)
+    assert lib.moe_combine(a["y"], a["dtype"], a["inv"], a["w"], a["wdt"], a["T"], a["k"], a["H"],
+                           a["out"], None) == status
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.moe_selftest_bounded_wait(0, None) == 2
+    assert lib.moe_selftest_bounded_wait(10_000_001, None) == 2
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        moe.load_library(tmp_path / "missing.so")

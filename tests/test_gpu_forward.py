@@ -1,0 +1,122 @@
+"""The whole chain on the GPU (moe_forward) against the oracle: full oracle on
+the reduced workloads, sampled tokens on the full-size workloads (the launch
+configuration the benchmark times), plus split-API equality, determinism and
+degenerate sizes."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import moe_oracle
+from tests.parity import assert_output_close, assert_route_matches, f64, u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _device_inputs(inp):
+    return {k: v.to(DEV) for k, v in inp.items()}
+
+
+def _forward(moe, cfg, d, ex=None):
+    ex = ex or moe.Experts(d["gate"], d["up"], d["down"])
+    idx = torch.empty(cfg.T, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(cfg.T, cfg.top_k, dtype=d["logits"].dtype, device=DEV)
+    out = moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, cfg.renormalize, indices=idx, weights=w)
+    torch.cuda.synchronize()
+    return out, idx, w, ex
+
+
+@pytest.mark.parametrize("name", sorted(workloads.SMALL_CONFIGS))
+def test_forward_full_oracle(cuda_lib, name):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    inp = workloads.generate(cfg)
+    out, idx, w, _ = _forward(moe, cfg, _device_inputs(inp))
+    ref = moe_oracle.forward(inp["x"], inp["logits"], inp["gate"], inp["up"], inp["down"], cfg.top_k,
+                             cfg.renormalize)
+    assert np.array_equal(u32(idx), ref.route.indices)
+    assert_output_close(f64(out), ref.out, cfg.torch_dtype)
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("cfg_id,n_sample", [(2, 192), (3, 48), (4, 16), (5, 192)])
+def test_forward_full_size_sampled(cuda_lib, cfg_id, n_sample):
+    """Full-size workloads in the benchmark's launch configuration: routing
+    and dispatch compared in full, outputs on sampled tokens (first, last and
+    a seeded sample)."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[cfg_id]
+    inp = workloads.generate(cfg)
+    d = _device_inputs(inp)
+    out, idx, w, ex = _forward(moe, cfg, d)
+    rt = moe_oracle.route(inp["logits"], cfg.top_k, cfg.renormalize)
+    assert np.array_equal(u32(idx), rt.indices)
+    _, _, w32 = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize, weights_fp32=True)
+    assert_route_matches(idx, w, w32, rt, cfg.torch_dtype)
+    rng = np.random.default_rng(cfg_id)
+    toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, size=min(n_sample, cfg.T), replace=False)]))
+    ref = moe_oracle.forward_tokens(inp["x"], inp["logits"], inp["gate"], inp["up"], inp["down"], cfg.top_k,
+                                    cfg.renormalize, toks)
+    got = f64(out)[toks]
+    assert_output_close(got, ref, cfg.torch_dtype, f"out[sampled {len(toks)} tokens]")
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["f32_contract", "bf16_fine", "f16_zipf", "bf16_ragged"])
+def test_forward_equals_split_api(cuda_lib, name):
+    """moe_forward is bit-identical to route -> dispatch -> forward_dispatched -> combine."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    d = _device_inputs(workloads.generate(cfg))
+    out, idx, w, ex = _forward(moe, cfg, d)
+    idx2, w2 = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx2, cfg.E, d["x"])
+    y = moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets)
+    out2 = moe.moe_combine(y, disp.inv, w2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+    assert torch.equal(w.view(torch.uint8), w2.view(torch.uint8))  # bitwise, NaN rows included
+    assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8))
+
+
+@pytest.mark.parametrize("name", ["bf16_fine", "f16_zipf"])
+def test_forward_deterministic(cuda_lib, name):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    d = _device_inputs(workloads.generate(cfg))
+    a, _, _, ex = _forward(moe, cfg, d)
+    b, _, _, _ = _forward(moe, cfg, d, ex)
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("T", [0, 1, 3])
+def test_forward_tiny_token_counts(cuda_lib, T):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_fine"].scaled("tiny", T=max(T, 1), seed=99)
+    inp = workloads.generate(cfg)
+    inp["x"], inp["logits"] = inp["x"][:T], inp["logits"][:T]
+    d = _device_inputs(inp)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    out = moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, cfg.renormalize)
+    torch.cuda.synchronize()
+    assert out.shape == (T, cfg.H)
+    if T:
+        ref = moe_oracle.forward(inp["x"], inp["logits"], inp["gate"], inp["up"], inp["down"], cfg.top_k,
+                                 cfg.renormalize)
+        assert_output_close(f64(out), ref.out, cfg.torch_dtype)
+
+
+def test_forward_workspace_too_small_is_rejected(cuda_lib):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_ragged"]
+    d = _device_inputs(workloads.generate(cfg))
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    need = moe.moe_forward_workspace_size(ex, cfg.T, cfg.top_k)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, True, workspace=ws)
+    assert err.value.status == 6
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_forward(ex, d["x"], d["logits"], cfg.E + 1, True)
+    assert err.value.status == 4

@@ -91,6 +91,8 @@ SMALL_CONFIGS = {
                                   E=16, top_k=3, seed=2005),
     "f32_ragged": CONFIGS[1].scaled("f32_ragged_T333_H200_I136_E7_k3", T=333, H=200, I=136, E=7,
                                     top_k=3, logits_kind="normal", seed=2006),
+    "bf16_ragged": CONFIGS[2].scaled("bf16_ragged_T77_H136_I200_E5_k2", T=77, H=136, I=200, E=5,
+                                     top_k=2, seed=2007),
 }
 
 

@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the local MoE forward chain (route -> dispatch -> SwiGLU experts
+-> combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole chain over one batch of the BF16
+fine-grained prefill workload (T=4096, H=2048, I=768, E=128, top_k=8,
+renormalize), inputs resident in HBM. Each timed step is bracketed by CUDA
+events on the launching stream, with events between the stages, and L2 is
+flushed (256 MiB write) between steps outside the events. Under torchrun each
+rank runs its own batch (weak scaling, replicated experts, no collective on
+the data path); the time is the maximum over ranks.
+
+Printed (rank 0, one JSON line): tokens/s, grouped-GEMM TFLOP/s against the
+measured BF16 peak, route+dispatch microseconds, the decode workload's HBM
+GB/s over the touched expert weights, the roofline of the dominant kernel,
+the end-to-end number through moe_forward with host buffers, the CPU oracle
+baseline, kernel launches and the SM clocks seen during the run.
+
+--impl reference times the CPU oracle (the only reference this path has) on
+bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE fwd tokens/s + grouped-GEMM TFLOP/s vs bf16 peak; decode HBM GB/s"
+PREFILL = workloads.CONFIGS[2]
+DECODE = workloads.CONFIGS[4]
+FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 8  # route, dispatch count/scan/scatter/gather, gate/up GEMM, down GEMM, combine
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(cfg, n_gpus):
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
+            "renormalize": cfg.renormalize, "tokens_per_gpu": cfg.T,
+            "global_batch_tokens": cfg.T * n_gpus,
+            "parallelism": f"dp{n_gpus} (tokens split across GPUs, experts replicated)",
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = Path(os.environ.get("TMPDIR", "/tmp")) / f"moe_bench_clocks_{os.getpid()}.csv"
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            sel = ["-i", bus]
+        except Exception:
+            sel = []
+        cmd = ["nvidia-smi", *sel, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in self.path.read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                rows.append(parts)
+        self.path.unlink(missing_ok=True)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 200.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Chain:
+    """Pre-allocated buffers and the raw C-ABI calls of one forward step."""
+
+    def __init__(self, moe, cfg, dev):
+        self.moe, self.lib, self.cfg, self.dev = moe, moe.load_library(), cfg, dev
+        inp = workloads.generate(cfg)
+        self.host = inp
+        d = {k: v.to(dev) for k, v in inp.items()}
+        self.d = d
+        self.ex = moe.Experts(d["gate"], d["up"], d["down"])
+        T, k, E, H, I = cfg.T, cfg.top_k, cfg.E, cfg.H, cfg.I
+        n = T * k
+        e = dict(device=dev)
+        self.idx = torch.empty(T, k, dtype=torch.int32, **e)
+        self.w = torch.empty(T, k, dtype=cfg.torch_dtype, **e)
+        self.counts = torch.empty(E, dtype=torch.int32, **e)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, **e)
+        self.row_src = torch.empty(n, dtype=torch.int32, **e)
+        self.inv = torch.empty(n, dtype=torch.int32, **e)
+        self.xd = torch.empty(n, H, dtype=cfg.torch_dtype, **e)
+        self.h = torch.empty(n, I, dtype=cfg.torch_dtype, **e)
+        self.yd = torch.empty(n, H, dtype=cfg.torch_dtype, **e)
+        self.out = torch.empty(T, H, dtype=cfg.torch_dtype, **e)
+        self.dws = torch.empty(max(1, self.lib.moe_dispatch_workspace_size(T, E, k)), dtype=torch.uint8, **e)
+        self.fws = torch.empty(max(1, self.lib.moe_forward_workspace_size(self.ex.handle, T, k)),
+                               dtype=torch.uint8, **e)
+        self.dt = moe._dt(d["x"])
+
+    def step(self, stream, ev=None):
+        """route | dispatch | gate/up GEMM | down GEMM | combine, events between."""
+        c, lib, P = self.cfg, self.lib, self.moe._ptr
+        s = ctypes.c_void_p(stream.cuda_stream)
+        T, k, E, H = c.T, c.top_k, c.E, c.H
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rc = 0
+        rec(0)
+        rc |= lib.moe_route(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx), P(self.w),
+                            None, s)
+        rec(1)
+        rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts), P(self.offsets),
+                               P(self.row_src), P(self.inv), P(self.xd), P(self.dws), self.dws.numel(), s)
+        rec(2)
+        rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h), s)
+        rec(3)
+        rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), s)
+        rec(4)
+        rc |= lib.moe_combine(P(self.yd), self.dt, P(self.inv), P(self.w), self.dt, T, k, H, P(self.out), s)
+        rec(5)
+        if rc:
+            raise RuntimeError("a C-ABI call failed: " + lib.moe_last_error().decode())
+
+    def touched_experts(self) -> int:
+        return int((self.counts.cpu() > 0).sum())
+
+
+def timed_steps(chain, stream, flush, steps, warmup):
+    """Run warmup + timed steps; return per-stage mean seconds and the total."""
+    for _ in range(warmup):
+        flush.zero_()
+        chain.step(stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        chain.step(stream, evs[i])
+    torch.cuda.synchronize()
+    stages = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(steps)]) / 1e3
+    total = float(sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(steps))) / 1e3
+    return stages.mean(axis=0), total
+
+
+def e2e_steps(chain, stream, flush, steps):
+    """moe_forward through the public API with pinned host x/logits in and the
+    output back to pinned host memory, copies inside the timed region."""
+    moe, c = chain.moe, chain.cfg
+    hx, hl = chain.host["x"].pin_memory(), chain.host["logits"].pin_memory()
+    hout = torch.empty(c.T, c.H, dtype=c.torch_dtype).pin_memory()
+    dx, dl = torch.empty_like(chain.d["x"]), torch.empty_like(chain.d["logits"])
+    ms = []
+    for i in range(steps + 2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dx.copy_(hx, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        moe.moe_forward(chain.ex, dx, dl, c.top_k, c.renormalize, out=chain.out, workspace=chain.fws)
+        hout.copy_(chain.out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            ms.append(a.elapsed_time(b))
+    h2d = hx.numel() * hx.element_size() + hl.numel() * hl.element_size()
+    d2h = hout.numel() * hout.element_size()
+    return float(np.mean(ms)) / 1e3, h2d, d2h
+
+
+def traffic_record(kernel_source: Path):
+    """ncu DRAM bytes per launch of the dominant kernel, if they were taken on
+    the current kernel source (else None)."""
+    p = ROOT / "profiles" / "ncu_traffic.json"
+    if not p.exists():
+        return None
+    rec = json.loads(p.read_text())
+    sha = hashlib.sha256(kernel_source.read_bytes()).hexdigest()
+    return rec if rec.get("source_sha256") == sha else None
+
+
+def cpu_baseline_prefill(inp, n_tokens=256):
+    """The oracle, as it stands, on the first n_tokens of the prefill batch."""
+    from oracle import moe_oracle
+
+    c = PREFILL
+    t0 = time.perf_counter()
+    moe_oracle.forward(inp["x"][:n_tokens], inp["logits"][:n_tokens], inp["gate"], inp["up"], inp["down"],
+                       c.top_k, c.renormalize)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"first {n_tokens} of {c.T} tokens of {c.name}: FP32 routing, dispatch, f64 SwiGLU "
+                      f"experts and combine ({dt:.1f} s)"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import moe_routing_swiglu_gb300 as moe
+    from moe_routing_swiglu_gb300 import _build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if local_rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    moe.load_library()
+    peaks, peaks_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    chain = Chain(moe, PREFILL, dev)
+    decode = Chain(moe, DECODE, dev)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stages, total = timed_steps(chain, stream, flush, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total = max_over_ranks(total, world, dev)
+    e2e_s, h2d, d2h = e2e_steps(chain, stream, flush, min(args.steps, 20))
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    dec_stages, dec_total = timed_steps(decode, stream, flush, min(args.steps, 50), args.warmup)
+    clk = clocks.stop()
+    assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
+
+    c = PREFILL
+    ms_per_step = total / args.steps * 1e3
+    tokens_per_s = world * c.T * args.steps / total
+    t_route, t_disp, t_gu, t_down, t_comb = [float(x) for x in stages]
+    es = 2
+    gemm_flops = c.expert_flops
+    gemm_tflops = gemm_flops / (t_gu + t_down) / 1e12
+    touched = chain.touched_experts()
+    # K3 (gate/up GEMM): algorithmic work per launch
+    k3_flops = 4 * c.T * c.top_k * c.H * c.I
+    k3_bytes = touched * 2 * c.I * c.H * es + c.T * c.H * es + c.T * c.top_k * c.I * es
+    k3_tflops = k3_flops / t_gu / 1e12
+    k3_gbs = k3_bytes / t_gu / 1e9
+    t_floor_tensor = k3_flops / (peaks["bf16_tflops"] * 1e12)
+    t_floor_hbm = k3_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "hbm" if t_floor_hbm >= t_floor_tensor else "tensor"
+    traffic = traffic_record(ROOT / "moe_routing_swiglu_gb300" / "csrc" / "experts_tc.cu")
+    roof = {"kernel": "experts_tc_kernel<bf16, gate/up + SwiGLU> (K3)", "bound": bound,
+            "achieved": round(k3_gbs if bound == "hbm" else k3_tflops, 2),
+            "peak": peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": round((k3_gbs / peaks["hbm_gbs"]) if bound == "hbm" else (k3_tflops / peaks["bf16_tflops"]), 4),
+            "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+            "algorithmic_bytes": k3_bytes, "algorithmic_flops": k3_flops, "us": round(t_gu * 1e6, 2),
+            "tensor_frac": round(k3_tflops / peaks["bf16_tflops"], 4),
+            "hbm_frac": round(k3_gbs / peaks["hbm_gbs"], 4), "peak_source": peaks_src}
+
+    d = DECODE
+    dec_touched = decode.touched_experts()
+    dec_bytes = dec_touched * 3 * d.I * d.H * es
+    dec_fwd = float(dec_total) / min(args.steps, 50)
+    dec_exp = float(dec_stages[2] + dec_stages[3])
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) logits and x, N(0, 1/sqrt(fan_in)) expert weights (random init)",
+        "config": workload_config(c, world),
+        "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
+                         "frac_bf16_sustained": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
+                         "flops_per_step": gemm_flops, "gate_up_us": round(t_gu * 1e6, 2),
+                         "down_us": round(t_down * 1e6, 2)},
+        "route_dispatch_us": {"route": round(t_route * 1e6, 2), "dispatch": round(t_disp * 1e6, 2),
+                              "total": round((t_route + t_disp) * 1e6, 2)},
+        "combine_us": round(t_comb * 1e6, 2),
+        "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
+                   "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dec_touched,
+                   "touched_weight_bytes": dec_bytes,
+                   "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),
+                   "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
+                   "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
+        "roofline": roof,
+        "e2e": {"value": round(world * c.T / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "api": "moe_forward"},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if world > 1:
+        dist.barrier()
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline_prefill(chain.host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The CPU oracle on bounded samples of the prefill batch (rank 0 only)."""
+    if rank != 0:
+        return
+    from oracle import moe_oracle
+
+    c = PREFILL
+    n_tok = 16
+    inp = workloads.generate(c)
+    times = []
+    for i in range(args.warmup + args.steps):
+        lo = (i * n_tok) % c.T
+        t0 = time.perf_counter()
+        moe_oracle.forward(inp["x"][lo:lo + n_tok], inp["logits"][lo:lo + n_tok], inp["gate"], inp["up"],
+                           inp["down"], c.top_k, c.renormalize)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n_tok * args.steps / total
+    cores = len(os.sched_getaffinity(0))
+    sample = f"{n_tok} consecutive tokens of {c.name} per step through the whole oracle chain"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) logits and x, N(0, 1/sqrt(fan_in)) expert weights (random init)",
+        "config": workload_config(c, world),
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

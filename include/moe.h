@@ -167,6 +167,22 @@ moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void
                                           size_t workspace_bytes, void* stream);
 
 /*
+ * moe_experts_gate_up / moe_experts_down - the two grouped-GEMM stages of
+ * moe_experts_forward_dispatched, for callers that want h or want to time or
+ * schedule the stages apart. Same arguments and checks as above; no
+ * workspace.
+ *
+ *   gate_up:  x_dispatched [rows, H] -> h [rows, I],
+ *             h = SiLU(W_gate[e] x) * (W_up[e] x), FP32 accumulation, rounded
+ *             to the experts' dtype.
+ *   down:     h [rows, I] -> y_dispatched [rows, H], y = W_down[e] h.
+ */
+moe_status moe_experts_gate_up(const moe_experts* experts, const void* x_dispatched,
+                               const uint32_t* offsets, int64_t rows, void* h, void* stream);
+moe_status moe_experts_down(const moe_experts* experts, const void* h, const uint32_t* offsets,
+                            int64_t rows, void* y_dispatched, void* stream);
+
+/*
  * moe_combine - restore token order and take the routing-weighted sum
  * (DispatchedTokens::combine; ruDNN user guide section 6: combine uses the
  * dispatch mapping to restore token order and merges the expert outputs with

@@ -102,22 +102,40 @@ moe_status check_current_device(const moe_experts* ex) {
   return MOE_OK;
 }
 
-moe_status run_experts(const moe_experts* ex, const void* xd, const uint32_t* offsets, int64_t rows,
-                       void* h, void* y, cudaStream_t s) {
+// One expert GEMM stage: gate_up (x_dispatched -> h) or down (h -> y).
+moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const uint32_t* offsets,
+                     int64_t rows, void* out, cudaStream_t s) {
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32) {
-    err = moe::launch_experts_simt_f32(static_cast<const float*>(xd), offsets, static_cast<int>(ex->E),
-                                       rows, static_cast<const float*>(ex->gate),
-                                       static_cast<const float*>(ex->up),
-                                       static_cast<const float*>(ex->down), ex->H, ex->I,
-                                       static_cast<float*>(h), static_cast<float*>(y), s);
+    err = moe::launch_experts_simt_f32(gate_up, static_cast<const float*>(a), offsets,
+                                       static_cast<int>(ex->E), rows,
+                                       static_cast<const float*>(gate_up ? ex->gate : ex->down),
+                                       static_cast<const float*>(gate_up ? ex->up : nullptr), ex->H,
+                                       ex->I, static_cast<float*>(out), s);
   } else {
-    err = moe::launch_experts_tc(ex->tc, ex->dtype, xd, offsets, static_cast<int>(ex->E), rows,
-                                 ex->H, ex->I, h, y, ex->num_sms, s, &why);
+    err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, offsets, static_cast<int>(ex->E), rows,
+                                 ex->H, ex->I, out, ex->num_sms, s, &why);
   }
-  if (err != cudaSuccess) return cuda_fail(err, "expert GEMM launch", why);
+  if (err != cudaSuccess) return cuda_fail(err, gate_up ? "gate/up GEMM launch" : "down GEMM launch", why);
   return MOE_OK;
+}
+
+moe_status run_experts(const moe_experts* ex, const void* xd, const uint32_t* offsets, int64_t rows,
+                       void* h, void* y, cudaStream_t s) {
+  moe_status st = run_stage(ex, true, xd, offsets, rows, h, s);
+  if (st != MOE_OK) return st;
+  return run_stage(ex, false, h, offsets, rows, y, s);
+}
+
+moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t* offsets, int64_t rows,
+                            const void* out) {
+  if (ex == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "experts and offsets must be non-NULL");
+  if (rows < 0 || rows >= int64_t{0xFFFFFFFF}) return fail(MOE_ERR_SHAPE, "rows must be in 0 .. 2^32-2");
+  if (rows > 0 && (a == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "input and output must be non-NULL");
+  if (ex->dtype != MOE_F32 && (!aligned16(a) || !aligned16(out)))
+    return fail(MOE_ERR_ALIGNMENT, "input and output must be 16-byte aligned");
+  return check_current_device(ex);
 }
 
 }  // namespace
@@ -257,6 +275,24 @@ moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_d
                    static_cast<cudaStream_t>(stream));
   if (st != MOE_OK) return st;
   return ok();
+}
+
+moe_status moe_experts_gate_up(const moe_experts* ex, const void* x_dispatched,
+                               const uint32_t* offsets, int64_t rows, void* h, void* stream) {
+  moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, h);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return ok();
+  st = run_stage(ex, true, x_dispatched, offsets, rows, h, static_cast<cudaStream_t>(stream));
+  return st != MOE_OK ? st : ok();
+}
+
+moe_status moe_experts_down(const moe_experts* ex, const void* h, const uint32_t* offsets, int64_t rows,
+                            void* y_dispatched, void* stream) {
+  moe_status st = check_stage_args(ex, h, offsets, rows, y_dispatched);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return ok();
+  st = run_stage(ex, false, h, offsets, rows, y_dispatched, static_cast<cudaStream_t>(stream));
+  return st != MOE_OK ? st : ok();
 }
 
 moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,

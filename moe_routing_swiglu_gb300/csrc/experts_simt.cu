@@ -101,17 +101,19 @@ int64_t tile_bound(int64_t rows, int E, int bm, int64_t n_tiles) {
 
 }  // namespace
 
-cudaError_t launch_experts_simt_f32(const float* x_dispatched, const uint32_t* offsets, int E,
-                                    int64_t rows, const float* gate, const float* up,
-                                    const float* down, int64_t H, int64_t I, float* h, float* y,
-                                    cudaStream_t stream) {
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const uint32_t* offsets, int E,
+                                    int64_t rows, const float* w0, const float* w1, int64_t H,
+                                    int64_t I, float* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const int64_t g1 = tile_bound(rows, E, SB_M, (I + SB_N - 1) / SB_N);
-  experts_simt_kernel<true><<<static_cast<unsigned>(g1), SB_THREADS, 0, stream>>>(
-      x_dispatched, offsets, E, gate, up, H, I, rows, h);
-  const int64_t g2 = tile_bound(rows, E, SB_M, (H + SB_N - 1) / SB_N);
-  experts_simt_kernel<false><<<static_cast<unsigned>(g2), SB_THREADS, 0, stream>>>(
-      h, offsets, E, down, nullptr, I, H, rows, y);
+  if (gate_up) {
+    const int64_t g = tile_bound(rows, E, SB_M, (I + SB_N - 1) / SB_N);
+    experts_simt_kernel<true><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
+        a, offsets, E, w0, w1, H, I, rows, out);
+  } else {
+    const int64_t g = tile_bound(rows, E, SB_M, (H + SB_N - 1) / SB_N);
+    experts_simt_kernel<false><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
+        a, offsets, E, w0, nullptr, I, H, rows, out);
+  }
   return cudaGetLastError();
 }
 

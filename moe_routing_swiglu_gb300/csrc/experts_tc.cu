@@ -384,27 +384,24 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 }
 
 template <typename T>
-cudaError_t launch_pair(const TcWeights& w, moe_dtype dtype, const void* xd,
-                        const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                        void* h, void* y, int num_sms, cudaStream_t stream, const char** why) {
+cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
+                         const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
+                         void* out, int num_sms, cudaStream_t stream, const char** why) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
   if (err != cudaSuccess) return err;
-  CUtensorMap ta, th;
-  if (!encode_2d(&ta, dtype, xd, static_cast<uint64_t>(H), static_cast<uint64_t>(rows)) ||
-      !encode_2d(&th, dtype, h, static_cast<uint64_t>(I), static_cast<uint64_t>(rows))) {
+  const int64_t K = gate_up ? H : I;
+  const int64_t n_out = gate_up ? I : H;
+  CUtensorMap ta;
+  if (!encode_2d(&ta, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows))) {
     *why = "cuTensorMapEncodeTiled rejected the activation tensor map";
     return cudaErrorInvalidValue;
   }
-  const int nt1 = static_cast<int>((I + BN / 2 - 1) / (BN / 2));
-  const int nt2 = static_cast<int>((H + BN - 1) / BN);
-  TcArgs a1{offsets, h, E, nt1, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
-            static_cast<uint32_t>(rows), static_cast<uint32_t>(tile_bound(rows, E, nt1)), status};
-  err = launch_one<T, true>(ta, w.gate, w.up, a1, rows, num_sms, stream);
-  if (err != cudaSuccess) return err;
-  TcArgs a2{offsets, y, E, nt2, static_cast<int>((I + BK - 1) / BK), static_cast<int>(H),
-            static_cast<uint32_t>(rows), static_cast<uint32_t>(tile_bound(rows, E, nt2)), status};
-  return launch_one<T, false>(th, w.down, w.down, a2, rows, num_sms, stream);
+  const int nt = static_cast<int>(gate_up ? (I + BN / 2 - 1) / (BN / 2) : (H + BN - 1) / BN);
+  TcArgs args{offsets, out, E, nt, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
+              static_cast<uint32_t>(rows), static_cast<uint32_t>(tile_bound(rows, E, nt)), status};
+  if (gate_up) return launch_one<T, true>(ta, w.gate, w.up, args, rows, num_sms, stream);
+  return launch_one<T, false>(ta, w.down, w.down, args, rows, num_sms, stream);
 }
 
 }  // namespace
@@ -423,13 +420,13 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
   return true;
 }
 
-cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, const void* x_dispatched,
+cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* h, void* y, int num_sms, cudaStream_t stream, const char** why) {
+                              void* out, int num_sms, cudaStream_t stream, const char** why) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
-    return launch_pair<__nv_bfloat16>(w, dtype, x_dispatched, offsets, E, rows, H, I, h, y, num_sms, stream, why);
-  return launch_pair<__half>(w, dtype, x_dispatched, offsets, E, rows, H, I, h, y, num_sms, stream, why);
+    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, num_sms, stream, why);
+  return launch_stage<__half>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, num_sms, stream, why);
 }
 
 cudaError_t read_device_status(uint32_t* code, bool clear) {

@@ -31,11 +31,11 @@ cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint
                            const void* weights, moe_dtype weights_dtype, int64_t T, int top_k,
                            int64_t H, void* out, cudaStream_t stream);
 
-// ---- K7 FP32 experts on CUDA cores (experts_simt.cu)
-cudaError_t launch_experts_simt_f32(const float* x_dispatched, const uint32_t* offsets, int E,
-                                    int64_t rows, const float* gate, const float* up,
-                                    const float* down, int64_t H, int64_t I, float* h, float* y,
-                                    cudaStream_t stream);
+// ---- K7 FP32 experts on CUDA cores (experts_simt.cu). gate_up: a = x_dispatched
+// [rows, H], w0/w1 = gate/up, out = h [rows, I]; else a = h, w0 = down, out = y [rows, H].
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const uint32_t* offsets, int E,
+                                    int64_t rows, const float* w0, const float* w1, int64_t H,
+                                    int64_t I, float* out, cudaStream_t stream);
 
 // ---- K3/K4 F16/BF16 experts on tcgen05 tensor cores (experts_tc.cu)
 struct TcWeights {
@@ -43,9 +43,10 @@ struct TcWeights {
 };
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,
                        int64_t E, int64_t H, int64_t I, TcWeights* out, const char** why);
-cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, const void* x_dispatched,
+// gate_up: K3, a = x_dispatched [rows, H] -> out = h [rows, I]; else K4, a = h -> out = y [rows, H].
+cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* h, void* y, int num_sms, cudaStream_t stream, const char** why);
+                              void* out, int num_sms, cudaStream_t stream, const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 

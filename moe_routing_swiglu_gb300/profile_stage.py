@@ -1,0 +1,66 @@
+"""Run one stage of the MoE chain a few times on one workload, for profilers.
+
+    python -m moe_routing_swiglu_gb300.profile_stage --workload cfg2 --stage gate_up --reps 3
+
+The inputs are the seeded synthetic workloads of ``workloads.py``; routing and
+dispatch run once to set up the stage's inputs, then the chosen stage runs
+``--reps`` times back to back (stream-ordered) and the device is synchronised.
+Stages: route, dispatch, gate_up, down, combine, forward (moe_forward).
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parents[1]
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+import moe_routing_swiglu_gb300 as moe  # noqa: E402
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    names = {f"cfg{i}": c for i, c in workloads.CONFIGS.items()}
+    names.update(workloads.SMALL_CONFIGS)
+    ap.add_argument("--workload", default="cfg2", choices=sorted(names))
+    ap.add_argument("--stage", default="gate_up",
+                    choices=["route", "dispatch", "gate_up", "down", "combine", "forward"])
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args(argv)
+    cfg = names[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    moe.load_library()
+    d = {k: v.to(dev) for k, v in workloads.generate(cfg).items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, w = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    h = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    y = moe.moe_experts_down(ex, h, disp.offsets)
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        if args.stage == "route":
+            moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize, indices=idx, weights=w)
+        elif args.stage == "dispatch":
+            moe.moe_dispatch(idx, cfg.E, d["x"])
+        elif args.stage == "gate_up":
+            moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h)
+        elif args.stage == "down":
+            moe.moe_experts_down(ex, h, disp.offsets, out=y)
+        elif args.stage == "combine":
+            moe.moe_combine(y, disp.inv, w)
+        else:
+            moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, cfg.renormalize)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    print(f"{args.stage} x{args.reps} on {cfg.name}: ok")
+
+
+if __name__ == "__main__":
+    main()

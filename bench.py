@@ -252,8 +252,9 @@ def traffic_record(kernel_source: Path):
     return rec if rec.get("source_sha256") == sha else None
 
 
-def cpu_baseline_prefill(inp, n_tokens=256):
-    """The oracle, as it stands, on the first n_tokens of the prefill batch."""
+def cpu_baseline_prefill(inp, n_tokens=PREFILL.T):
+    """The oracle, as it stands, on the first n_tokens of the prefill batch
+    (by default the whole batch: a few seconds of CPU work on the host)."""
     from oracle import moe_oracle
 
     c = PREFILL
@@ -263,8 +264,8 @@ def cpu_baseline_prefill(inp, n_tokens=256):
     dt = time.perf_counter() - t0
     return {"value": n_tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": f"first {n_tokens} of {c.T} tokens of {c.name}: FP32 routing, dispatch, f64 SwiGLU "
-                      f"experts and combine ({dt:.1f} s)"}
+            "sample": f"{n_tokens} of {c.T} tokens of {c.name} (one batch): FP32 routing, dispatch, "
+                      f"f64 SwiGLU experts and combine, {dt:.1f} s"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -410,8 +411,8 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -123,6 +123,33 @@ moe_status moe_dispatch(const uint32_t* indices, int64_t T, int64_t E, int32_t t
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * moe_dispatch_noalloc - moe_dispatch without a workspace argument, for
+ * callers that cannot allocate device memory when they dispatch: a plugin
+ * that reaches the library through this C ABI from a host framework owning
+ * every device allocation, or a serving loop whose memory budget is fixed at
+ * start-up and may not grow afterwards. The pages have no counterpart; the
+ * outputs are the same as moe_dispatch's, bit for bit.
+ *
+ * Arguments and outputs are those of moe_dispatch. The scratch instead lives
+ * in a fixed 1 MiB (MOE_DISPATCH_NOALLOC_SCRATCH_BYTES) array inside the
+ * library's device image; every GPU that loads the library holds it until the
+ * process exits. Requests whose scratch, ceil(T*top_k/2048)*E*4 bytes, exceeds
+ * it are rejected with MOE_ERR_SHAPE before anything is launched. No call
+ * allocates or frees device memory. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls on a device share
+ * the array and it keeps the last call's contents (each call writes every
+ * entry it reads, so nothing needs clearing): calls that may overlap on the
+ * GPU, such as calls on different streams without ordering between them, race
+ * on it and must not be issued.
+ */
+#define MOE_DISPATCH_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_dispatch_noalloc(const uint32_t* indices, int64_t T, int64_t E, int32_t top_k,
+                                const void* x, moe_dtype dtype, int64_t H, uint32_t* counts,
+                                uint32_t* offsets, uint32_t* row_src, uint32_t* inv,
+                                void* x_dispatched, void* stream);
+
+/*
  * moe_experts_create - validate and wrap bias-free SwiGLU expert weights
  * (SwiGluExperts::new; ruDNN user guide section 5: gate and up [E, I, H],
  * down [E, H, I], one float dtype, one device).

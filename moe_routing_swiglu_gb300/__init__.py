@@ -36,6 +36,8 @@ SIGNATURES = {
     "moe_dispatch_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "moe_dispatch": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, ctypes.c_int, _I64, _P, _P, _P, _P, _P,
                                     _P, _SZ, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, ctypes.c_int, _I64, _P, _P, _P, _P, _P,
+                                            _P]),
     "moe_experts_create": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                           ctypes.POINTER(ctypes.c_void_p)]),
     "moe_experts_destroy": (None, [_P]),
@@ -161,6 +163,30 @@ def moe_dispatch(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None
     _check(lib.moe_dispatch(_ptr(indices), T, num_experts, k, _ptr(x), xdt, H, _ptr(counts),
                             _ptr(offsets), _ptr(row_src), _ptr(inv), _ptr(xd), _ptr(ws),
                             ws.numel(), _stream(stream)))
+    return DispatchedTokens(counts, offsets, row_src, inv, xd)
+
+
+def moe_dispatch_noalloc(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None = None,
+                         stream=None) -> DispatchedTokens:
+    """moe_dispatch with the library's fixed 1 MiB scratch instead of a
+    workspace, for callers that cannot allocate device memory when they
+    dispatch (the output tensors here are still allocated by torch)."""
+    lib = load_library()
+    _dev_tensor(indices, "indices")
+    T, k = indices.shape
+    dev = indices.device
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    row_src = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    xd = None
+    H, xdt = 0, MOE_F32
+    if x is not None:
+        _dev_tensor(x, "x")
+        H, xdt = x.shape[1], _dt(x)
+        xd = torch.empty(T * k, H, dtype=x.dtype, device=dev)
+    _check(lib.moe_dispatch_noalloc(_ptr(indices), T, num_experts, k, _ptr(x), xdt, H, _ptr(counts),
+                                    _ptr(offsets), _ptr(row_src), _ptr(inv), _ptr(xd), _stream(stream)))
     return DispatchedTokens(counts, offsets, row_src, inv, xd)
 
 

@@ -205,6 +205,34 @@ moe_status moe_dispatch(const uint32_t* indices, int64_t T, int64_t E, int32_t t
   return ok();
 }
 
+moe_status moe_dispatch_noalloc(const uint32_t* indices, int64_t T, int64_t E, int32_t top_k,
+                                const void* x, moe_dtype dtype, int64_t H, uint32_t* counts,
+                                uint32_t* offsets, uint32_t* row_src, uint32_t* inv,
+                                void* x_dispatched, void* stream) {
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  if (top_k < 1 || top_k > E) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= E");
+  if (T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (counts == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "counts and offsets must be non-NULL");
+  if (T > 0 && (indices == nullptr || row_src == nullptr || inv == nullptr))
+    return fail(MOE_ERR_NULL, "indices, row_src and inv must be non-NULL");
+  if (x_dispatched != nullptr) {
+    if (x == nullptr) return fail(MOE_ERR_NULL, "x_dispatched needs x");
+    if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+    if (H < 1) return fail(MOE_ERR_SHAPE, "H must be >= 1");
+  }
+  const size_t need = moe::dispatch_scratch_bytes(T, E, top_k);
+  if (need > moe::NOALLOC_DISPATCH_SCRATCH_BYTES)
+    return fail(MOE_ERR_SHAPE, "moe_dispatch_noalloc: ceil(T*top_k/2048)*E*4 = " + std::to_string(need) +
+                                   " bytes exceeds its fixed 1 MiB scratch; use moe_dispatch with a workspace");
+  void* scratch = nullptr;
+  cudaError_t err = moe::noalloc_dispatch_scratch(&scratch);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch_noalloc scratch set-up");
+  err = moe::launch_dispatch(indices, T, static_cast<int>(E), top_k, x, dtype, H, counts, offsets, row_src,
+                             inv, x_dispatched, scratch, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch_noalloc launch");
+  return ok();
+}
+
 moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dtype,
                               int64_t E, int64_t H, int64_t I, moe_experts** out) {
   if (out == nullptr) return fail(MOE_ERR_NULL, "out must be non-NULL");

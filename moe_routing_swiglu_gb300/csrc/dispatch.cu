@@ -15,6 +15,8 @@
 //               histograms give each warp its first row per expert, and
 //               __match_any_sync ranks equal experts inside each 32-slot step.
 // An index >= E is never dispatched; its inv entry is INVALID_ROW.
+#include <mutex>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -163,7 +165,34 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const VecT* __rest
   }
 }
 
+// Fixed scratch of moe_dispatch_noalloc. Every GPU that loads this library
+// holds this array (1 MiB) in its device image until the process exits; all
+// calls on a device share it.
+static __device__ __align__(256) uint32_t g_noalloc_dispatch_scratch[NOALLOC_DISPATCH_SCRATCH_BYTES / 4];
+
 }  // namespace
+
+cudaError_t noalloc_dispatch_scratch(void** ptr) {
+  // In host code the array's name is only a stand-in for the device symbol;
+  // the device address comes from cudaGetSymbolAddress, looked up once per
+  // device with that device current and cached.
+  constexpr int kMaxDevices = 256;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_dispatch_scratch);
+    if (err != cudaSuccess) return err;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {
   const int64_t n = T * top_k;

@@ -21,6 +21,10 @@ cudaError_t launch_route(const void* logits, moe_dtype dtype, int64_t T, int E, 
 // ---- K2 dispatch (dispatch.cu)
 constexpr int DISPATCH_CHUNK = 2048;  // flat slots per counting/scatter block
 size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k);
+// Device address of the fixed scratch array used by moe_dispatch_noalloc on
+// the current device (set up on first use per device).
+constexpr size_t NOALLOC_DISPATCH_SCRATCH_BYTES = size_t{1} << 20;
+cudaError_t noalloc_dispatch_scratch(void** ptr);
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,

@@ -47,6 +47,7 @@ PREFILL = workloads.CONFIGS[2]
 DECODE = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 8  # route, dispatch count/scan/scatter/gather, gate/up GEMM, down GEMM, combine
+# (plus one 4-byte memset node before each GEMM that resets its tile counter)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -171,6 +172,7 @@ class Chain:
         self.dws = torch.empty(max(1, self.lib.moe_dispatch_workspace_size(T, E, k)), dtype=torch.uint8, **e)
         self.fws = torch.empty(max(1, self.lib.moe_forward_workspace_size(self.ex.handle, T, k)),
                                dtype=torch.uint8, **e)
+        self.sws = torch.empty(moe.STAGE_WORKSPACE_BYTES, dtype=torch.uint8, **e)
         self.dt = moe._dt(d["x"])
 
     def step(self, stream, ev=None):
@@ -187,9 +189,11 @@ class Chain:
         rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts), P(self.offsets),
                                P(self.row_src), P(self.inv), P(self.xd), P(self.dws), self.dws.numel(), s)
         rec(2)
-        rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h), s)
+        rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h), P(self.sws),
+                                      self.sws.numel(), s)
         rec(3)
-        rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), s)
+        rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), P(self.sws),
+                                   self.sws.numel(), s)
         rec(4)
         rc |= lib.moe_combine(P(self.yd), self.dt, P(self.inv), P(self.w), self.dt, T, k, H, P(self.out), s)
         rec(5)

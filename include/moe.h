@@ -185,7 +185,8 @@ void moe_experts_destroy(moe_experts* experts);
  *                 projection.
  *   workspace     device scratch of
  *                 moe_experts_forward_dispatched_workspace_size(experts, rows)
- *                 bytes (holds h).
+ *                 bytes (holds h and the GEMMs' tile counter), 256-byte
+ *                 aligned.
  */
 size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* experts, int64_t rows);
 moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void* x_dispatched,
@@ -196,18 +197,22 @@ moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void
 /*
  * moe_experts_gate_up / moe_experts_down - the two grouped-GEMM stages of
  * moe_experts_forward_dispatched, for callers that want h or want to time or
- * schedule the stages apart. Same arguments and checks as above; no
- * workspace.
+ * schedule the stages apart. Same arguments and checks as above.
  *
  *   gate_up:  x_dispatched [rows, H] -> h [rows, I],
  *             h = SiLU(W_gate[e] x) * (W_up[e] x), FP32 accumulation, rounded
  *             to the experts' dtype.
  *   down:     h [rows, I] -> y_dispatched [rows, H], y = W_down[e] h.
+ *   workspace at least 256 bytes, 256-byte aligned (the tensor-core kernels'
+ *             tile counter, reset on the stream by each call); two calls
+ *             that may run at the same time need separate workspaces.
  */
 moe_status moe_experts_gate_up(const moe_experts* experts, const void* x_dispatched,
-                               const uint32_t* offsets, int64_t rows, void* h, void* stream);
+                               const uint32_t* offsets, int64_t rows, void* h, void* workspace,
+                               size_t workspace_bytes, void* stream);
 moe_status moe_experts_down(const moe_experts* experts, const void* h, const uint32_t* offsets,
-                            int64_t rows, void* y_dispatched, void* stream);
+                            int64_t rows, void* y_dispatched, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /*
  * moe_combine - restore token order and take the routing-weighted sum
@@ -259,7 +264,8 @@ moe_status moe_forward(const moe_experts* experts, const void* x, const void* lo
  * and records a code here instead of hanging the GPU. Codes (first one
  * wins): 0x11 producer waiting for a free stage, 0x12 MMA waiting for a
  * loaded stage, 0x13 MMA waiting for a drained accumulator, 0x14 epilogue
- * waiting for a finished accumulator, 0x15 / 0x16 teardown drains, 0x100
+ * waiting for a finished accumulator, 0x15 / 0x16 teardown drains, 0x17 a
+ * wait on the shared-memory tile ring of the tile scheduler, 0x100
  * moe_selftest_bounded_wait. Synchronises the current device; *code = 0 when
  * no wait has timed out.
  */

@@ -43,8 +43,8 @@ SIGNATURES = {
     "moe_experts_destroy": (None, [_P]),
     "moe_experts_forward_dispatched_workspace_size": (_SZ, [_P, _I64]),
     "moe_experts_forward_dispatched": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
-    "moe_experts_gate_up": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P]),
-    "moe_experts_down": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P]),
+    "moe_experts_gate_up": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
+    "moe_experts_down": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
     "moe_combine": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _I64, _I32, _I64, _P, _P]),
     "moe_forward_workspace_size": (_SZ, [_P, _I64, _I32]),
     "moe_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -231,26 +231,33 @@ def moe_experts_forward_dispatched(experts: Experts, x_dispatched: torch.Tensor,
     return y
 
 
+STAGE_WORKSPACE_BYTES = 256
+
+
 def moe_experts_gate_up(experts: Experts, x_dispatched: torch.Tensor, offsets: torch.Tensor, out=None,
-                        stream=None):
+                        workspace=None, stream=None):
     """First GEMM stage: h [rows, I] = SiLU(x W_gate^T) * (x W_up^T) per expert."""
     lib = load_library()
     _dev_tensor(x_dispatched, "x_dispatched")
     rows = x_dispatched.shape[0]
     h = out if out is not None else torch.empty(rows, experts.I, dtype=experts.dtype,
                                                 device=x_dispatched.device)
+    ws = _workspace(STAGE_WORKSPACE_BYTES, x_dispatched.device, workspace)
     _check(lib.moe_experts_gate_up(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows, _ptr(h),
-                                   _stream(stream)))
+                                   _ptr(ws), ws.numel(), _stream(stream)))
     return h
 
 
-def moe_experts_down(experts: Experts, h: torch.Tensor, offsets: torch.Tensor, out=None, stream=None):
+def moe_experts_down(experts: Experts, h: torch.Tensor, offsets: torch.Tensor, out=None, workspace=None,
+                     stream=None):
     """Second GEMM stage: y [rows, H] = h W_down^T per expert."""
     lib = load_library()
     _dev_tensor(h, "h")
     rows = h.shape[0]
     y = out if out is not None else torch.empty(rows, experts.H, dtype=experts.dtype, device=h.device)
-    _check(lib.moe_experts_down(experts.handle, _ptr(h), _ptr(offsets), rows, _ptr(y), _stream(stream)))
+    ws = _workspace(STAGE_WORKSPACE_BYTES, h.device, workspace)
+    _check(lib.moe_experts_down(experts.handle, _ptr(h), _ptr(offsets), rows, _ptr(y), _ptr(ws), ws.numel(),
+                                _stream(stream)))
     return y
 
 

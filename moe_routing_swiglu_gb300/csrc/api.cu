@@ -66,7 +66,7 @@ moe_status check_route_args(const void* logits, int dtype, int64_t T, int64_t E,
 }
 
 struct ForwardLayout {
-  size_t indices, weights, counts, offsets, row_src, inv, scratch, xd, h, yd, total;
+  size_t indices, weights, counts, offsets, row_src, inv, scratch, sched, xd, h, yd, total;
 };
 
 ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
@@ -86,6 +86,7 @@ ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
   L.row_src = take(n * 4);
   L.inv = take(n * 4);
   L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
+  L.sched = take(moe::TC_SCHED_BYTES);
   L.xd = take(n * static_cast<size_t>(ex->H) * es);
   L.h = take(n * static_cast<size_t>(ex->I) * es);
   L.yd = take(n * static_cast<size_t>(ex->H) * es);
@@ -104,7 +105,7 @@ moe_status check_current_device(const moe_experts* ex) {
 
 // One expert GEMM stage: gate_up (x_dispatched -> h) or down (h -> y).
 moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const uint32_t* offsets,
-                     int64_t rows, void* out, cudaStream_t s) {
+                     int64_t rows, void* out, void* sched, cudaStream_t s) {
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32) {
@@ -115,22 +116,25 @@ moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const u
                                        ex->I, static_cast<float*>(out), s);
   } else {
     err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, offsets, static_cast<int>(ex->E), rows,
-                                 ex->H, ex->I, out, ex->num_sms, s, &why);
+                                 ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why);
   }
   if (err != cudaSuccess) return cuda_fail(err, gate_up ? "gate/up GEMM launch" : "down GEMM launch", why);
   return MOE_OK;
 }
 
 moe_status run_experts(const moe_experts* ex, const void* xd, const uint32_t* offsets, int64_t rows,
-                       void* h, void* y, cudaStream_t s) {
-  moe_status st = run_stage(ex, true, xd, offsets, rows, h, s);
+                       void* h, void* y, void* sched, cudaStream_t s) {
+  moe_status st = run_stage(ex, true, xd, offsets, rows, h, sched, s);
   if (st != MOE_OK) return st;
-  return run_stage(ex, false, h, offsets, rows, y, s);
+  return run_stage(ex, false, h, offsets, rows, y, sched, s);
 }
 
 moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t* offsets, int64_t rows,
-                            const void* out) {
+                            const void* out, const void* ws, size_t ws_bytes) {
   if (ex == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "experts and offsets must be non-NULL");
+  if (ws == nullptr || ws_bytes < moe::TC_SCHED_BYTES)
+    return fail(MOE_ERR_WORKSPACE, "workspace must hold at least 256 bytes");
+  if (!aligned256(ws)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   if (rows < 0 || rows >= int64_t{0xFFFFFFFF}) return fail(MOE_ERR_SHAPE, "rows must be in 0 .. 2^32-2");
   if (rows > 0 && (a == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "input and output must be non-NULL");
   if (ex->dtype != MOE_F32 && (!aligned16(a) || !aligned16(out)))
@@ -279,7 +283,8 @@ void moe_experts_destroy(moe_experts* experts) { delete experts; }
 
 size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* ex, int64_t rows) {
   if (ex == nullptr || rows < 0) return 0;
-  return align_up(static_cast<size_t>(rows) * static_cast<size_t>(ex->I) * dtype_size(ex->dtype) + 1, 256);
+  return align_up(static_cast<size_t>(rows) * static_cast<size_t>(ex->I) * dtype_size(ex->dtype) + 1, 256) +
+         moe::TC_SCHED_BYTES;
 }
 
 moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_dispatched,
@@ -299,27 +304,29 @@ moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_d
   moe_status st = check_current_device(ex);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
+  const size_t h_bytes = need - moe::TC_SCHED_BYTES;
   st = run_experts(ex, x_dispatched, offsets, rows, workspace, y_dispatched,
-                   static_cast<cudaStream_t>(stream));
+                   static_cast<uint8_t*>(workspace) + h_bytes, static_cast<cudaStream_t>(stream));
   if (st != MOE_OK) return st;
   return ok();
 }
 
 moe_status moe_experts_gate_up(const moe_experts* ex, const void* x_dispatched,
-                               const uint32_t* offsets, int64_t rows, void* h, void* stream) {
-  moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, h);
+                               const uint32_t* offsets, int64_t rows, void* h, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, h, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
-  st = run_stage(ex, true, x_dispatched, offsets, rows, h, static_cast<cudaStream_t>(stream));
+  st = run_stage(ex, true, x_dispatched, offsets, rows, h, workspace, static_cast<cudaStream_t>(stream));
   return st != MOE_OK ? st : ok();
 }
 
 moe_status moe_experts_down(const moe_experts* ex, const void* h, const uint32_t* offsets, int64_t rows,
-                            void* y_dispatched, void* stream) {
-  moe_status st = check_stage_args(ex, h, offsets, rows, y_dispatched);
+                            void* y_dispatched, void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_stage_args(ex, h, offsets, rows, y_dispatched, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
-  st = run_stage(ex, false, h, offsets, rows, y_dispatched, static_cast<cudaStream_t>(stream));
+  st = run_stage(ex, false, h, offsets, rows, y_dispatched, workspace, static_cast<cudaStream_t>(stream));
   return st != MOE_OK ? st : ok();
 }
 
@@ -379,7 +386,7 @@ moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
   err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, x, ex->dtype, ex->H, counts,
                              offsets, row_src, inv, xd, ws + L.scratch, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward dispatch launch");
-  st = run_experts(ex, xd, offsets, rows, h, yd, s);
+  st = run_experts(ex, xd, offsets, rows, h, yd, ws + L.sched, s);
   if (st != MOE_OK) return st;
   err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward combine launch");

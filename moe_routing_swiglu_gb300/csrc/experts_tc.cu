@@ -4,24 +4,43 @@
 // Per dispatched row r of expert e ("tiny-llm deep dive 5: ops.rs", section
 // on SiLU, FFN(x) = W_down (SiLU(W_gate x) * W_up x); shapes from the ruDNN
 // user guide, section 5):
-//   K3  acc = x_r [gate[e]; up[e]]^T      (K = H), epilogue h = SiLU(g) * u
-//   K4  acc = h_r down[e]^T               (K = I), epilogue y = acc
+//   K3  h_r = SiLU(W_gate[e] x_r) * (W_up[e] x_r)    (K = H)
+//   K4  y_r = W_down[e] h_r                          (K = I)
 // The SiLU-and-multiply is fused into K3's epilogue, so the gate and up
 // projections never reach HBM ("PyTorch general ops", section on RMSNorm
 // and SiLU x Mul).
 //
-// One persistent CTA per SM, 192 threads in three roles:
-//   warp 0 lane 0   TMA producer: A tile (128 rows x 64 K) + B tile (256 rows x 64 K)
-//                   per stage, 4 stages of 48 KB, 128-byte swizzle.
-//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per stage into
-//                   one of two 256-column TMEM accumulators; also allocates TMEM.
-//   warps 2..5      epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//                   lanes 32*(w%4)..), FP32 math, rounding, masked global stores.
-// Tiles: for K3 a tile is 128 rows x (128 gate + 128 up) columns, so gate and
-// up columns of the same i meet in one accumulator; for K4 it is 128 rows x
-// 256 output columns. The tile plan comes from the device offsets (the host
-// never learns per-expert counts); row tiles vary fastest so CTAs running at
-// the same time share each weight tile through L2.
+// Operand roles. The MMA's M side (128 TMEM lanes) holds expert weight rows
+// and its N side holds the expert's tokens, N = the tile's token count
+// rounded up to 16 (at most 256): an expert with 270 rows is one 256-token
+// tile plus one 16-token tile, and a decode expert with 1-2 tokens costs
+// N = 16. Each k-step issues two MMAs that share the token tile:
+//   K3 tile: A0 = gate rows c0..c0+127, A1 = up rows c0..c0+127  -> D0, D1
+//   K4 tile: A0 = down rows n0..n0+127, A1 = down rows n0+128..n0+255
+// so one token tile feeds 256 weight rows (the token rows are re-read from
+// L2 half as often as with one MMA), and TMEM lane i of D0 and D1 holds the
+// gate and up values of the same channel in the same thread.
+//
+// One persistent CTA per SM, 320 threads in three roles:
+//   warp 0 lane 0   scheduler + TMA producer: claims tiles from a global
+//                   counter (atomicAdd), publishes them in a 4-deep ring in
+//                   shared memory, and streams 3 stages of (2 x 16 KB weights
+//                   + N x 128 B tokens), 128-byte swizzle; token rows come
+//                   in 128-row and 16-row boxes so a short tile moves only
+//                   its rows.
+//   warp 1 lane 0   MMA issuer: 2 x 4 tcgen05.mma (M=128, N, K=16) per stage
+//                   into D0 (TMEM columns 0..N-1) and D1 (256..256+N-1); the
+//                   instruction descriptor carries the tile's N. Warp 1 also
+//                   allocates the 512 TMEM columns.
+//   warps 2..9      epilogue: warp w reads TMEM lanes 32*(w%4).. and takes
+//                   every other 32-token chunk; it computes the outputs in
+//                   FP32 (K3: SiLU(g)*u), transposes its 32 x 32 block
+//                   through a warp-private shared buffer and writes each
+//                   token's 64-byte runs with 16-byte stores.
+// Tiles: expert e has ceil(count_e / 256) token blocks times the weight
+// blocks; token blocks vary fastest and tiles are claimed in order, so the
+// CTAs that share a weight tile run together and read it from L2. The plan
+// comes from the device offsets (the host never learns per-expert counts).
 //
 // Every mbarrier wait is bounded (about a second). A wait that runs out
 // records a code in the device status word, raises the CTA's abort flag so
@@ -42,26 +61,34 @@ __device__ uint32_t g_moe_device_status = 0;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128;            // weight rows per MMA (TMEM lanes)
+constexpr int TB = 256;            // tokens per token block (max N)
+constexpr int BK = 64;             // one 128-byte swizzle atom of 16-bit elements
+constexpr int STAGES = 3;
 constexpr int UMMA_K = 16;
-constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KB
-constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;  // bytes landing per stage
-constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
-constexpr int NUM_THREADS = 192;
+constexpr int RING = 4;            // tile ring depth
+constexpr int ROW_BYTES = BK * 2;             // 128 B per row per stage
+constexpr int A_BYTES = BM * ROW_BYTES;       // 16 KB per weight tile
+constexpr int B_BYTES = TB * ROW_BYTES;       // 32 KB (N = 256)
+constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t D1_COL = 256;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
+constexpr int XPOSE_BYTES = 32 * 32 * 2;      // per-warp transpose buffer
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+constexpr uint32_t TILE_END = 0xFFFFFFFFu;
 
-constexpr int SMEM_A = 0;
-constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
-constexpr int SMEM_BAR = SMEM_B + STAGES * B_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_MISC = SMEM_BAR + 128;
+constexpr int SMEM_STAGES = 0;
+constexpr int SMEM_XPOSE = SMEM_STAGES + STAGES * STAGE_BYTES;
+constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_BYTES;
+// full[S], empty[S], tile_full[R], tile_empty[R], tfull, tempty, drain
+constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 3;
+constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
+constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
 constexpr int SMEM_TILES = SMEM_MISC + 16;
 constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
-static_assert(NUM_BARS * 8 <= 128, "barrier area");
+static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // Status codes recorded by a wait that timed out.
@@ -71,48 +98,48 @@ constexpr uint32_t ST_MMA_TMEM_EMPTY = 0x13;
 constexpr uint32_t ST_EPI_TMEM_FULL = 0x14;
 constexpr uint32_t ST_MMA_DRAIN = 0x15;
 constexpr uint32_t ST_PRODUCER_DRAIN = 0x16;
+constexpr uint32_t ST_TILE_RING = 0x17;
 constexpr uint32_t ST_SELFTEST = 0x100;
 
 struct TcArgs {
   const uint32_t* offsets;  // [E + 1]
   void* out;                // [rows, n_out]: h for K3, y for K4
+  uint32_t* sched;          // tile counter, zero at launch
   int E;
-  int n_tiles;              // column tiles per expert
+  int n_wblocks;            // weight blocks per expert (I/128 for K3, H/256 for K4)
   int k_blocks;             // ceil(K / BK)
   int n_out;                // output columns (I for K3, H for K4)
-  uint32_t rows_total;      // rows of the activation and output matrices
+  uint32_t rows_total;      // rows of the token and output matrices
   uint32_t tile_cap;        // host bound on the tile count
   uint32_t* status;
 };
 
-template <typename T>
-__device__ __forceinline__ void store_row_chunk(T* dst, int64_t col0, int64_t n_out,
-                                                const uint32_t (&packed)[16]) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    if (col0 + v * 8 + 8 <= n_out) {
-      *reinterpret_cast<uint4*>(dst + col0 + v * 8) =
-          make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-    }
-  }
+// SiLU(g) = g * sigmoid(g), sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
+// tanh.approx (relative error about 2^-11, below the 16-bit output's rounding).
+__device__ __forceinline__ float silu_f32(float g) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
+  return g * fmaf(0.5f, t, 0.5f);
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
-
+// Tensor maps: a0/a1 weight tiles (128-row boxes: K3 gate/up, K4 down rows
+// n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes.
 template <typename T, bool GATE_UP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
-                      const __grid_constant__ CUtensorMap tm_b0,
-                      const __grid_constant__ CUtensorMap tm_b1, const TcArgs args) {
+    experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                      const __grid_constant__ CUtensorMap tm_a1,
+                      const __grid_constant__ CUtensorMap tm_b128,
+                      const __grid_constant__ CUtensorMap tm_b16, const TcArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem + SMEM_A;
-  uint8_t* sB = smem + SMEM_B;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tile_full = empty + STAGES;
+  uint64_t* tile_empty = tile_full + RING;
+  uint64_t* tfull = tile_empty + RING;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  volatile uint32_t* ring = reinterpret_cast<volatile uint32_t*>(smem + SMEM_RING);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
   uint32_t* tile_start = reinterpret_cast<uint32_t*>(smem + SMEM_TILES);
@@ -125,20 +152,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+    for (int r = 0; r < RING; ++r) {
+      mbar_init(&tile_full[r], 1);
+      mbar_init(&tile_empty[r], NUM_EPI_WARPS);
     }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, NUM_EPI_WARPS);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_b0);
-    tma_prefetch_desc(&tm_b1);
+    tma_prefetch_desc(&tm_a0);
+    tma_prefetch_desc(&tm_a1);
+    tma_prefetch_desc(&tm_b128);
+    tma_prefetch_desc(&tm_b16);
   }
   __syncwarp();
-  if (warp == 0) build_tile_prefix(args.offsets, args.E, BM, args.n_tiles, tile_start);
+  if (warp == 0) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks, tile_start);
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
@@ -151,37 +181,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t total = min(tile_start[args.E], args.tile_cap);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ scheduler + TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (uint32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, BM, args.n_tiles);
+      for (uint32_t it = 0;; ++it) {
+        const uint32_t slot = it % RING;
+        if (!mbar_wait_bounded(&tile_empty[slot], ((it / RING) & 1u) ^ 1u, abort_flag, args.status,
+                               ST_TILE_RING, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const uint32_t claimed = atomicAdd(args.sched, 1u);
+        const uint32_t tile = claimed < total ? claimed : TILE_END;
+        ring[slot] = tile;
+        mbar_arrive(&tile_full[slot]);  // release: the ring entry is visible to the waiters
+        if (tile == TILE_END) break;
+        const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+        const int n_tok = (tc.rows + 15) & ~15;        // N of this tile
+        const int n128 = n_tok >> 7;                   // 128-row boxes
+        const int n16 = (n_tok & 127) >> 4;            // then 16-row boxes
+        const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + n_tok * ROW_BYTES);
+        const int wrow0 = GATE_UP ? tc.n * BM : tc.n * (2 * BM);
+        const int wrow1 = GATE_UP ? tc.n * BM : tc.n * (2 * BM) + BM;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  ST_PRODUCER_EMPTY, WAIT_LIMIT_NS)) {
             ok = false;
             break;
           }
-          uint8_t* a_dst = sA + stage * A_BYTES;
-          uint8_t* b_dst = sB + stage * B_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          tma_load_2d(a_dst, &tm_a, &full[stage], kb * BK, static_cast<int>(tc.row0));
-          if (GATE_UP) {
-            tma_load_3d(b_dst, &tm_b0, &full[stage], kb * BK, tc.n * (BN / 2), tc.e);
-            tma_load_3d(b_dst + B_BYTES / 2, &tm_b1, &full[stage], kb * BK, tc.n * (BN / 2), tc.e);
-          } else {
-            tma_load_3d(b_dst, &tm_b0, &full[stage], kb * BK, tc.n * BN, tc.e);
-            tma_load_3d(b_dst + B_BYTES / 2, &tm_b0, &full[stage], kb * BK, tc.n * BN + BN / 2, tc.e);
-          }
+          uint8_t* st = smem + SMEM_STAGES + stage * STAGE_BYTES;
+          const int k0 = kb * BK;
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_3d(st, &tm_a0, &full[stage], k0, wrow0, tc.e);
+          tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], k0, wrow1, tc.e);
+          uint8_t* b_dst = st + 2 * A_BYTES;
+          int r = 0;
+          for (int b = 0; b < n128; ++b, r += 128)
+            tma_load_2d(b_dst + r * ROW_BYTES, &tm_b128, &full[stage], k0, static_cast<int>(tc.row0) + r);
+          for (int b = 0; b < n16; ++b, r += 16)
+            tma_load_2d(b_dst + r * ROW_BYTES, &tm_b16, &full[stage], k0, static_cast<int>(tc.row0) + r);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        if (!ok) break;
       }
       if (!ok) {
         // Let the copies already in flight land before the block can exit.
@@ -198,20 +246,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
-      constexpr uint32_t IDESC = idesc_f16(kBF16, BM, BN);
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (uint32_t tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, args.status,
-                               ST_MMA_TMEM_EMPTY, WAIT_LIMIT_NS)) {
+      for (uint32_t it = 0;; ++it) {
+        const uint32_t slot = it % RING;
+        if (!mbar_wait_bounded(&tile_full[slot], (it / RING) & 1u, abort_flag, args.status,
+                               ST_TILE_RING, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const uint32_t tile = ring[slot];
+        if (tile == TILE_END) break;
+        const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+        const int n_tok = (tc.rows + 15) & ~15;
+        const uint32_t idesc = idesc_f16(kBF16, BM, n_tok);
+        if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, abort_flag, args.status, ST_MMA_TMEM_EMPTY,
+                               WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status, ST_MMA_FULL,
                                  WAIT_LIMIT_NS)) {
@@ -219,13 +275,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+          const uint32_t a0 = smem_u32(smem + SMEM_STAGES + stage * STAGE_BYTES);
+          const uint32_t a1 = a0 + A_BYTES;
+          const uint32_t b = a0 + 2 * A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            umma_f16(d_tmem, sdesc_kmajor_sw128(a_addr + k * UMMA_K * 2),
-                     sdesc_kmajor_sw128(b_addr + k * UMMA_K * 2), IDESC,
-                     (kb > 0 || k > 0) ? 1u : 0u);
+            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint64_t bd = sdesc_kmajor_sw128(b + k * UMMA_K * 2);
+            umma_f16(tmem_base, sdesc_kmajor_sw128(a0 + k * UMMA_K * 2), bd, idesc, acc);
+            umma_f16(tmem_base + D1_COL, sdesc_kmajor_sw128(a1 + k * UMMA_K * 2), bd, idesc, acc);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -234,9 +292,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        umma_commit(tfull);
+        acc_phase ^= 1u;
       }
       // Every MMA issued above completes before TMEM is released.
       umma_commit(drain);
@@ -245,56 +302,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    int acc = 0;
+    const int ew = warp - 2;                    // 0..7
+    const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
+    const int half = ew >> 2;                   // takes chunks half, half+2, ...
+    uint16_t* xp = reinterpret_cast<uint16_t*>(smem + SMEM_XPOSE + ew * XPOSE_BYTES);
+    const int rd_tok = lane >> 2;               // transpose read-back: token within 8
+    const int rd_part = lane & 3;               // 16-byte run within the 64-byte row
     uint32_t acc_phase = 0;
-    for (uint32_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, BM, args.n_tiles);
-      const bool ready = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.status,
-                                           ST_EPI_TMEM_FULL, WAIT_LIMIT_NS);
-      // The tcgen05.ld below is warp-collective: the whole warp goes on or stops.
-      if (!__all_sync(FULL_MASK, ready)) break;
+    bool live = true;
+    for (uint32_t it = 0; live; ++it) {
+      const uint32_t slot = it % RING;
+      bool ok = mbar_wait_bounded(&tile_full[slot], (it / RING) & 1u, abort_flag, args.status,
+                                  ST_TILE_RING, WAIT_LIMIT_NS);
+      const uint32_t tile = ok ? static_cast<uint32_t>(ring[slot]) : static_cast<uint32_t>(TILE_END);
+      if (!__all_sync(FULL_MASK, ok) || tile == TILE_END) break;
+      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+      ok = mbar_wait_bounded(tfull, acc_phase, abort_flag, args.status, ST_EPI_TMEM_FULL, WAIT_LIMIT_NS);
+      // tcgen05.ld is warp-collective: the whole warp goes on or stops.
+      if (!__all_sync(FULL_MASK, ok)) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
-      const bool row_ok = r < tc.rows && tc.row0 + static_cast<uint32_t>(r) < args.rows_total;
-      T* dst = static_cast<T*>(args.out) + (static_cast<int64_t>(tc.row0) + r) * args.n_out;
-      if (GATE_UP) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, g);
-          tmem_ld_32x32b_x32(t_row + BN / 2 + c * 32, u);
-          tmem_ld_wait();
-          uint32_t packed[16];
+      const int n_tok = (tc.rows + 15) & ~15;
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      // Output columns of this warp's 32 lanes (two blocks for K4).
+      const int64_t colA = GATE_UP ? static_cast<int64_t>(tc.n) * BM + quad * 32
+                                   : static_cast<int64_t>(tc.n) * (2 * BM) + quad * 32;
+      for (int c0 = 32 * half; c0 < n_tok; c0 += 64) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0), v0);
+        tmem_ld_32x32b_x32(t_lane + D1_COL + static_cast<uint32_t>(c0), v1);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float h0 = silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-            const float h1 = silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-            packed[i] = pack2<T>(h0, h1);
-          }
-          if (row_ok) store_row_chunk<T>(dst, static_cast<int64_t>(tc.n) * (BN / 2) + c * 32, args.n_out, packed);
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t d[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, d);
-          tmem_ld_wait();
-          uint32_t packed[16];
+        for (int blk = 0; blk < (GATE_UP ? 1 : 2); ++blk) {
+          // Lane = output column, j = token: write column-major, read token rows.
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            packed[i] = pack2<T>(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+          for (int j = 0; j < 32; ++j) {
+            float val;
+            if (GATE_UP) {
+              val = silu_f32(__uint_as_float(v0[j])) * __uint_as_float(v1[j]);
+            } else {
+              val = __uint_as_float(blk == 0 ? v0[j] : v1[j]);
+            }
+            const T hv = from_f32<T>(val);
+            xp[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
           }
-          if (row_ok) store_row_chunk<T>(dst, static_cast<int64_t>(tc.n) * BN + c * 32, args.n_out, packed);
+          __syncwarp();
+          const int64_t col = colA + (blk == 0 ? 0 : BM) + rd_part * 8;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int j = p * 8 + rd_tok;
+            const uint4 row = *reinterpret_cast<const uint4*>(xp + j * 32 + rd_part * 8);
+            const int t_in = c0 + j;
+            if (t_in < tc.rows && tc.row0 + static_cast<uint32_t>(t_in) < args.rows_total &&
+                col + 8 <= args.n_out) {
+              T* dst = static_cast<T*>(args.out) + (static_cast<int64_t>(tc.row0) + t_in) * args.n_out + col;
+              *reinterpret_cast<uint4*>(dst) = row;
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (lane == 0) {
+        mbar_arrive(tempty);
+        mbar_arrive(&tile_empty[slot]);
+      }
+      acc_phase ^= 1u;
     }
   }
 
@@ -338,70 +411,76 @@ CUtensorMapDataType tmap_dtype(moe_dtype d) {
   return d == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// [outer, inner] row-major 16-bit matrix, box 64 (inner) x 128 (outer).
-bool encode_2d(CUtensorMap* m, moe_dtype dt, const void* ptr, uint64_t inner, uint64_t outer) {
+// [outer, inner] row-major 16-bit matrix, box 64 (inner) x box_rows (outer).
+bool encode_2d(CUtensorMap* m, moe_dtype dt, const void* ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, tmap_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [E, rows, inner] row-major 16-bit tensor, box 64 x 128 x 1.
+// [E, rows, inner] row-major 16-bit tensor, box 64 x box_rows x 1.
 bool encode_3d(CUtensorMap* m, moe_dtype dt, const void* ptr, uint64_t inner, uint64_t rows,
-               uint64_t E) {
+               uint64_t E, uint32_t box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {inner, rows, E};
   const cuuint64_t strides[2] = {inner * 2, rows * inner * 2};
-  const cuuint32_t box[3] = {BK, BN / 2, 1};
+  const cuuint32_t box[3] = {BK, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, tmap_dtype(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int64_t tile_bound(int64_t rows, int E, int64_t n_tiles) {
-  const int64_t m_tiles = rows / BM + (rows < E ? rows : E);
-  return m_tiles * n_tiles;
+// Upper bound on the tile count: token blocks of at most 256 rows per expert.
+int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks) {
+  const int64_t t_blocks = rows / TB + (rows < E ? rows : E);
+  return t_blocks * n_wblocks;
 }
 
 template <typename T, bool GATE_UP>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                       const TcArgs& args, int64_t rows, int num_sms, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b128,
+                       const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream) {
   auto kern = experts_tc_kernel<T, GATE_UP>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  const int64_t bound = tile_bound(rows, args.E, args.n_tiles);
-  const int grid = static_cast<int>(bound < num_sms ? bound : num_sms);
+  const int grid = static_cast<int>(args.tile_cap < static_cast<uint32_t>(num_sms) ? args.tile_cap : num_sms);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, b0, b1, args);
+  err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a0, a1, b128, b16, args);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                          const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                         void* out, int num_sms, cudaStream_t stream, const char** why) {
+                         void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
+                         const char** why) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
   if (err != cudaSuccess) return err;
   const int64_t K = gate_up ? H : I;
   const int64_t n_out = gate_up ? I : H;
-  CUtensorMap ta;
-  if (!encode_2d(&ta, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows))) {
-    *why = "cuTensorMapEncodeTiled rejected the activation tensor map";
+  CUtensorMap t128, t16;
+  if (!encode_2d(&t128, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 128) ||
+      !encode_2d(&t16, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 16)) {
+    *why = "cuTensorMapEncodeTiled rejected the token tensor map";
     return cudaErrorInvalidValue;
   }
-  const int nt = static_cast<int>(gate_up ? (I + BN / 2 - 1) / (BN / 2) : (H + BN - 1) / BN);
-  TcArgs args{offsets, out, E, nt, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
-              static_cast<uint32_t>(rows), static_cast<uint32_t>(tile_bound(rows, E, nt)), status};
-  if (gate_up) return launch_one<T, true>(ta, w.gate, w.up, args, rows, num_sms, stream);
-  return launch_one<T, false>(ta, w.down, w.down, args, rows, num_sms, stream);
+  const int nw = static_cast<int>(gate_up ? (I + BM - 1) / BM : (H + 2 * BM - 1) / (2 * BM));
+  const int64_t cap = tile_bound(rows, E, nw);
+  TcArgs args{offsets, out, sched, E, nw, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
+              static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status};
+  if (gate_up) return launch_one<T, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
+  return launch_one<T, false>(w.down, w.down, t128, t16, args, num_sms, stream);
 }
 
 }  // namespace
@@ -412,8 +491,8 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
     *why = "the CUDA driver does not provide cuTensorMapEncodeTiled";
     return false;
   }
-  if (!encode_3d(&out->gate, dtype, gate, H, I, E) || !encode_3d(&out->up, dtype, up, H, I, E) ||
-      !encode_3d(&out->down, dtype, down, I, H, E)) {
+  if (!encode_3d(&out->gate, dtype, gate, H, I, E, BM) || !encode_3d(&out->up, dtype, up, H, I, E, BM) ||
+      !encode_3d(&out->down, dtype, down, I, H, E, BM)) {
     *why = "cuTensorMapEncodeTiled rejected an expert weight tensor map";
     return false;
   }
@@ -422,11 +501,13 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
 
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* out, int num_sms, cudaStream_t stream, const char** why) {
+                              void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
+                              const char** why) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
-    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, num_sms, stream, why);
-  return launch_stage<__half>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, num_sms, stream, why);
+    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, sched, num_sms,
+                                       stream, why);
+  return launch_stage<__half>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, sched, num_sms, stream, why);
 }
 
 cudaError_t read_device_status(uint32_t* code, bool clear) {

@@ -48,9 +48,12 @@ struct TcWeights {
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,
                        int64_t E, int64_t H, int64_t I, TcWeights* out, const char** why);
 // gate_up: K3, a = x_dispatched [rows, H] -> out = h [rows, I]; else K4, a = h -> out = y [rows, H].
+// sched: one uint32 of device memory for the tile counter (zeroed on the stream before the launch).
+constexpr size_t TC_SCHED_BYTES = 256;
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* out, int num_sms, cudaStream_t stream, const char** why);
+                              void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
+                              const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 

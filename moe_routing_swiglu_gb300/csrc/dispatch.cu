@@ -4,16 +4,17 @@
 // handing the index table to the compute kernels instead of pre-gathering;
 // the optional x_dispatched copy below serves the split API.
 //
-// The flat slots f = t*k + j are cut into chunks of DISPATCH_CHUNK. Three
-// passes make the layout stable (row order inside an expert = ascending f)
+// The flat slots f = t*k + j are cut into chunks of DISPATCH_CHUNK; two
+// launches make the layout stable (row order inside an expert = ascending f)
 // without atomics on the output:
 //   1. count:   per-chunk expert histogram          -> scratch[c][e]
-//   2. scan:    per expert, exclusive prefix over chunks plus the expert's
-//               offset                               -> scratch[c][e] = first row
-//               and counts / offsets
-//   3. scatter: inside a chunk, 8 warps take 256 slots each; per-warp
-//               histograms give each warp its first row per expert, and
-//               __match_any_sync ranks equal experts inside each 32-slot step.
+//   2. scatter: every chunk block re-derives what it needs from all chunks'
+//               histograms (expert totals -> exclusive scan -> offsets; the
+//               sum over earlier chunks -> its first row per expert); block 0
+//               writes counts and offsets. Inside a chunk, 8 warps take 256
+//               slots each: per-warp histograms give each warp its first row
+//               per expert, and __match_any_sync ranks equal experts inside
+//               each 32-slot step. Indices are loaded once into registers.
 // An index >= E is never dispatched; its inv entry is INVALID_ROW.
 #include <mutex>
 
@@ -26,111 +27,116 @@ namespace {
 constexpr int SCATTER_WARPS = 8;
 constexpr int SLOTS_PER_WARP = DISPATCH_CHUNK / SCATTER_WARPS;  // 256
 
-__global__ void __launch_bounds__(512) dispatch_count_kernel(const uint32_t* __restrict__ indices,
+__global__ void __launch_bounds__(256) dispatch_count_kernel(const uint32_t* __restrict__ indices,
                                                              int64_t n, int E,
                                                              uint32_t* __restrict__ hist) {
   __shared__ uint32_t h[ROUTE_MAX_E];
+  constexpr int PER = DISPATCH_CHUNK / 256;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK;
+  uint32_t e_reg[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int64_t f = base + threadIdx.x + 256 * i;
+    e_reg[i] = f < n ? indices[f] : 0xFFFFFFFFu;
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK;
-  for (int i = threadIdx.x; i < DISPATCH_CHUNK; i += blockDim.x) {
-    const int64_t f = base + i;
-    if (f < n) {
-      const uint32_t e = indices[f];
-      if (e < static_cast<uint32_t>(E)) atomicAdd(&h[e], 1u);
-    }
-  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (e_reg[i] < static_cast<uint32_t>(E)) atomicAdd(&h[e_reg[i]], 1u);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = h[e];
 }
 
-// One block of 1024 threads. hist[c][e] becomes the first dispatched row of
-// chunk c's slots for expert e.
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(uint32_t* __restrict__ hist,
-                                                             int nchunks, int E,
-                                                             uint32_t* __restrict__ counts,
-                                                             uint32_t* __restrict__ offsets) {
-  __shared__ uint32_t tot[ROUTE_MAX_E];
-  __shared__ uint32_t warp_sums[32];
-  const int tid = threadIdx.x;
-  // per-expert prefix over chunks (one expert per thread, E <= 1024)
-  uint32_t run = 0;
-  if (tid < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t v = hist[static_cast<int64_t>(c) * E + tid];
-      hist[static_cast<int64_t>(c) * E + tid] = run;
-      run += v;
-    }
-  }
-  // exclusive scan of the per-expert totals across the block
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = (tid < E) ? run : 0;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t o = __shfl_up_sync(FULL_MASK, incl, off);
-    if (lane >= off) incl += o;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t ws = warp_sums[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t o = __shfl_up_sync(FULL_MASK, ws, off);
-      if (lane >= off) ws += o;
-    }
-    warp_sums[lane] = ws;  // inclusive over warps
-  }
-  __syncthreads();
-  const uint32_t before_warp = warp > 0 ? warp_sums[warp - 1] : 0u;
-  const uint32_t excl = before_warp + incl - ((tid < E) ? run : 0u);
-  if (tid < E) {
-    tot[tid] = excl;
-    counts[tid] = run;
-    offsets[tid] = excl;
-  }
-  if (tid == 0) offsets[E] = warp_sums[31];
-  __syncthreads();
-  if (tid < E) {
-    for (int c = 0; c < nchunks; ++c) hist[static_cast<int64_t>(c) * E + tid] += tot[tid];
-  }
-}
-
 __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
-    const uint32_t* __restrict__ indices, int64_t n, int E, const uint32_t* __restrict__ first_row,
+    const uint32_t* __restrict__ indices, int64_t n, int E, int nchunks,
+    const uint32_t* __restrict__ hist, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets,
     uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv) {
   __shared__ uint32_t wh[SCATTER_WARPS][ROUTE_MAX_E];
+  __shared__ uint32_t first[ROUTE_MAX_E];   // first row of this chunk per expert
+  __shared__ uint32_t tot[ROUTE_MAX_E];
+  __shared__ uint32_t warp_sums[SCATTER_WARPS];
+  constexpr int STEPS = SLOTS_PER_WARP / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t chunk0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK;
-  const int64_t w0 = chunk0 + static_cast<int64_t>(warp) * SLOTS_PER_WARP;
+  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK +
+                     static_cast<int64_t>(warp) * SLOTS_PER_WARP;
+  uint32_t e_reg[STEPS];
+#pragma unroll
+  for (int i = 0; i < STEPS; ++i) {
+    const int64_t f = w0 + 32 * i + lane;
+    e_reg[i] = f < n ? indices[f] : 0xFFFFFFFFu;
+  }
+  // expert totals over all chunks and this chunk's offset from earlier chunks
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    uint32_t before = 0, all = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t v = hist[static_cast<int64_t>(c) * E + e];
+      before += c < static_cast<int>(blockIdx.x) ? v : 0u;
+      all += v;
+    }
+    first[e] = before;
+    tot[e] = all;
+  }
   for (int e = lane; e < E; e += 32) wh[warp][e] = 0;
-  __syncwarp();
-  for (int i = lane; i < SLOTS_PER_WARP; i += 32) {
-    const int64_t f = w0 + i;
-    if (f < n) {
-      const uint32_t e = indices[f];
-      if (e < static_cast<uint32_t>(E)) atomicAdd(&wh[warp][e], 1u);
+  __syncthreads();
+  // exclusive scan of the totals over experts: warp w scans experts [w*E/8 ...)
+  {
+    const int per = (E + SCATTER_WARPS - 1) / SCATTER_WARPS;
+    const int e_lo = warp * per, e_hi = min(E, e_lo + per);
+    uint32_t carry = 0;
+    for (int b = e_lo; b < e_hi; b += 32) {
+      const int e = b + lane;
+      const uint32_t v = e < e_hi ? tot[e] : 0u;
+      uint32_t incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(FULL_MASK, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (e < e_hi) tot[e] = carry + incl - v;   // exclusive within the warp's range
+      carry += __shfl_sync(FULL_MASK, incl, 31);
+    }
+    if (lane == 0) warp_sums[warp] = carry;
+  }
+#pragma unroll
+  for (int i = 0; i < STEPS; ++i)
+    if (e_reg[i] < static_cast<uint32_t>(E)) atomicAdd(&wh[warp][e_reg[i]], 1u);
+  __syncthreads();
+  {
+    const int per = (E + SCATTER_WARPS - 1) / SCATTER_WARPS;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      uint32_t off = tot[e];
+      for (int w = 0; w < e / per; ++w) off += warp_sums[w];
+      if (blockIdx.x == 0) offsets[e] = off;
+      uint32_t run = off + first[e];
+#pragma unroll
+      for (int w = 0; w < SCATTER_WARPS; ++w) {
+        const uint32_t v = wh[w][e];
+        wh[w][e] = run;
+        run += v;
+      }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      uint32_t all = 0;
+      for (int w = 0; w < SCATTER_WARPS; ++w) all += warp_sums[w];
+      offsets[E] = all;
     }
   }
-  __syncthreads();
-  // turn per-warp counts into each warp's first row per expert
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    uint32_t run = first_row[static_cast<int64_t>(blockIdx.x) * E + e];
-#pragma unroll
-    for (int w = 0; w < SCATTER_WARPS; ++w) {
-      const uint32_t v = wh[w][e];
-      wh[w][e] = run;
-      run += v;
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      uint32_t all = 0;
+      for (int c = 0; c < nchunks; ++c) all += hist[static_cast<int64_t>(c) * E + e];
+      counts[e] = all;
     }
   }
   __syncthreads();
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int step = 0; step < SLOTS_PER_WARP; step += 32) {
-    const int64_t f = w0 + step + lane;
+#pragma unroll
+  for (int i = 0; i < STEPS; ++i) {
+    const int64_t f = w0 + 32 * i + lane;
     const bool in_range = f < n;
-    uint32_t e = in_range ? indices[f] : 0xFFFFFFFFu;
-    const bool valid = in_range && e < static_cast<uint32_t>(E);
-    if (!valid) e = 0xFFFFFFFFu;
+    const bool valid = e_reg[i] < static_cast<uint32_t>(E);
+    const uint32_t e = valid ? e_reg[i] : 0xFFFFFFFFu;
     const uint32_t peers = __match_any_sync(FULL_MASK, e);
     uint32_t row = 0;
     if (valid) row = wh[warp][e] + __popc(peers & lt_mask);
@@ -143,6 +149,14 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     } else if (in_range) {
       inv[f] = INVALID_ROW;
     }
+  }
+}
+
+// With no slots at all the scatter kernel has no blocks: write zero counts/offsets.
+__global__ void dispatch_empty_kernel(int E, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    if (e < E) counts[e] = 0;
+    offsets[e] = 0;
   }
 }
 
@@ -208,13 +222,11 @@ cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k
   const int nchunks = static_cast<int>((n + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
   uint32_t* hist = static_cast<uint32_t*>(scratch);
   if (nchunks > 0) {
-    dispatch_count_kernel<<<nchunks, 512, 0, stream>>>(indices, n, E, hist);
-  }
-  // The scan also writes counts/offsets when there are no slots at all.
-  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(hist, nchunks, E, counts, offsets);
-  if (nchunks > 0) {
-    dispatch_scatter_kernel<<<nchunks, SCATTER_WARPS * 32, 0, stream>>>(indices, n, E, hist,
-                                                                        row_src, inv);
+    dispatch_count_kernel<<<nchunks, 256, 0, stream>>>(indices, n, E, hist);
+    dispatch_scatter_kernel<<<nchunks, SCATTER_WARPS * 32, 0, stream>>>(indices, n, E, nchunks, hist, counts,
+                                                                        offsets, row_src, inv);
+  } else {
+    dispatch_empty_kernel<<<1, 256, 0, stream>>>(E, counts, offsets);
   }
   if (x_dispatched != nullptr && n > 0) {
     const int64_t row_bytes = H * static_cast<int64_t>(dtype_size(dtype));

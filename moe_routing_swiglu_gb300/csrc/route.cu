@@ -8,30 +8,51 @@
 //
 // Layout: lane l of the warp holds experts l*V .. l*V+V-1 (V = ceil(E/32)
 // rounded up to a power of two), so walking lanes then registers visits the
-// experts in id order. That lets every lane form the softmax denominator as a
-// left-to-right FP32 sum over experts 0..E-1 (the broadcast order below), the
-// same order the oracle uses, so FP32 weights differ only by expf's ulps.
-// Selection is k rounds of a warp arg-max on (logit, id) with the order
-// "larger logit, then smaller id"; the winner's lane marks it taken.
+// experts in id order.
+//  * The denominator s = e_0 + e_1 + ... + e_{E-1} is a left-to-right FP32
+//    sum (the order the oracle uses, so FP32 weights differ only by expf's
+//    ulps): the lanes store their e_i to a warp-private shared buffer in id
+//    order and every lane adds them back in that order (broadcast reads).
+//  * Selection is k rounds of a warp arg-max over 64-bit keys
+//    (order-preserving bits of the logit, then the complement of the id), so
+//    the largest key is the largest logit with ties to the smaller id; the
+//    owner lane zeroes a taken key.
+//  * Slot j's lane then recomputes e_j = exp(l_j - m) (the same expression the
+//    sum used, hence the same value), divides by s, and the renormalizing sum
+//    is taken over slots 0..k-1 in order.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ bool better(float va, uint32_t ia, float vb, uint32_t ib) {
-  return va > vb || (va == vb && ia < ib);
+constexpr int ROUTE_WARPS = 8;
+
+// Larger key = larger logit; equal logits: larger key = smaller id. -0.0 is
+// folded into +0.0 first so the two compare equal, as floats do.
+__device__ __forceinline__ uint64_t route_key(float v, uint32_t id) {
+  uint32_t b = __float_as_uint(v + 0.0f);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(b) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - id);
+}
+
+__device__ __forceinline__ float key_logit(uint64_t key) {
+  const uint32_t b = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
 
 template <typename TL, int V>
-__global__ void __launch_bounds__(256) route_kernel(const TL* __restrict__ logits, int64_t T,
-                                                    int E, int k, int renormalize,
-                                                    uint32_t* __restrict__ indices,
-                                                    TL* __restrict__ weights,
-                                                    float* __restrict__ weights32) {
+__global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(const TL* __restrict__ logits, int64_t T,
+                                                                 int E, int k, int renormalize,
+                                                                 uint32_t* __restrict__ indices,
+                                                                 TL* __restrict__ weights,
+                                                                 float* __restrict__ weights32) {
+  __shared__ __align__(16) float e_sm[ROUTE_WARPS][32 * V];
   const int lane = threadIdx.x & 31;
+  float* my_e = e_sm[threadIdx.x >> 5];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float qnan = __int_as_float(0x7FC00000);
 
   for (int64_t t = warp0; t < T; t += nwarps) {
     const TL* row = logits + t * E;
@@ -54,8 +75,8 @@ __global__ void __launch_bounds__(256) route_kernel(const TL* __restrict__ logit
       // rule over all-equal keys picks ids 0..k-1.
       for (int j = lane; j < k; j += 32) {
         idx_row[j] = static_cast<uint32_t>(j);
-        weights[t * k + j] = from_f32<TL>(__int_as_float(0x7FC00000));
-        if (weights32 != nullptr) weights32[t * k + j] = __int_as_float(0x7FC00000);
+        weights[t * k + j] = from_f32<TL>(qnan);
+        if (weights32 != nullptr) weights32[t * k + j] = qnan;
       }
       continue;
     }
@@ -67,78 +88,95 @@ __global__ void __launch_bounds__(256) route_kernel(const TL* __restrict__ logit
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, off));
 
-    // e_i = exp(l_i - m) in FP32.
-    float e[V];
+    // e_i = exp(l_i - m), stored in id order; s = e_0 + ... + e_{E-1}.
 #pragma unroll
-    for (int v = 0; v < V; ++v) e[v] = (lane * V + v) < E ? expf(__fsub_rn(l[v], m)) : 0.0f;
-
-    // s = e_0 + e_1 + ... + e_{E-1}, left to right, identical on every lane.
-    float s = 0.0f;
-    for (int src = 0; src < 32; ++src) {
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const float ev = __shfl_sync(FULL_MASK, e[v], src);
-        if (src * V + v < E) s = __fadd_rn(s, ev);
-      }
+    for (int v = 0; v < V; ++v) {
+      const int id = lane * V + v;
+      my_e[id] = id < E ? expf(__fsub_rn(l[v], m)) : 0.0f;
     }
+    __syncwarp();
+    float s = 0.0f;
+    const int e4 = E & ~3;
+    for (int i = 0; i < e4; i += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(my_e + i);
+      s = __fadd_rn(s, q.x);
+      s = __fadd_rn(s, q.y);
+      s = __fadd_rn(s, q.z);
+      s = __fadd_rn(s, q.w);
+    }
+    for (int i = e4; i < E; ++i) s = __fadd_rn(s, my_e[i]);
+    __syncwarp();
 
-    // k rounds of arg-max over untaken experts; slot j keeps round j's winner.
-    uint32_t taken = 0;
-    float z = 0.0f;        // sum of selected p in slot order (renormalize)
-    float p_keep[V];       // slot j's p lives on lane j % 32, register j / 32
-    uint32_t id_keep[V];
+    // k rounds of arg-max; slot j's id ends on lane j % 32, register j / 32.
+    uint64_t key[V];
 #pragma unroll
-    for (int q = 0; q < V; ++q) { p_keep[q] = 0.0f; id_keep[q] = 0; }
+    for (int v = 0; v < V; ++v) {
+      const uint32_t id = static_cast<uint32_t>(lane * V + v);
+      key[v] = id < static_cast<uint32_t>(E) ? route_key(l[v], id) : 0ull;
+    }
+    uint32_t keep_id[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) keep_id[q] = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      uint32_t bi = 0xFFFFFFFFu;
+      uint64_t best = key[0];
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const uint32_t id = static_cast<uint32_t>(lane * V + v);
-        if (id < static_cast<uint32_t>(E) && !((taken >> v) & 1u) && better(l[v], id, bv, bi)) {
-          bv = l[v];
-          bi = id;
-        }
-      }
+      for (int v = 1; v < V; ++v) best = best > key[v] ? best : key[v];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(FULL_MASK, bv, off);
-        const uint32_t oi = __shfl_xor_sync(FULL_MASK, bi, off);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        const uint64_t o = __shfl_xor_sync(FULL_MASK, best, off);
+        best = best > o ? best : o;
       }
-      const int owner = static_cast<int>(bi / V);
-      const int slot = static_cast<int>(bi % V);
-      float ew = 0.0f;
+      const uint32_t id = 0xFFFFFFFFu - static_cast<uint32_t>(best);
+      if (lane == static_cast<int>(id / V)) {
+        const int slot = static_cast<int>(id % V);
 #pragma unroll
-      for (int v = 0; v < V; ++v) if (v == slot) ew = e[v];
-      ew = __shfl_sync(FULL_MASK, ew, owner);
-      if (lane == owner) taken |= 1u << slot;
-      const float p = __fdiv_rn(ew, s);
-      z = __fadd_rn(z, p);
+        for (int v = 0; v < V; ++v)
+          if (v == slot) key[v] = 0ull;
+      }
+      if (lane == (j & 31)) {
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
-        if (q == (j >> 5) && lane == (j & 31)) { p_keep[q] = p; id_keep[q] = bi; }
+        for (int q = 0; q < V; ++q)
+          if (q == (j >> 5)) keep_id[q] = id;
       }
     }
 
+    // p_j = e_j / s on slot j's lane; renormalize by the slot-ordered sum.
+    float p[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+      const int j = q * 32 + lane;
+      p[q] = 0.0f;
+      if (j < k) p[q] = __fdiv_rn(my_e[keep_id[q]], s);
+    }
+    float z = 0.0f;
+    if (renormalize) {
+      for (int j = 0; j < k; ++j) {
+        float pj = 0.0f;
+#pragma unroll
+        for (int q = 0; q < V; ++q)
+          if (q == (j >> 5)) pj = p[q];
+        z = __fadd_rn(z, __shfl_sync(FULL_MASK, pj, j & 31));
+      }
+    }
 #pragma unroll
     for (int q = 0; q < V; ++q) {
       const int j = q * 32 + lane;
       if (j < k) {
-        const float w = renormalize ? __fdiv_rn(p_keep[q], z) : p_keep[q];
-        idx_row[j] = id_keep[q];
+        const float w = renormalize ? __fdiv_rn(p[q], z) : p[q];
+        idx_row[j] = keep_id[q];
         weights[t * k + j] = from_f32<TL>(w);
         if (weights32 != nullptr) weights32[t * k + j] = w;
       }
     }
+    __syncwarp();
   }
 }
 
 template <typename TL>
 cudaError_t launch_route_t(const void* logits, int64_t T, int E, int k, bool renorm,
                            uint32_t* indices, void* weights, float* w32, cudaStream_t stream) {
-  const int threads = 256;
-  const int64_t want = (T + 7) / 8;
+  const int threads = ROUTE_WARPS * 32;
+  const int64_t want = (T + ROUTE_WARPS - 1) / ROUTE_WARPS;
   const int blocks = static_cast<int>(want < 65535 * 8 ? want : 65535 * 8);
   const TL* lg = static_cast<const TL*>(logits);
   TL* w = static_cast<TL*>(weights);

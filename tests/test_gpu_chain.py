@@ -71,9 +71,12 @@ def test_dispatch_parity(cuda_lib, name):
     _check_dispatch(cuda_lib, ref.indices, cfg.T, cfg.E, cfg.top_k, inp["x"])
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (2049, 3, 2), (5000, 1024, 9), (700, 64, 64), (4097, 8, 1)])
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (2049, 3, 2), (5000, 1024, 9), (700, 64, 64), (4097, 8, 1),
+                                   (70000, 64, 2), (33000, 1000, 4)])
 def test_dispatch_skewed_and_edge(cuda_lib, T, E, k):
-    """Chunk boundaries (2048 slots), one hot expert, many empty experts, E = 1024, k = E."""
+    """Chunk boundaries (2048 slots), one hot expert, many empty experts, E = 1024, k = E;
+    the last two exceed the one-block limit (131072 slots) and take the
+    three-kernel path."""
     rng = np.random.default_rng(T + E + k)
     p = rng.random(E) ** 8
     p[0] += 5

@@ -49,7 +49,8 @@ def _case(T, k, E, H, seed, dtype):
 def test_noalloc_dispatch_matches_moe_dispatch_twice(cuda_lib):
     lib = cuda_lib.load_library()
     stream = P(torch.cuda.current_stream().cuda_stream)
-    cases = [(9000, 6, 64, 256, 11, torch.float16), (700, 8, 128, 512, 12, torch.bfloat16)]
+    # the first case exceeds the one-block dispatch limit, so the fixed scratch is used
+    cases = [(70000, 2, 64, 64, 11, torch.float16), (700, 8, 128, 512, 12, torch.bfloat16)]
     for T, k, E, H, seed, dtype in cases:
         idx, x = _case(T, k, E, H, seed, dtype)
         ref = _buffers(T, k, E, H, dtype)

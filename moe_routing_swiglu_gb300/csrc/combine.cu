@@ -4,8 +4,10 @@
 //
 // out[t, :] = sum_{j=0..k-1} w[t, j] * y[inv[t*k + j], :], accumulated in FP32
 // in slot order j = 0, 1, ..., k-1, then rounded to the output dtype. One
-// block per token (grid-stride); each thread owns 16-byte vectors of the row.
-// No atomics, so the result does not depend on scheduling. A slot whose inv
+// block per token (grid-stride): the token's k row numbers and weights are
+// staged in shared memory, then each thread owns 16-byte vectors of the row
+// and keeps 4 slot-row loads in flight before their in-order FMAs. No
+// atomics, so the result does not depend on scheduling. A slot whose inv
 // entry is INVALID_ROW (an index >= E at dispatch), or any entry >= T*k,
 // makes its token's row NaN instead of reading out of range.
 #include "moe_common.cuh"
@@ -13,6 +15,8 @@
 
 namespace moe {
 namespace {
+
+constexpr int COMBINE_MAX_K = 1024;  // top_k <= E <= 1024
 
 template <typename T> struct Vec;
 template <> struct Vec<float> { static constexpr int N = 4; };
@@ -43,29 +47,52 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
                                                       int k, int64_t H, uint32_t rows,
                                                       T* __restrict__ out) {
   constexpr int NV = VEC ? Vec<T>::N : 1;
+  constexpr int G = 4;  // slot rows whose loads are in flight together
+  __shared__ uint32_t s_row[COMBINE_MAX_K];
+  __shared__ float s_w[COMBINE_MAX_K];
+  __shared__ int s_bad;
   const float qnan = __int_as_float(0x7FC00000);
   for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      const uint32_t r = inv[t * k + j];
+      s_row[j] = r < rows ? r : 0u;           // an invalid entry reads row 0 ...
+      s_w[j] = to_f32(w[t * k + j]);
+      if (r >= rows) s_bad = 1;               // ... and the whole row becomes NaN
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
     for (int64_t c = static_cast<int64_t>(threadIdx.x) * NV; c < H; c += static_cast<int64_t>(blockDim.x) * NV) {
       float acc[NV];
 #pragma unroll
       for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const float wj = to_f32(w[t * k + j]);
-        const uint32_t r = inv[t * k + j];
-        if (r >= rows) {  // INVALID_ROW, or a map entry out of range
+      int j0 = 0;
+      for (; j0 + G <= k; j0 += G) {
+        float v[G][NV];
 #pragma unroll
-          for (int i = 0; i < NV; ++i) acc[i] = qnan;
-          continue;
+        for (int g = 0; g < G; ++g) {
+          const T* src = y + static_cast<int64_t>(s_row[j0 + g]) * H + c;
+          if constexpr (VEC) load_vec<T>(src, v[g]);
+          else v[g][0] = to_f32(src[0]);
         }
-        const T* src = y + static_cast<int64_t>(r) * H + c;
-        if constexpr (VEC) {
-          float v[NV];
-          load_vec<T>(src, v);
 #pragma unroll
-          for (int i = 0; i < NV; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
-        } else {
-          acc[0] = fmaf(wj, to_f32(src[0]), acc[0]);
-        }
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = fmaf(s_w[j0 + g], v[g][i], acc[i]);
+      }
+      for (; j0 < k; ++j0) {
+        float v[NV];
+        const T* src = y + static_cast<int64_t>(s_row[j0]) * H + c;
+        if constexpr (VEC) load_vec<T>(src, v);
+        else v[0] = to_f32(src[0]);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = fmaf(s_w[j0], v[i], acc[i]);
+      }
+      if (bad) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = qnan;
       }
       T* dst = out + t * H + c;
       if constexpr (VEC) {

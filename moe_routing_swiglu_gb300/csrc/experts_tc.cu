@@ -62,34 +62,42 @@ __device__ uint32_t g_moe_device_status = 0;
 namespace {
 
 constexpr int BM = 128;            // weight rows per MMA (TMEM lanes)
-constexpr int TB = 256;            // tokens per token block (max N)
 constexpr int BK = 64;             // one 128-byte swizzle atom of 16-bit elements
-constexpr int STAGES = 3;
 constexpr int UMMA_K = 16;
 constexpr int RING = 4;            // tile ring depth
 constexpr int ROW_BYTES = BK * 2;             // 128 B per row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;       // 16 KB per weight tile
-constexpr int B_BYTES = TB * ROW_BYTES;       // 32 KB (N = 256)
-constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t D1_COL = 256;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int XPOSE_BYTES = 32 * 32 * 2;      // per-warp transpose buffer
+constexpr int STAGE_SMEM = 192 * 1024;        // shared memory given to pipeline stages
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 constexpr uint32_t TILE_END = 0xFFFFFFFFu;
 
-constexpr int SMEM_STAGES = 0;
-constexpr int SMEM_XPOSE = SMEM_STAGES + STAGES * STAGE_BYTES;
-constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_BYTES;
-// full[S], empty[S], tile_full[R], tile_empty[R], tfull, tempty, drain
-constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 3;
-constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
-constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
-constexpr int SMEM_TILES = SMEM_MISC + 16;
-constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
-static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// Layout for a token-block cap TBM (the largest N of a tile): 256 for
+// prefill; 32 for decode, where the smaller token tile leaves room for more
+// stages (more weight bytes in flight).
+template <int TBM>
+struct TcCfg {
+  static constexpr int B_BYTES = TBM * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+  static constexpr int STAGES = STAGE_SMEM / STAGE_BYTES;
+  static constexpr int SMEM_STAGES = 0;
+  static constexpr int SMEM_XPOSE = SMEM_STAGES + STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_BYTES;
+  // full[S], empty[S], tile_full[R], tile_empty[R], tfull, tempty, drain
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 3;
+  static constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
+  static constexpr int SMEM_TILES = SMEM_MISC + 16;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(TBM % 32 == 0 && TBM <= 256, "token block");
+};
 
 // Status codes recorded by a wait that timed out.
 constexpr uint32_t ST_PRODUCER_EMPTY = 0x11;
@@ -124,25 +132,29 @@ __device__ __forceinline__ float silu_f32(float g) {
 
 // Tensor maps: a0/a1 weight tiles (128-row boxes: K3 gate/up, K4 down rows
 // n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes.
-template <typename T, bool GATE_UP>
+template <typename T, bool GATE_UP, int TBM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
                       const __grid_constant__ CUtensorMap tm_b128,
                       const __grid_constant__ CUtensorMap tm_b16, const TcArgs args) {
+  using C = TcCfg<TBM>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int TB = TBM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::SMEM_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tile_full = empty + STAGES;
   uint64_t* tile_empty = tile_full + RING;
   uint64_t* tfull = tile_empty + RING;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  volatile uint32_t* ring = reinterpret_cast<volatile uint32_t*>(smem + SMEM_RING);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
-  uint32_t* tile_start = reinterpret_cast<uint32_t*>(smem + SMEM_TILES);
+  volatile uint32_t* ring = reinterpret_cast<volatile uint32_t*>(smem + C::SMEM_RING);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+  uint32_t* tile_start = reinterpret_cast<uint32_t*>(smem + C::SMEM_TILES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -212,7 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          uint8_t* st = smem + SMEM_STAGES + stage * STAGE_BYTES;
+          uint8_t* st = smem + C::SMEM_STAGES + stage * STAGE_BYTES;
           const int k0 = kb * BK;
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_3d(st, &tm_a0, &full[stage], k0, wrow0, tc.e);
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + SMEM_STAGES + stage * STAGE_BYTES);
+          const uint32_t a0 = smem_u32(smem + C::SMEM_STAGES + stage * STAGE_BYTES);
           const uint32_t a1 = a0 + A_BYTES;
           const uint32_t b = a0 + 2 * A_BYTES;
 #pragma unroll
@@ -305,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;                    // 0..7
     const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
     const int half = ew >> 2;                   // takes chunks half, half+2, ...
-    uint16_t* xp = reinterpret_cast<uint16_t*>(smem + SMEM_XPOSE + ew * XPOSE_BYTES);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * XPOSE_BYTES);
     const int rd_tok = lane >> 2;               // transpose read-back: token within 8
     const int rd_part = lane & 3;               // 16-byte run within the 64-byte row
     uint32_t acc_phase = 0;
@@ -439,16 +451,17 @@ bool encode_3d(CUtensorMap* m, moe_dtype dt, const void* ptr, uint64_t inner, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Upper bound on the tile count: token blocks of at most 256 rows per expert.
-int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks) {
-  const int64_t t_blocks = rows / TB + (rows < E ? rows : E);
+// Upper bound on the tile count: token blocks of at most tbm rows per expert.
+int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks, int tbm) {
+  const int64_t t_blocks = rows / tbm + (rows < E ? rows : E);
   return t_blocks * n_wblocks;
 }
 
-template <typename T, bool GATE_UP>
+template <typename T, bool GATE_UP, int TBM>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b128,
                        const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream) {
-  auto kern = experts_tc_kernel<T, GATE_UP>;
+  auto kern = experts_tc_kernel<T, GATE_UP, TBM>;
+  constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int grid = static_cast<int>(args.tile_cap < static_cast<uint32_t>(num_sms) ? args.tile_cap : num_sms);
@@ -476,11 +489,18 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
     return cudaErrorInvalidValue;
   }
   const int nw = static_cast<int>(gate_up ? (I + BM - 1) / BM : (H + 2 * BM - 1) / (2 * BM));
-  const int64_t cap = tile_bound(rows, E, nw);
+  // Decode-sized batches (at most 8 rows per expert on average) stream
+  // weights with 32-token blocks and deeper pipelines; prefill uses 256.
+  const bool small = rows <= 8 * static_cast<int64_t>(E);
+  const int64_t cap = tile_bound(rows, E, nw, small ? 32 : 256);
   TcArgs args{offsets, out, sched, E, nw, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
               static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status};
-  if (gate_up) return launch_one<T, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
-  return launch_one<T, false>(w.down, w.down, t128, t16, args, num_sms, stream);
+  if (small) {
+    if (gate_up) return launch_one<T, true, 32>(w.gate, w.up, t128, t16, args, num_sms, stream);
+    return launch_one<T, false, 32>(w.down, w.down, t128, t16, args, num_sms, stream);
+  }
+  if (gate_up) return launch_one<T, true, 256>(w.gate, w.up, t128, t16, args, num_sms, stream);
+  return launch_one<T, false, 256>(w.down, w.down, t128, t16, args, num_sms, stream);
 }
 
 }  // namespace

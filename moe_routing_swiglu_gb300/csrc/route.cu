@@ -17,9 +17,9 @@
 //    (order-preserving bits of the logit, then the complement of the id), so
 //    the largest key is the largest logit with ties to the smaller id; the
 //    owner lane zeroes a taken key.
-//  * Slot j's lane then recomputes e_j = exp(l_j - m) (the same expression the
-//    sum used, hence the same value), divides by s, and the renormalizing sum
-//    is taken over slots 0..k-1 in order.
+//  * Slot j's lane then reads its e_j back from that buffer (the value the sum
+//    used), divides by s, and the renormalizing sum is taken over slots
+//    0..k-1 in order.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -34,11 +34,6 @@ __device__ __forceinline__ uint64_t route_key(float v, uint32_t id) {
   uint32_t b = __float_as_uint(v + 0.0f);
   b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
   return (static_cast<uint64_t>(b) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - id);
-}
-
-__device__ __forceinline__ float key_logit(uint64_t key) {
-  const uint32_t b = static_cast<uint32_t>(key >> 32);
-  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
 
 template <typename TL, int V>

@@ -62,3 +62,19 @@ def test_tc_identity_experts_closed_form(cuda_lib):
     torch.cuda.synchronize()
     xf = f64(x)
     assert_output_close(f64(y), xf * xf / (1 + np.exp(-xf)), torch.bfloat16, "identity experts")
+
+
+def test_tc_decode_path_with_a_hot_expert(cuda_lib):
+    """Few rows per expert on average (the 32-token-block path) while one
+    expert holds about 75 rows (three token blocks) and most hold none."""
+    cfg = workloads.SMALL_CONFIGS["bf16_fine"].scaled("hot_decode", T=100, H=256, I=384, E=64, top_k=2, seed=91)
+    inp = workloads.generate(cfg)
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.permutation(64)[:2] for _ in range(cfg.T)]).astype(np.uint32)
+    idx[:75, 0] = 3
+    idx[:75, 1] = np.where(idx[:75, 1] == 3, 7, idx[:75, 1])
+    dp = moe_oracle.dispatch(idx, cfg.E)
+    assert dp.counts.max() > 32 and cfg.T * cfg.top_k <= 8 * cfg.E
+    y = _run_experts(cuda_lib, cfg, inp, dp)
+    yref = moe_oracle.experts_forward_dispatched(inp["x"], inp["gate"], inp["up"], inp["down"], dp, cfg.top_k)
+    assert_output_close(f64(y), yref, torch.bfloat16, "y_dispatched")

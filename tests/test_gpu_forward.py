@@ -80,6 +80,24 @@ def test_forward_equals_split_api(cuda_lib, name):
     assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8))
 
 
+@pytest.mark.parametrize("cfg_id", [2, 5])
+def test_forward_equals_split_api_full_size(cuda_lib, cfg_id):
+    """At full size (thousands of tiles): moe_forward is bit-identical, three
+    times in a row, to the split route -> dispatch -> experts -> combine path."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[cfg_id]
+    d = _device_inputs(workloads.generate(cfg))
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx2, w2 = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx2, cfg.E, d["x"])
+    y = moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets)
+    ref = moe.moe_combine(y, disp.inv, w2)
+    for _ in range(3):
+        out, _, _, _ = _forward(moe, cfg, d, ex)
+        assert torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+    assert moe.moe_device_status() == 0
+
+
 @pytest.mark.parametrize("name", ["bf16_fine", "f16_zipf"])
 def test_forward_deterministic(cuda_lib, name):
     moe = cuda_lib

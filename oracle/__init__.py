@@ -6,13 +6,18 @@ never calls the CUDA library.
 """
 from .moe_oracle import (  # noqa: F401
     DispatchResult,
+    GroupRoutingOptions,
     RouteResult,
+    check_group_options,
     combine,
     dispatch,
     experts_forward_dispatched,
     forward,
     forward_tokens,
+    forward_tokens_routed,
+    forward_with_routing,
     route,
+    route_sigmoid_grouped,
     round_to_dtype,
     silu,
     widen,

@@ -128,6 +128,98 @@ def route(logits, top_k: int, renormalize: bool, out_dtype: torch.dtype | None =
 
 
 @dataclass
+class GroupRoutingOptions:
+    """GroupRoutingOptions of the grouped sigmoid routing (ruDNN user guide,
+    section 10): top_k, groups, selected_groups, group_top_two, renormalize,
+    scale."""
+    top_k: int
+    groups: int
+    selected_groups: int
+    group_top_two: bool
+    renormalize: bool
+    scale: float
+
+
+def check_group_options(E: int, o: GroupRoutingOptions):
+    """The ranges the guide states: experts 1..=1024, groups 1..=128, top_k
+    1..=64; experts divisible by groups; selected groups valid; top_k at most
+    the experts of the selected groups; two experts per group for
+    group_top_two; scale finite and positive."""
+    G = E // o.groups if o.groups else 0
+    ok = (1 <= E <= 1024 and 1 <= o.groups <= 128 and 1 <= o.top_k <= 64 and E % o.groups == 0
+          and 1 <= o.selected_groups <= o.groups and o.top_k <= o.selected_groups * G
+          and (not o.group_top_two or G >= 2) and np.isfinite(o.scale) and o.scale > 0)
+    if not ok:
+        raise ValueError("invalid GroupRoutingOptions for E=%d: %r" % (E, o))
+
+
+def route_sigmoid_grouped(logits, bias, o: GroupRoutingOptions,
+                          out_dtype: torch.dtype | None = None) -> RouteResult:
+    """Group-limited sigmoid routing with a selection-only correction bias
+    (ruDNN user guide, section 10; the group-max, top-groups, mask, top-k
+    steps of the DeepSeek-style routing in "PyTorch general ops", section
+    "MoE routing: topk, scatter and masked_fill").
+
+    In FP32: s_i = 1 / (1 + exp(-l_i)); corrected c_i = s_i + bias_i (bias
+    only steers selection); group score = max of c over the group, or the
+    sum of its two largest c with group_top_two; the selected_groups best
+    groups (ties to the lower group id); among their experts the top_k
+    largest c (ties to the lower id), slot 0 the largest; weights are the
+    uncorrected s of the selected experts, divided by their slot-ordered sum
+    when renormalize, then multiplied by scale, then cast to the logits dtype.
+    Reading: a row holding a NaN (logit or bias) keeps NaN weights and
+    indices 0..k-1, as the softmax contract does for non-finite rows."""
+    if out_dtype is None:
+        out_dtype = logits.dtype if isinstance(logits, torch.Tensor) else torch.float32
+    l32 = widen(logits).astype(np.float32)
+    T, E = l32.shape
+    check_group_options(E, o)
+    k, G = o.top_k, E // o.groups
+    one = np.float32(1.0)
+    e = _exp32((-l32).astype(np.float32))
+    with np.errstate(over="ignore", divide="ignore"):
+        s = (one / (one + e).astype(np.float32)).astype(np.float32)
+    if bias is not None:
+        b32 = widen(bias).astype(np.float32).reshape(1, E)
+        c = (s + b32).astype(np.float32)
+    else:
+        c = s
+    bad = np.isnan(c).any(axis=1)
+
+    cg = c.reshape(T, o.groups, G).astype(np.float32)
+    if o.group_top_two:
+        srt = -np.sort(-cg.astype(np.float64), axis=2)             # descending, exact
+        gs = (srt[:, :, 0].astype(np.float32) + srt[:, :, 1].astype(np.float32)).astype(np.float32)
+    else:
+        gs = cg.max(axis=2)
+    gsel = np.argsort(-gs.astype(np.float64), axis=1, kind="stable")[:, :o.selected_groups]
+    in_sel = np.zeros((T, o.groups), dtype=bool)
+    np.put_along_axis(in_sel, gsel, True, axis=1)
+    expert_ok = np.repeat(in_sel, G, axis=1)
+    key = np.where(expert_ok, -c.astype(np.float64), np.inf)    # excluded experts sort last
+    order = np.argsort(key, axis=1, kind="stable")[:, :k]
+    order[bad] = np.arange(k)
+    indices = order.astype(np.uint32)
+
+    w = np.take_along_axis(s, order, axis=1).astype(np.float32)
+    if o.renormalize:
+        z = np.zeros(T, dtype=np.float32)
+        for j in range(k):
+            z = (z + w[:, j]).astype(np.float32)
+        w = (w / z[:, None]).astype(np.float32)
+    w = (w * np.float32(o.scale)).astype(np.float32)
+    w[bad] = np.nan
+
+    s64 = 1.0 / (1.0 + np.exp(-l32.astype(np.float64)))
+    w64 = np.take_along_axis(s64, order, axis=1)
+    if o.renormalize:
+        w64 = w64 / w64.sum(axis=1, keepdims=True)
+    w64 = w64 * float(o.scale)
+    w64[bad] = np.nan
+    return RouteResult(indices, w, round_to_dtype(w, out_dtype), w64, bad)
+
+
+@dataclass
 class DispatchResult:
     counts: np.ndarray   # [E] uint32
     offsets: np.ndarray  # [E+1] uint32, exclusive prefix of counts
@@ -223,6 +315,17 @@ def forward(x, logits, gate, up, down, top_k: int, renormalize: bool) -> Forward
     return ForwardResult(rt, dp, y, out)
 
 
+def forward_with_routing(x, gate, up, down, rt: RouteResult) -> ForwardResult:
+    """Dispatch, experts and combine for a given routing result (the same
+    chain after any routing function)."""
+    T, k = rt.indices.shape
+    E = gate.shape[0]
+    dp = dispatch(rt.indices, E)
+    y = experts_forward_dispatched(x, gate, up, down, dp, k)
+    out = combine(y, dp.inv, rt.weights, T, k)
+    return ForwardResult(rt, dp, y, out)
+
+
 def forward_tokens(x, logits, gate, up, down, top_k: int, renormalize: bool,
                    tokens: np.ndarray) -> np.ndarray:
     """The forward output for a subset of tokens only, [len(tokens), H] in f64.
@@ -230,6 +333,13 @@ def forward_tokens(x, logits, gate, up, down, top_k: int, renormalize: bool,
     on its own logits row and sent through its k experts."""
     tokens = np.asarray(tokens, dtype=np.int64)
     rt = route(logits[tokens], top_k, renormalize, out_dtype=logits.dtype)
+    return forward_tokens_routed(x, gate, up, down, rt, tokens)
+
+
+def forward_tokens_routed(x, gate, up, down, rt: RouteResult, tokens: np.ndarray) -> np.ndarray:
+    """forward_tokens for a routing result already taken on the sampled rows
+    (rt.indices[i] belongs to token tokens[i]), whatever routing made it."""
+    tokens = np.asarray(tokens, dtype=np.int64)
     x64 = widen(x[tokens])
     out = np.zeros((tokens.size, x64.shape[1]), dtype=np.float64)
     for e in np.unique(rt.indices):

@@ -1,16 +1,20 @@
 """Plant a plausible mistake in the CPU oracle (never in the CUDA path) and check
 that at least one pin of ``test_oracle_pins`` catches it."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 from oracle import moe_oracle
 from tests.test_oracle_pins import PINS
+from tests.test_oracle_sigmoid_pins import SIGMOID_PINS
 
 _route = moe_oracle.route
 _dispatch = moe_oracle.dispatch
 _combine = moe_oracle.combine
 _rows = moe_oracle._swiglu_rows
+_grouped = moe_oracle.route_sigmoid_grouped
 
 
 def _route_ignoring_renormalize(logits, top_k, renormalize, out_dtype=None):
@@ -83,6 +87,34 @@ def _forward_expert0_down(x, logits, gate, up, down, top_k, renormalize):
     return moe_oracle.__dict__["_forward_orig"](x, logits, gate, up, down0, top_k, renormalize)
 
 
+def _grouped_with(**changes):
+    def fn(logits, bias, o, out_dtype=None):
+        return _grouped(logits, bias, dataclasses.replace(o, **changes), out_dtype)
+    return fn
+
+
+def _grouped_no_group_limit(logits, bias, o, out_dtype=None):
+    return _grouped(logits, bias, dataclasses.replace(o, groups=1, selected_groups=1, group_top_two=False),
+                    out_dtype)
+
+
+def _grouped_bias_ignored(logits, bias, o, out_dtype=None):
+    return _grouped(logits, None, o, out_dtype)
+
+
+def _grouped_bias_in_weights(logits, bias, o, out_dtype=None):
+    rt = _grouped(logits, bias, o, out_dtype)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float32)[rt.indices.astype(np.int64)]
+        rt.weights32 = (rt.weights32 + b).astype(np.float32)
+        rt.weights64 = rt.weights64 + b
+    return rt
+
+
+def _grouped_sigmoid_wrong_sign(logits, bias, o, out_dtype=None):
+    return _grouped(-logits, bias, o, out_dtype)
+
+
 MUTATIONS = {
     "no_renormalize": ("route", _route_ignoring_renormalize),
     "ties_to_higher_id": ("route", _route_ties_to_higher_id),
@@ -109,5 +141,28 @@ def test_planted_mistake_is_caught(name, monkeypatch):
         try:
             pin(moe_oracle)
         except Exception as exc:  # an assertion or a shape error both count
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin catches the planted mistake {name!r}"
+
+
+SIGMOID_MUTATIONS = {
+    "grouped_ignores_renormalize": _grouped_with(renormalize=False),
+    "grouped_ignores_scale": _grouped_with(scale=1.0),
+    "grouped_max_instead_of_top_two": _grouped_with(group_top_two=False),
+    "grouped_no_group_limit": _grouped_no_group_limit,
+    "grouped_bias_ignored": _grouped_bias_ignored,
+    "grouped_bias_in_weights": _grouped_bias_in_weights,
+    "grouped_sigmoid_wrong_sign": _grouped_sigmoid_wrong_sign,
+}
+
+
+@pytest.mark.parametrize("name", sorted(SIGMOID_MUTATIONS))
+def test_planted_routing_mistake_is_caught(name, monkeypatch):
+    monkeypatch.setattr(moe_oracle, "route_sigmoid_grouped", SIGMOID_MUTATIONS[name])
+    caught = []
+    for pin in SIGMOID_PINS:
+        try:
+            pin(moe_oracle)
+        except Exception as exc:
             caught.append((pin.__name__, type(exc).__name__))
     assert caught, f"no pin catches the planted mistake {name!r}"

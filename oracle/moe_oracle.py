@@ -196,8 +196,10 @@ def route_sigmoid_grouped(logits, bias, o: GroupRoutingOptions,
     in_sel = np.zeros((T, o.groups), dtype=bool)
     np.put_along_axis(in_sel, gsel, True, axis=1)
     expert_ok = np.repeat(in_sel, G, axis=1)
-    key = np.where(expert_ok, -c.astype(np.float64), np.inf)    # excluded experts sort last
-    order = np.argsort(key, axis=1, kind="stable")[:, :k]
+    # Experts of the selected groups first (also one whose corrected score is
+    # -inf), then by descending c, ties to the lower id.
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((ids, -c.astype(np.float64), ~expert_ok), axis=1)[:, :k]
     order[bad] = np.arange(k)
     indices = order.astype(np.uint32)
 

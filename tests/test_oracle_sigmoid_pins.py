@@ -115,7 +115,7 @@ def pin_brute_force_grouped_selection(m):
                     o = Opt(k, groups, sel, top_two, False, 1.0)
                     p = rng.choice([0.25, 0.5, 0.75], size=(6, E))
                     l = torch.tensor(np.log(p / (1 - p)), dtype=torch.float32)
-                    b = torch.tensor(rng.choice([0.0, 0.25], size=E), dtype=torch.float32)
+                    b = torch.tensor(rng.choice([0.0, 0.25, 0.0, 0.25, -np.inf], size=E), dtype=torch.float32)
                     rt = m.route_sigmoid_grouped(l, b, o)
                     s = (np.float32(1) / (np.float32(1) + np.exp(-l.numpy().astype(np.float64)).astype(np.float32))
                          ).astype(np.float32)
@@ -143,6 +143,17 @@ def pin_deepseek_style_restatement(m):
     w = w / w.sum(dim=-1, keepdim=True)
     assert np.array_equal(rt.indices.astype(np.int64), ids.numpy())
     np.testing.assert_allclose(rt.weights32, w.numpy(), rtol=2e-6)
+
+
+def pin_minus_inf_bias_stays_in_its_group(m):
+    """An expert of a selected group whose bias is -inf still ranks ahead of
+    every expert outside the selected groups: scores [0.5, 0.5 | 0.9, s3]
+    with bias [0, 0, 0, -inf], one group of two by max, top-2 -> [2, 3]."""
+    l = torch.tensor([[0.0, 0.0, _logit(0.9), 0.3]])
+    b = torch.tensor([0.0, 0.0, 0.0, -np.inf], dtype=torch.float32)
+    rt = m.route_sigmoid_grouped(l, b, Opt(2, 2, 1, False, False, 1.0))
+    assert rt.indices[0].tolist() == [2, 3]
+    assert np.isfinite(rt.weights32[0]).all()
 
 
 def pin_sigmoid_nan_rows(m):
@@ -205,6 +216,7 @@ SIGMOID_PINS = [
     pin_renormalized_sum_is_scale,
     pin_brute_force_grouped_selection,
     pin_deepseek_style_restatement,
+    pin_minus_inf_bias_stays_in_its_group,
     pin_sigmoid_nan_rows,
     pin_option_ranges,
     pin_grouped_forward_per_token,

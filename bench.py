@@ -16,7 +16,9 @@ Printed (rank 0, one JSON line): tokens/s, grouped-GEMM TFLOP/s against the
 measured BF16 peak, route+dispatch microseconds, the decode workload's HBM
 GB/s over the touched expert weights, the roofline of the dominant kernel,
 the end-to-end number through moe_forward with host buffers, the CPU oracle
-baseline, kernel launches and the SM clocks seen during the run.
+baseline, kernel launches and the SM clocks seen during the run. A second,
+shorter run of the same chain with the grouped sigmoid routing in place of
+the softmax routing reports its tokens/s and routing time.
 
 --impl reference times the CPU oracle (the only reference this path has) on
 bounded samples of the same workload.
@@ -174,6 +176,15 @@ class Chain:
                                dtype=torch.uint8, **e)
         self.sws = torch.empty(moe.STAGE_WORKSPACE_BYTES, dtype=torch.uint8, **e)
         self.dt = moe._dt(d["x"])
+        self.grouped = None  # (bias device tensor or None, GroupRoutingOptions) to route by sigmoid groups
+
+    def use_grouped_routing(self, routing):
+        """Route by the grouped sigmoid routing from now on (routing: workloads.GroupedRouting)."""
+        assert routing.top_k == self.cfg.top_k
+        bias = workloads.grouped_bias(self.cfg.E, routing)
+        opts = self.moe.GroupRoutingOptions(routing.top_k, routing.groups, routing.selected_groups,
+                                            routing.group_top_two, routing.renormalize, routing.scale)
+        self.grouped = (None if bias is None else bias.to(self.dev), opts)
 
     def step(self, stream, ev=None):
         """route | dispatch | gate/up GEMM | down GEMM | combine, events between."""
@@ -183,8 +194,13 @@ class Chain:
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
         rc = 0
         rec(0)
-        rc |= lib.moe_route(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx), P(self.w),
-                            None, s)
+        if self.grouped is None:
+            rc |= lib.moe_route(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx),
+                                P(self.w), None, s)
+        else:
+            bias, opts = self.grouped
+            rc |= lib.moe_route_sigmoid_grouped(P(self.d["logits"]), self.dt, T, E, P(bias), ctypes.byref(opts),
+                                                P(self.idx), P(self.w), None, s)
         rec(1)
         rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts), P(self.offsets),
                                P(self.row_src), P(self.inv), P(self.xd), P(self.dws), self.dws.numel(), s)
@@ -307,6 +323,12 @@ def run_ours(args, rank, world, local_rank):
     e2e_s, h2d, d2h = e2e_steps(chain, stream, flush, min(args.steps, 20))
     e2e_s = max_over_ranks(e2e_s, world, dev)
     dec_stages, dec_total = timed_steps(decode, stream, flush, min(args.steps, 50), args.warmup)
+    grouped_cfg, grouped_routing = workloads.GROUPED["bf16_prefill_grouped"]
+    assert grouped_cfg is PREFILL
+    chain.use_grouped_routing(grouped_routing)
+    g_steps = min(args.steps, 200)
+    g_stages, g_total = timed_steps(chain, stream, flush, g_steps, args.warmup)
+    g_total = max_over_ranks(g_total, world, dev)
     clk = clocks.stop()
     assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
 
@@ -361,6 +383,14 @@ def run_ours(args, rank, world, local_rank):
                    "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),
                    "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
                    "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
+        "sigmoid_grouped": {
+            "workload": f"{c.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
+                        f"{grouped_routing.selected_groups} selected, top-two group scores, scale "
+                        f"{grouped_routing.scale}, FP32 bias N(0, {grouped_routing.bias_std}^2)",
+            "tokens_per_s": round(world * c.T * g_steps / g_total, 1),
+            "us_per_step": round(g_total / g_steps * 1e6, 2),
+            "route_us": round(float(g_stages[0]) * 1e6, 2),
+            "softmax_route_us": round(t_route * 1e6, 2)},
         "roofline": roof,
         "e2e": {"value": round(world * c.T / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "moe_forward"},

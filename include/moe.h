@@ -257,6 +257,70 @@ moe_status moe_forward(const moe_experts* experts, const void* x, const void* lo
                        size_t workspace_bytes, void* stream);
 
 /*
+ * moe_group_routing_options - GroupRoutingOptions of the group-limited
+ * sigmoid routing (ruDNN user guide, section 10).
+ *
+ *   top_k            1..64, at most selected_groups * (E / groups).
+ *   groups           1..128 and divides E.
+ *   selected_groups  1..groups: groups whose experts may be chosen.
+ *   group_top_two    nonzero: a group scores the sum of its two largest
+ *                    corrected scores (needs E / groups >= 2); zero: its
+ *                    largest corrected score.
+ *   renormalize      nonzero: divide the chosen weights by their sum.
+ *   scale            finite and > 0: multiplies the weights last.
+ */
+typedef struct {
+  int32_t top_k;
+  int32_t groups;
+  int32_t selected_groups;
+  int32_t group_top_two;
+  int32_t renormalize;
+  float scale;
+} moe_group_routing_options;
+
+/*
+ * moe_route_sigmoid_grouped - group-limited, bias-corrected sigmoid routing
+ * (route_sigmoid_grouped, ruDNN user guide section 10; the group steps
+ * follow the DeepSeek-style routing of "PyTorch general ops").
+ *
+ *   logits        device, [T, E] in `dtype` (MOE_F32, MOE_F16, MOE_BF16),
+ *                 1 <= E <= 1024, T >= 0 (T = 0 enqueues nothing).
+ *   bias          device, [E] float (FP32), or NULL for no correction; it
+ *                 steers the selection only. 4-byte aligned.
+ *   options       host pointer, read during the call only.
+ *   indices       device, [T, top_k] uint32 out: slot 0 the largest
+ *                 corrected score; ties to the lower id (groups too).
+ *   weights       device, [T, top_k] out in `dtype`: the uncorrected sigmoid
+ *                 scores of the chosen experts, optionally renormalized,
+ *                 times scale, rounded to `dtype` (round to nearest even).
+ *   weights_fp32  device, [T, top_k] float out before that rounding, or NULL.
+ *
+ * Scores are FP32: s = 1 / (1 + exp(-l)), c = s + bias. A row with a NaN
+ * logit (or any NaN bias) gets NaN weights and indices 0..top_k-1. A group
+ * whose two largest corrected scores are +inf and -inf has a NaN score and
+ * ranks below every other group. Errors: MOE_ERR_TOP_K for top_k outside
+ * 1..64 or above the selected groups' experts, MOE_ERR_SHAPE for any other
+ * option or size out of range, MOE_ERR_DTYPE, MOE_ERR_NULL, MOE_ERR_ALIGNMENT.
+ */
+moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_t T, int64_t E,
+                                     const float* bias, const moe_group_routing_options* options,
+                                     uint32_t* indices, void* weights, float* weights_fp32, void* stream);
+
+/*
+ * moe_forward_sigmoid_grouped - the whole local chain with grouped sigmoid
+ * routing (SwiGluExperts::forward_sigmoid_grouped, ruDNN user guide section
+ * 10): moe_route_sigmoid_grouped, then dispatch, SwiGLU experts and combine
+ * exactly as moe_forward does. Arguments as in moe_forward, with `bias` and
+ * `options` as in moe_route_sigmoid_grouped; the workspace is
+ * moe_forward_workspace_size(experts, T, options->top_k) bytes.
+ */
+moe_status moe_forward_sigmoid_grouped(const moe_experts* experts, const void* x, const void* logits,
+                                       moe_dtype logits_dtype, int64_t T, const float* bias,
+                                       const moe_group_routing_options* options, void* out,
+                                       uint32_t* indices_opt, void* weights_opt, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
  * moe_device_status - read (and clear, if `clear` is nonzero) the device
  * status word. The expert GEMM kernels bound every pipeline wait (about one
  * second); a wait that runs out stops its kernel's remaining work, lets the

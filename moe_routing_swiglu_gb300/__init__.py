@@ -26,8 +26,21 @@ STATUS_NAMES = {
     9: "MOE_ERR_DEVICE_CHECK",
 }
 
+
+class GroupRoutingOptions(ctypes.Structure):
+    """moe_group_routing_options (GroupRoutingOptions of the grouped sigmoid
+    routing): top_k, groups, selected_groups, group_top_two, renormalize, scale."""
+    _fields_ = [("top_k", ctypes.c_int32), ("groups", ctypes.c_int32), ("selected_groups", ctypes.c_int32),
+                ("group_top_two", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+    def __init__(self, top_k, groups, selected_groups, group_top_two=False, renormalize=True, scale=1.0):
+        super().__init__(int(top_k), int(groups), int(selected_groups), int(bool(group_top_two)),
+                         int(bool(renormalize)), float(scale))
+
+
 # Every entry point declared in include/moe.h: name -> (restype, argtypes).
 _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_OPT = ctypes.POINTER(GroupRoutingOptions)
 SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -48,6 +61,9 @@ SIGNATURES = {
     "moe_combine": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _I64, _I32, _I64, _P, _P]),
     "moe_forward_workspace_size": (_SZ, [_P, _I64, _I32]),
     "moe_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_sigmoid_grouped": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _OPT, _P, _P, _P, _P]),
+    "moe_forward_sigmoid_grouped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _P, _OPT, _P, _P, _P, _P,
+                                                   _SZ, _P]),
     "moe_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32]),
     "moe_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _P]),
 }
@@ -292,6 +308,60 @@ def moe_forward(experts: Experts, x: torch.Tensor, logits: torch.Tensor, top_k: 
                            int(bool(renormalize)), _ptr(o), _ptr(indices), _ptr(weights), _ptr(ws),
                            ws.numel(), _stream(stream)))
     return o
+
+
+def _options(options) -> GroupRoutingOptions:
+    if isinstance(options, GroupRoutingOptions):
+        return options
+    return GroupRoutingOptions(options.top_k, options.groups, options.selected_groups, options.group_top_two,
+                               options.renormalize, options.scale)
+
+
+def moe_route_sigmoid_grouped(logits: torch.Tensor, bias: torch.Tensor | None, options, *, indices=None,
+                              weights=None, weights_fp32=False, stream=None):
+    """route_sigmoid_grouped: (indices [T,k], weights [T,k] in the logits
+    dtype[, FP32 weights before the cast]). `options` is a
+    GroupRoutingOptions (or any object with the same fields); `bias` is an
+    FP32 [E] device tensor or None."""
+    lib = load_library()
+    _dev_tensor(logits, "logits")
+    if bias is not None:
+        _dev_tensor(bias, "bias")
+        if bias.dtype != torch.float32:
+            raise MoeError(3, "bias must be float32")
+    o = _options(options)
+    T, E = logits.shape
+    k = o.top_k
+    dev = logits.device
+    if indices is None:
+        indices = torch.empty(T, k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(T, k, dtype=logits.dtype, device=dev)
+    w32 = torch.empty(T, k, dtype=torch.float32, device=dev) if weights_fp32 is True else (
+        weights_fp32 if isinstance(weights_fp32, torch.Tensor) else None)
+    _check(lib.moe_route_sigmoid_grouped(_ptr(logits), _dt(logits), T, E, _ptr(bias), ctypes.byref(o),
+                                         _ptr(indices), _ptr(weights), _ptr(w32), _stream(stream)))
+    return (indices, weights, w32) if w32 is not None else (indices, weights)
+
+
+def moe_forward_sigmoid_grouped(experts: Experts, x: torch.Tensor, logits: torch.Tensor,
+                                bias: torch.Tensor | None, options, *, out=None, indices=None, weights=None,
+                                workspace=None, stream=None):
+    """SwiGluExperts::forward_sigmoid_grouped: the whole chain with grouped
+    sigmoid routing, out [T, H]."""
+    lib = load_library()
+    _dev_tensor(x, "x")
+    _dev_tensor(logits, "logits")
+    if bias is not None:
+        _dev_tensor(bias, "bias")
+    o = _options(options)
+    T = x.shape[0]
+    res = out if out is not None else torch.empty(T, experts.H, dtype=experts.dtype, device=x.device)
+    ws = _workspace(lib.moe_forward_workspace_size(experts.handle, T, o.top_k), x.device, workspace)
+    _check(lib.moe_forward_sigmoid_grouped(experts.handle, _ptr(x), _ptr(logits), _dt(logits), T, _ptr(bias),
+                                           ctypes.byref(o), _ptr(res), _ptr(indices), _ptr(weights), _ptr(ws),
+                                           ws.numel(), _stream(stream)))
+    return res
 
 
 def moe_device_status(clear: bool = True) -> int:

@@ -65,6 +65,38 @@ moe_status check_route_args(const void* logits, int dtype, int64_t T, int64_t E,
   return MOE_OK;
 }
 
+// GroupRoutingOptions ranges (ruDNN user guide, section 10).
+moe_status check_group_options(const moe_group_routing_options* o, int64_t E, moe::GroupRouteParams* p) {
+  if (o == nullptr) return fail(MOE_ERR_NULL, "options must be non-NULL");
+  if (o->groups < 1 || o->groups > 128) return fail(MOE_ERR_SHAPE, "groups must satisfy 1 <= groups <= 128");
+  if (E % o->groups != 0) return fail(MOE_ERR_SHAPE, "the expert count must be divisible by groups");
+  if (o->selected_groups < 1 || o->selected_groups > o->groups)
+    return fail(MOE_ERR_SHAPE, "selected_groups must satisfy 1 <= selected_groups <= groups");
+  const int64_t G = E / o->groups;
+  if (o->top_k < 1 || o->top_k > 64) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= 64");
+  if (o->top_k > o->selected_groups * G)
+    return fail(MOE_ERR_TOP_K, "top_k exceeds the experts of the selected groups");
+  if (o->group_top_two != 0 && G < 2)
+    return fail(MOE_ERR_SHAPE, "group_top_two needs at least two experts per group");
+  if (!(o->scale > 0.0f) || !(o->scale <= std::numeric_limits<float>::max()))
+    return fail(MOE_ERR_SHAPE, "scale must be finite and positive");
+  if (p != nullptr) {
+    p->k = o->top_k;
+    p->groups = o->groups;
+    p->group_size = static_cast<int>(G);
+    p->selected = o->selected_groups;
+    p->top_two = o->group_top_two != 0;
+    p->renormalize = o->renormalize != 0;
+    p->scale = o->scale;
+  }
+  return MOE_OK;
+}
+
+moe_status check_bias(const float* bias) {
+  if (reinterpret_cast<uintptr_t>(bias) % 4 != 0) return fail(MOE_ERR_ALIGNMENT, "bias must be 4-byte aligned");
+  return MOE_OK;
+}
+
 struct ForwardLayout {
   size_t indices, weights, counts, offsets, row_src, inv, scratch, sched, xd, h, yd, total;
 };
@@ -140,6 +172,46 @@ moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t
   if (ex->dtype != MOE_F32 && (!aligned16(a) || !aligned16(out)))
     return fail(MOE_ERR_ALIGNMENT, "input and output must be 16-byte aligned");
   return check_current_device(ex);
+}
+
+// Route (by the given launch), dispatch, experts, combine: the body of
+// moe_forward and moe_forward_sigmoid_grouped once the routing arguments
+// are checked.
+template <typename RouteLaunch>
+moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_dtype, int64_t T, int top_k,
+                         void* out, uint32_t* indices_opt, void* weights_opt, void* workspace,
+                         size_t workspace_bytes, cudaStream_t s, RouteLaunch route) {
+  if (T > 0 && (x == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "x and out must be non-NULL");
+  const ForwardLayout L = forward_layout(ex, T, top_k);
+  if (workspace == nullptr || workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_forward_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  moe_status st = check_current_device(ex);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* indices = indices_opt ? indices_opt : reinterpret_cast<uint32_t*>(ws + L.indices);
+  void* weights = weights_opt ? weights_opt : static_cast<void*>(ws + L.weights);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(ws + L.counts);
+  uint32_t* offsets = reinterpret_cast<uint32_t*>(ws + L.offsets);
+  uint32_t* row_src = reinterpret_cast<uint32_t*>(ws + L.row_src);
+  uint32_t* inv = reinterpret_cast<uint32_t*>(ws + L.inv);
+  void* xd = ws + L.xd;
+  void* h = ws + L.h;
+  void* yd = ws + L.yd;
+  const int64_t rows = T * top_k;
+
+  cudaError_t err = route(indices, weights, s);
+  if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
+  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, x, ex->dtype, ex->H, counts,
+                             offsets, row_src, inv, xd, ws + L.scratch, s);
+  if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
+  st = run_experts(ex, xd, offsets, rows, h, yd, ws + L.sched, s);
+  if (st != MOE_OK) return st;
+  err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
+  if (err != cudaSuccess) return cuda_fail(err, "forward combine launch");
+  return ok();
 }
 
 }  // namespace
@@ -358,39 +430,55 @@ moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
   if (ex == nullptr) return fail(MOE_ERR_NULL, "experts must be non-NULL");
   moe_status st = check_route_args(logits, logits_dtype, T, ex->E, top_k, logits, logits);
   if (st != MOE_OK) return st;
-  if (T > 0 && (x == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "x and out must be non-NULL");
-  const ForwardLayout L = forward_layout(ex, T, top_k);
-  if (workspace == nullptr || workspace_bytes < L.total)
-    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_forward_workspace_size()");
-  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  st = check_current_device(ex);
+  auto route = [&](uint32_t* indices, void* weights, cudaStream_t s) {
+    return moe::launch_route(logits, logits_dtype, T, static_cast<int>(ex->E), top_k, renormalize != 0,
+                             indices, weights, nullptr, s);
+  };
+  return forward_chain(ex, x, logits_dtype, T, top_k, out, indices_opt, weights_opt, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream), route);
+}
+
+moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_t T, int64_t E,
+                                     const float* bias, const moe_group_routing_options* options,
+                                     uint32_t* indices, void* weights, float* weights_fp32, void* stream) {
+  if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  moe::GroupRouteParams p{};
+  moe_status st = check_group_options(options, E, &p);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !slots_fit(T, p.k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && (logits == nullptr || indices == nullptr || weights == nullptr))
+    return fail(MOE_ERR_NULL, "logits, indices and weights must be non-NULL");
+  st = check_bias(bias);
   if (st != MOE_OK) return st;
   if (T == 0) return ok();
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* indices = indices_opt ? indices_opt : reinterpret_cast<uint32_t*>(ws + L.indices);
-  void* weights = weights_opt ? weights_opt : static_cast<void*>(ws + L.weights);
-  uint32_t* counts = reinterpret_cast<uint32_t*>(ws + L.counts);
-  uint32_t* offsets = reinterpret_cast<uint32_t*>(ws + L.offsets);
-  uint32_t* row_src = reinterpret_cast<uint32_t*>(ws + L.row_src);
-  uint32_t* inv = reinterpret_cast<uint32_t*>(ws + L.inv);
-  void* xd = ws + L.xd;
-  void* h = ws + L.h;
-  void* yd = ws + L.yd;
-  const int64_t rows = T * top_k;
-
-  cudaError_t err = moe::launch_route(logits, logits_dtype, T, static_cast<int>(ex->E), top_k,
-                                      renormalize != 0, indices, weights, nullptr, s);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_forward route launch");
-  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, x, ex->dtype, ex->H, counts,
-                             offsets, row_src, inv, xd, ws + L.scratch, s);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_forward dispatch launch");
-  st = run_experts(ex, xd, offsets, rows, h, yd, ws + L.sched, s);
-  if (st != MOE_OK) return st;
-  err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_forward combine launch");
+  cudaError_t err = moe::launch_route_sigmoid_grouped(logits, dtype, T, static_cast<int>(E), bias, p, indices,
+                                                      weights, weights_fp32, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_route_sigmoid_grouped launch");
   return ok();
+}
+
+moe_status moe_forward_sigmoid_grouped(const moe_experts* ex, const void* x, const void* logits,
+                                       moe_dtype logits_dtype, int64_t T, const float* bias,
+                                       const moe_group_routing_options* options, void* out,
+                                       uint32_t* indices_opt, void* weights_opt, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (ex == nullptr || options == nullptr) return fail(MOE_ERR_NULL, "experts and options must be non-NULL");
+  if (!dtype_valid(logits_dtype))
+    return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  moe::GroupRouteParams p{};
+  moe_status st = check_group_options(options, ex->E, &p);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !slots_fit(T, p.k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && logits == nullptr) return fail(MOE_ERR_NULL, "logits must be non-NULL");
+  st = check_bias(bias);
+  if (st != MOE_OK) return st;
+  auto route = [&](uint32_t* indices, void* weights, cudaStream_t s) {
+    return moe::launch_route_sigmoid_grouped(logits, logits_dtype, T, static_cast<int>(ex->E), bias, p,
+                                             indices, weights, nullptr, s);
+  };
+  return forward_chain(ex, x, logits_dtype, T, p.k, out, indices_opt, weights_opt, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream), route);
 }
 
 moe_status moe_device_status(uint32_t* code, int32_t clear) {

@@ -18,6 +18,20 @@ cudaError_t launch_route(const void* logits, moe_dtype dtype, int64_t T, int E, 
                          bool renormalize, uint32_t* indices, void* weights, float* weights_fp32,
                          cudaStream_t stream);
 
+// ---- grouped, bias-corrected sigmoid routing (route_grouped.cu)
+struct GroupRouteParams {
+  int k;            // top_k, 1..64
+  int groups;       // 1..128, divides E
+  int group_size;   // E / groups
+  int selected;     // selected groups, 1..groups
+  int top_two;      // group score: sum of the two largest corrected scores
+  int renormalize;  // divide the chosen weights by their sum
+  float scale;      // finite, > 0
+};
+cudaError_t launch_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_t T, int E,
+                                         const float* bias, const GroupRouteParams& p, uint32_t* indices,
+                                         void* weights, float* weights_fp32, cudaStream_t stream);
+
 // ---- K2 dispatch (dispatch.cu)
 constexpr int DISPATCH_CHUNK = 2048;  // flat slots per counting/scatter block
 size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k);

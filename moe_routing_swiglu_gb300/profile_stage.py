@@ -5,7 +5,9 @@
 The inputs are the seeded synthetic workloads of ``workloads.py``; routing and
 dispatch run once to set up the stage's inputs, then the chosen stage runs
 ``--reps`` times back to back (stream-ordered) and the device is synchronised.
-Stages: route, dispatch, gate_up, down, combine, forward (moe_forward).
+Stages: route, dispatch, gate_up, down, combine, forward (moe_forward), and
+route_grouped (the grouped sigmoid routing, on workloads that have a grouped
+variant in ``workloads.GROUPED``).
 """
 from __future__ import annotations
 
@@ -30,7 +32,7 @@ def main(argv=None):
     names.update(workloads.SMALL_CONFIGS)
     ap.add_argument("--workload", default="cfg2", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "gate_up", "down", "combine", "forward"])
+                    choices=["route", "dispatch", "gate_up", "down", "combine", "forward", "route_grouped"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     cfg = names[args.workload]
@@ -43,6 +45,15 @@ def main(argv=None):
     disp = moe.moe_dispatch(idx, cfg.E, d["x"])
     h = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
     y = moe.moe_experts_down(ex, h, disp.offsets)
+    grouped = [r for c, r in workloads.GROUPED.values() if c is cfg]
+    if args.stage == "route_grouped":
+        if not grouped:
+            ap.error(f"{args.workload} has no grouped-routing variant")
+        r = grouped[0]
+        bias = workloads.grouped_bias(cfg.E, r)
+        bias = None if bias is None else bias.to(dev)
+        opts = moe.GroupRoutingOptions(r.top_k, r.groups, r.selected_groups, r.group_top_two, r.renormalize,
+                                       r.scale)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         if args.stage == "route":
@@ -53,6 +64,8 @@ def main(argv=None):
             moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h)
         elif args.stage == "down":
             moe.moe_experts_down(ex, h, disp.offsets, out=y)
+        elif args.stage == "route_grouped":
+            moe.moe_route_sigmoid_grouped(d["logits"], bias, opts, indices=idx, weights=w)
         elif args.stage == "combine":
             moe.moe_combine(y, disp.inv, w)
         else:

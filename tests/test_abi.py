@@ -129,6 +129,45 @@ def test_combine_rejects_bad_arguments(lib, kwargs, status):
                            a["out"], None) == status
 
 
+def _grouped(lib, logits=FAKE, dtype=2, T=4, E=8, bias=None, opts=None, idx=FAKE, w=FAKE, **opt_kw):
+    o = dict(top_k=2, groups=4, selected_groups=2, group_top_two=True, renormalize=True, scale=1.0)
+    o.update(opt_kw)
+    options = moe.GroupRoutingOptions(**o) if opts is None else opts
+    ref = ctypes.byref(options) if options is not False else None
+    return lib.moe_route_sigmoid_grouped(logits, dtype, T, E, bias, ref, idx, w, None, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(w=None), 1), (dict(opts=False), 1),
+    (dict(dtype=3), 3), (dict(E=0), 2), (dict(E=1025), 2), (dict(T=-1), 2),
+    (dict(top_k=0), 4), (dict(top_k=65, E=128, groups=1, selected_groups=1), 4),
+    (dict(top_k=5, selected_groups=2), 4),                  # 2 groups of 2 experts hold only 4
+    (dict(groups=3), 2), (dict(groups=0), 2), (dict(groups=129, E=258), 2),
+    (dict(selected_groups=0), 2), (dict(selected_groups=5), 2),
+    (dict(groups=8, selected_groups=2, top_k=1), 2),        # top-two needs two experts per group
+    (dict(scale=0.0), 2), (dict(scale=-1.0), 2), (dict(scale=float("inf")), 2), (dict(scale=float("nan")), 2),
+    (dict(bias=P(0x100002)), 5),
+])
+def test_grouped_route_rejects_bad_arguments(lib, kwargs, status):
+    assert _grouped(lib, **kwargs) == status
+    assert lib.moe_last_error().decode() != ""
+
+
+def test_grouped_route_accepts_the_edges_on_the_host(lib):
+    """T = 0 enqueues nothing, so valid options return MOE_OK without a GPU."""
+    assert _grouped(lib, T=0, logits=None, idx=None, w=None) == 0
+    assert _grouped(lib, T=0, E=1024, groups=128, selected_groups=128, top_k=64, group_top_two=True) == 0
+    assert _grouped(lib, T=0, E=7, groups=1, selected_groups=1, top_k=7, group_top_two=False) == 0
+
+
+def test_grouped_forward_rejects_bad_arguments(lib):
+    o = moe.GroupRoutingOptions(2, 4, 2, True, True, 1.0)
+    args = [FAKE, FAKE, 2, 4, None, ctypes.byref(o), FAKE, None, None, FAKE, 1 << 20, None]
+    assert lib.moe_forward_sigmoid_grouped(None, *args) == 1
+    assert lib.moe_forward_sigmoid_grouped(FAKE, FAKE, FAKE, 2, 4, None, None, FAKE, None, None, FAKE, 1 << 20,
+                                           None) == 1
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.moe_selftest_bounded_wait(0, None) == 2
     assert lib.moe_selftest_bounded_wait(10_000_001, None) == 2

@@ -96,6 +96,45 @@ SMALL_CONFIGS = {
 }
 
 
+@dataclass(frozen=True)
+class GroupedRouting:
+    """Options of the group-limited sigmoid routing (ruDNN user guide,
+    section 10) and the recipe of its FP32 correction bias: N(0, bias_std^2)
+    from a torch Generator seeded with ``bias_seed`` (no bias if bias_std is 0)."""
+
+    groups: int
+    selected_groups: int
+    top_k: int
+    group_top_two: bool
+    renormalize: bool
+    scale: float
+    bias_std: float
+    bias_seed: int
+
+
+# Grouped sigmoid routing on the shapes of the workloads above (the pages give
+# no sizes for it): 8 groups of 16 experts, 4 selected, top-8, top-two group
+# scores and a 2.5 scale on the fine-grained prefill and decode shapes, and
+# smaller group layouts on the reduced workloads (one expert per group,
+# one group of all experts, groups of 6 and of 4).
+GROUPED = {
+    "bf16_prefill_grouped": (CONFIGS[2], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3002)),
+    "bf16_decode_grouped": (CONFIGS[4], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3004)),
+    "bf16_fine_grouped": (SMALL_CONFIGS["bf16_fine"], GroupedRouting(4, 2, 5, True, True, 1.0, 0.05, 3012)),
+    "f16_zipf_grouped": (SMALL_CONFIGS["f16_zipf"], GroupedRouting(4, 2, 3, False, False, 1.5, 0.1, 3015)),
+    "f32_ragged_grouped": (SMALL_CONFIGS["f32_ragged"], GroupedRouting(7, 3, 3, False, True, 1.0, 0.1, 3016)),
+    "bf16_ragged_grouped": (SMALL_CONFIGS["bf16_ragged"], GroupedRouting(1, 1, 2, True, False, 2.0, 0.0, 3017)),
+}
+
+
+def grouped_bias(E: int, r: GroupedRouting) -> torch.Tensor | None:
+    """The FP32 [E] correction bias of a grouped-routing workload, or None."""
+    if r.bias_std == 0:
+        return None
+    g = torch.Generator().manual_seed(r.bias_seed)
+    return (torch.randn(E, generator=g) * r.bias_std).to(torch.float32)
+
+
 def _chunk_seed(base: int, tensor_id: int, chunk: int) -> int:
     return (base * 1_000_003 + tensor_id * 10_007 + chunk) & 0x7FFF_FFFF_FFFF
 

@@ -68,7 +68,6 @@ constexpr int RING = 4;            // tile ring depth
 constexpr int ROW_BYTES = BK * 2;             // 128 B per row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;       // 16 KB per weight tile
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t D1_COL = 256;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int XPOSE_BYTES = 32 * 32 * 2;      // per-warp transpose buffer
@@ -84,11 +83,17 @@ struct TcCfg {
   static constexpr int B_BYTES = TBM * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
   static constexpr int STAGES = STAGE_SMEM / STAGE_BYTES;
+  // Accumulator buffers in TMEM: one tile needs D0 and D1 of TBM columns
+  // each, so tiles of up to 128 tokens get two buffers and the MMAs of the
+  // next tile run while the epilogue drains the previous one.
+  static constexpr int ACC = (2 * 2 * TBM <= static_cast<int>(TMEM_COLS)) ? 2 : 1;
+  static constexpr uint32_t ACC_COLS = TMEM_COLS / ACC;  // columns per buffer
+  static constexpr uint32_t D1 = ACC_COLS / 2;           // D1 offset within a buffer
   static constexpr int SMEM_STAGES = 0;
   static constexpr int SMEM_XPOSE = SMEM_STAGES + STAGES * STAGE_BYTES;
   static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_BYTES;
-  // full[S], empty[S], tile_full[R], tile_empty[R], tfull, tempty, drain
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 3;
+  // full[S], empty[S], tile_full[R], tile_empty[R], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
   static constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
   static constexpr int SMEM_TILES = SMEM_MISC + 16;
@@ -97,6 +102,7 @@ struct TcCfg {
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(TBM % 32 == 0 && TBM <= 256, "token block");
+  static_assert(2 * TBM <= static_cast<int>(ACC_COLS), "D0 and D1 fit one accumulator buffer");
 };
 
 // Status codes recorded by a wait that timed out.
@@ -148,9 +154,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tile_full = empty + STAGES;
   uint64_t* tile_empty = tile_full + RING;
-  uint64_t* tfull = tile_empty + RING;
-  uint64_t* tempty = tfull + 1;
-  uint64_t* drain = tempty + 1;
+  uint64_t* tfull = tile_empty + RING;   // [2]
+  uint64_t* tempty = tfull + 2;          // [2]
+  uint64_t* drain = tempty + 2;
   volatile uint32_t* ring = reinterpret_cast<volatile uint32_t*>(smem + C::SMEM_RING);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
@@ -168,8 +174,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tile_full[r], 1);
       mbar_init(&tile_empty[r], NUM_EPI_WARPS);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, NUM_EPI_WARPS);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], NUM_EPI_WARPS);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -260,7 +268,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase = 0;
       bool ok = true;
       for (uint32_t it = 0;; ++it) {
         const uint32_t slot = it % RING;
@@ -274,12 +281,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
         const int n_tok = (tc.rows + 15) & ~15;
         const uint32_t idesc = idesc_f16(kBF16, BM, n_tok);
-        if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, abort_flag, args.status, ST_MMA_TMEM_EMPTY,
+        const uint32_t acc = it % C::ACC;             // accumulator buffer of this tile
+        const uint32_t acc_use = it / C::ACC;         // earlier tiles on this buffer
+        if (!mbar_wait_bounded(&tempty[acc], (acc_use & 1u) ^ 1u, abort_flag, args.status, ST_MMA_TMEM_EMPTY,
                                WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status, ST_MMA_FULL,
                                  WAIT_LIMIT_NS)) {
@@ -292,10 +302,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b = a0 + 2 * A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
             const uint64_t bd = sdesc_kmajor_sw128(b + k * UMMA_K * 2);
-            umma_f16(tmem_base, sdesc_kmajor_sw128(a0 + k * UMMA_K * 2), bd, idesc, acc);
-            umma_f16(tmem_base + D1_COL, sdesc_kmajor_sw128(a1 + k * UMMA_K * 2), bd, idesc, acc);
+            umma_f16(d0, sdesc_kmajor_sw128(a0 + k * UMMA_K * 2), bd, idesc, accum);
+            umma_f16(d0 + C::D1, sdesc_kmajor_sw128(a1 + k * UMMA_K * 2), bd, idesc, accum);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -304,8 +314,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        umma_commit(tfull);
-        acc_phase ^= 1u;
+        umma_commit(&tfull[acc]);
       }
       // Every MMA issued above completes before TMEM is released.
       umma_commit(drain);
@@ -320,7 +329,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * XPOSE_BYTES);
     const int rd_tok = lane >> 2;               // transpose read-back: token within 8
     const int rd_part = lane & 3;               // 16-byte run within the 64-byte row
-    uint32_t acc_phase = 0;
     bool live = true;
     for (uint32_t it = 0; live; ++it) {
       const uint32_t slot = it % RING;
@@ -329,19 +337,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tile = ok ? static_cast<uint32_t>(ring[slot]) : static_cast<uint32_t>(TILE_END);
       if (!__all_sync(FULL_MASK, ok) || tile == TILE_END) break;
       const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
-      ok = mbar_wait_bounded(tfull, acc_phase, abort_flag, args.status, ST_EPI_TMEM_FULL, WAIT_LIMIT_NS);
+      const uint32_t acc = it % C::ACC;
+      ok = mbar_wait_bounded(&tfull[acc], (it / C::ACC) & 1u, abort_flag, args.status, ST_EPI_TMEM_FULL,
+                             WAIT_LIMIT_NS);
       // tcgen05.ld is warp-collective: the whole warp goes on or stops.
       if (!__all_sync(FULL_MASK, ok)) break;
       tc_fence_after();
       const int n_tok = (tc.rows + 15) & ~15;
-      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t t_lane = tmem_base + acc * C::ACC_COLS + (static_cast<uint32_t>(quad * 32) << 16);
       // Output columns of this warp's 32 lanes (two blocks for K4).
       const int64_t colA = GATE_UP ? static_cast<int64_t>(tc.n) * BM + quad * 32
                                    : static_cast<int64_t>(tc.n) * (2 * BM) + quad * 32;
       for (int c0 = 32 * half; c0 < n_tok; c0 += 64) {
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0), v0);
-        tmem_ld_32x32b_x32(t_lane + D1_COL + static_cast<uint32_t>(c0), v1);
+        tmem_ld_32x32b_x32(t_lane + C::D1 + static_cast<uint32_t>(c0), v1);
         tmem_ld_wait();
 #pragma unroll
         for (int blk = 0; blk < (GATE_UP ? 1 : 2); ++blk) {
@@ -376,10 +386,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(tempty);
+        mbar_arrive(&tempty[acc]);
         mbar_arrive(&tile_empty[slot]);
       }
-      acc_phase ^= 1u;
     }
   }
 
@@ -490,7 +499,9 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   }
   const int nw = static_cast<int>(gate_up ? (I + BM - 1) / BM : (H + 2 * BM - 1) / (2 * BM));
   // Decode-sized batches (at most 8 rows per expert on average) stream
-  // weights with 32-token blocks and deeper pipelines; prefill uses 256.
+  // weights with 32-token blocks, deeper pipelines and double-buffered
+  // accumulators; prefill uses 256-token blocks (each weight tile feeds
+  // twice the tokens; measured faster than 128 with double buffering).
   const bool small = rows <= 8 * static_cast<int64_t>(E);
   const int64_t cap = tile_bound(rows, E, nw, small ? 32 : 256);
   TcArgs args{offsets, out, sched, E, nw, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),

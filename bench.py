@@ -51,7 +51,7 @@ METRIC = "MoE fwd tokens/s + grouped-GEMM TFLOP/s vs bf16 peak; decode HBM GB/s"
 PREFILL = workloads.CONFIGS[2]
 DECODE = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 8  # route, dispatch count/scan/scatter/gather, gate/up GEMM, down GEMM, combine
+KERNELS_PER_STEP = 7  # route, dispatch count + scatter + gather, gate/up GEMM, down GEMM, combine
 # (plus one 4-byte memset node before each GEMM that resets its tile counter)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -171,7 +171,10 @@ class Chain:
         self.offsets = torch.empty(E + 1, dtype=torch.int32, **e)
         self.row_src = torch.empty(n, dtype=torch.int32, **e)
         self.inv = torch.empty(n, dtype=torch.int32, **e)
-        self.xd = torch.empty(n, H, dtype=cfg.torch_dtype, **e)
+        # moe_forward's choice: gather x rows in the gate/up GEMM for
+        # decode-sized batches, else materialise x_dispatched.
+        self.gather = n <= 8 * E
+        self.xd = None if self.gather else torch.empty(n, H, dtype=cfg.torch_dtype, **e)
         self.h = torch.empty(n, I, dtype=cfg.torch_dtype, **e)
         self.yd = torch.empty(n, H, dtype=cfg.torch_dtype, **e)
         self.out = torch.empty(T, H, dtype=cfg.torch_dtype, **e)
@@ -191,7 +194,9 @@ class Chain:
         self.grouped = (None if bias is None else bias.to(self.dev), opts)
 
     def step(self, stream, ev=None):
-        """route | dispatch | gate/up GEMM | down GEMM | combine, events between."""
+        """route | dispatch | gate/up GEMM | down GEMM | combine, events between:
+        the calls moe_forward makes (x rows gathered in the gate/up GEMM for
+        decode-sized batches, else through x_dispatched)."""
         c, lib, P = self.cfg, self.lib, self.moe._ptr
         s = ctypes.c_void_p(stream.cuda_stream)
         T, k, E, H = c.T, c.top_k, c.E, c.H
@@ -206,11 +211,19 @@ class Chain:
             rc |= lib.moe_route_sigmoid_grouped(P(self.d["logits"]), self.dt, T, E, P(bias), ctypes.byref(opts),
                                                 P(self.idx), P(self.w), None, s)
         rec(1)
-        rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts), P(self.offsets),
-                               P(self.row_src), P(self.inv), P(self.xd), P(self.dws), self.dws.numel(), s)
-        rec(2)
-        rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h), P(self.sws),
-                                      self.sws.numel(), s)
+        if self.gather:
+            rc |= lib.moe_dispatch(P(self.idx), T, E, k, None, self.dt, H, P(self.counts), P(self.offsets),
+                                   P(self.row_src), P(self.inv), None, P(self.dws), self.dws.numel(), s)
+            rec(2)
+            rc |= lib.moe_experts_gate_up_gather(self.ex.handle, P(self.d["x"]), T, P(self.row_src), k,
+                                                 P(self.offsets), T * k, P(self.h), P(self.sws), self.sws.numel(), s)
+        else:
+            rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts),
+                                   P(self.offsets), P(self.row_src), P(self.inv), P(self.xd), P(self.dws),
+                                   self.dws.numel(), s)
+            rec(2)
+            rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h),
+                                          P(self.sws), self.sws.numel(), s)
         rec(3)
         rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), P(self.sws),
                                    self.sws.numel(), s)
@@ -435,7 +448,7 @@ def run_ours(args, rank, world, local_rank):
         "route_dispatch_us": {"route": round(t_route * 1e6, 2), "dispatch": round(t_disp * 1e6, 2),
                               "total": round((t_route + t_disp) * 1e6, 2)},
         "combine_us": round(t_comb * 1e6, 2),
-        "timing": {"value": f"{args.steps} CUDA-graph replays of the step (its 8 kernels and 2 memsets), "
+        "timing": {"value": f"{args.steps} CUDA-graph replays of the step (its {KERNELS_PER_STEP} kernels and 2 memsets), "
                             "one event pair around each replay",
                    "stages": f"{stage_steps} steps launched directly with events between the stages "
                              f"({stage_total / stage_steps * 1e6:.1f} us per step including the events)"},

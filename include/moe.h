@@ -215,6 +215,25 @@ moe_status moe_experts_down(const moe_experts* experts, const void* h, const uin
                             void* stream);
 
 /*
+ * moe_experts_gate_up_gather - the gate/up stage reading each dispatched row
+ * straight from x: row r is x[row_src[r] / top_k] (row_src from
+ * moe_dispatch), so no x_dispatched copy is needed. This is the stage
+ * moe_forward runs; the pages have no separate entry for it (their split API
+ * materialises x_dispatched). h is bit-identical to moe_experts_gate_up on
+ * the x_dispatched that moe_dispatch would write.
+ *
+ *   x         device, [T, H] in the experts' dtype (16-byte aligned for F16/BF16).
+ *   row_src   device, [rows] uint32 from moe_dispatch; an entry >= T * top_k
+ *             reads as a zero row.
+ *   top_k     >= 1; rows <= T * top_k.
+ *   offsets, rows, h, workspace   as in moe_experts_gate_up.
+ */
+moe_status moe_experts_gate_up_gather(const moe_experts* experts, const void* x, int64_t T,
+                                      const uint32_t* row_src, int32_t top_k, const uint32_t* offsets,
+                                      int64_t rows, void* h, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/*
  * moe_combine - restore token order and take the routing-weighted sum
  * (DispatchedTokens::combine; ruDNN user guide section 6: combine uses the
  * dispatch mapping to restore token order and merges the expert outputs with
@@ -248,7 +267,9 @@ moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t
  *
  * Same numerics as calling moe_route, moe_dispatch,
  * moe_experts_forward_dispatched and moe_combine in turn: the outputs are
- * bit-identical to that sequence.
+ * bit-identical to that sequence. For decode-sized batches (T * top_k <=
+ * 8 * E) it dispatches the maps only and runs the gate/up stage as
+ * moe_experts_gate_up_gather, so x_dispatched is never written.
  */
 size_t moe_forward_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k);
 moe_status moe_forward(const moe_experts* experts, const void* x, const void* logits,

@@ -58,6 +58,7 @@ SIGNATURES = {
     "moe_experts_forward_dispatched": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
     "moe_experts_gate_up": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
     "moe_experts_down": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
+    "moe_experts_gate_up_gather": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _P, _I64, _P, _P, _SZ, _P]),
     "moe_combine": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _I64, _I32, _I64, _P, _P]),
     "moe_forward_workspace_size": (_SZ, [_P, _I64, _I32]),
     "moe_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -261,6 +262,23 @@ def moe_experts_gate_up(experts: Experts, x_dispatched: torch.Tensor, offsets: t
     ws = _workspace(STAGE_WORKSPACE_BYTES, x_dispatched.device, workspace)
     _check(lib.moe_experts_gate_up(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows, _ptr(h),
                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return h
+
+
+def moe_experts_gate_up_gather(experts: Experts, x: torch.Tensor, row_src: torch.Tensor, top_k: int,
+                               offsets: torch.Tensor, rows: int | None = None, out=None, workspace=None,
+                               stream=None):
+    """Gate/up stage reading dispatched row r from x[row_src[r] // top_k]:
+    h [rows, I] without an x_dispatched copy (rows defaults to row_src's length)."""
+    lib = load_library()
+    _dev_tensor(x, "x")
+    _dev_tensor(row_src, "row_src")
+    T = x.shape[0]
+    rows = row_src.shape[0] if rows is None else rows
+    h = out if out is not None else torch.empty(rows, experts.I, dtype=experts.dtype, device=x.device)
+    ws = _workspace(STAGE_WORKSPACE_BYTES, x.device, workspace)
+    _check(lib.moe_experts_gate_up_gather(experts.handle, _ptr(x), T, _ptr(row_src), top_k, _ptr(offsets), rows,
+                                          _ptr(h), _ptr(ws), ws.numel(), _stream(stream)))
     return h
 
 

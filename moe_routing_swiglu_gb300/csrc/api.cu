@@ -119,7 +119,7 @@ ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
   L.inv = take(n * 4);
   L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
   L.sched = take(moe::TC_SCHED_BYTES);
-  L.xd = take(n * static_cast<size_t>(ex->H) * es);
+  L.xd = take(moe::forward_gathers_rows(static_cast<int64_t>(n), ex->E) ? 0 : n * static_cast<size_t>(ex->H) * es);
   L.h = take(n * static_cast<size_t>(ex->I) * es);
   L.yd = take(n * static_cast<size_t>(ex->H) * es);
   L.total = off;
@@ -135,20 +135,21 @@ moe_status check_current_device(const moe_experts* ex) {
   return MOE_OK;
 }
 
-// One expert GEMM stage: gate_up (x_dispatched -> h) or down (h -> y).
-moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const uint32_t* offsets,
-                     int64_t rows, void* out, void* sched, cudaStream_t s) {
+// One expert GEMM stage: gate_up (x_dispatched, or x gathered through
+// row_src, -> h) or down (h -> y).
+moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const moe::TcGather* gather,
+                     const uint32_t* offsets, int64_t rows, void* out, void* sched, cudaStream_t s) {
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32) {
-    err = moe::launch_experts_simt_f32(gate_up, static_cast<const float*>(a), offsets,
+    err = moe::launch_experts_simt_f32(gate_up, static_cast<const float*>(a), gather, offsets,
                                        static_cast<int>(ex->E), rows,
                                        static_cast<const float*>(gate_up ? ex->gate : ex->down),
                                        static_cast<const float*>(gate_up ? ex->up : nullptr), ex->H,
                                        ex->I, static_cast<float*>(out), s);
   } else {
-    err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, offsets, static_cast<int>(ex->E), rows,
-                                 ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why);
+    err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, gather, offsets, static_cast<int>(ex->E),
+                                 rows, ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why);
   }
   if (err != cudaSuccess) return cuda_fail(err, gate_up ? "gate/up GEMM launch" : "down GEMM launch", why);
   return MOE_OK;
@@ -156,9 +157,9 @@ moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const u
 
 moe_status run_experts(const moe_experts* ex, const void* xd, const uint32_t* offsets, int64_t rows,
                        void* h, void* y, void* sched, cudaStream_t s) {
-  moe_status st = run_stage(ex, true, xd, offsets, rows, h, sched, s);
+  moe_status st = run_stage(ex, true, xd, nullptr, offsets, rows, h, sched, s);
   if (st != MOE_OK) return st;
-  return run_stage(ex, false, h, offsets, rows, y, sched, s);
+  return run_stage(ex, false, h, nullptr, offsets, rows, y, sched, s);
 }
 
 moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t* offsets, int64_t rows,
@@ -197,17 +198,25 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   uint32_t* offsets = reinterpret_cast<uint32_t*>(ws + L.offsets);
   uint32_t* row_src = reinterpret_cast<uint32_t*>(ws + L.row_src);
   uint32_t* inv = reinterpret_cast<uint32_t*>(ws + L.inv);
-  void* xd = ws + L.xd;
   void* h = ws + L.h;
   void* yd = ws + L.yd;
   const int64_t rows = T * top_k;
+  const bool gather_rows = moe::forward_gathers_rows(rows, ex->E);
+  void* xd = gather_rows ? nullptr : ws + L.xd;
 
+  // Decode-sized batches: dispatch writes the maps only and the gate/up GEMM
+  // reads each dispatched row straight from x through row_src. Larger
+  // batches: dispatch also writes x_dispatched, which the GEMM streams with
+  // TMA (faster there than gathering rows from every weight tile).
   cudaError_t err = route(indices, weights, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
-  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, x, ex->dtype, ex->H, counts,
-                             offsets, row_src, inv, xd, ws + L.scratch, s);
+  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
+                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
-  st = run_experts(ex, xd, offsets, rows, h, yd, ws + L.sched, s);
+  const moe::TcGather gather{x, row_src, top_k, T};
+  st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, ws + L.sched, s);
+  if (st != MOE_OK) return st;
+  st = run_stage(ex, false, h, nullptr, offsets, rows, yd, ws + L.sched, s);
   if (st != MOE_OK) return st;
   err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward combine launch");
@@ -389,7 +398,21 @@ moe_status moe_experts_gate_up(const moe_experts* ex, const void* x_dispatched,
   moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, h, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
-  st = run_stage(ex, true, x_dispatched, offsets, rows, h, workspace, static_cast<cudaStream_t>(stream));
+  st = run_stage(ex, true, x_dispatched, nullptr, offsets, rows, h, workspace, static_cast<cudaStream_t>(stream));
+  return st != MOE_OK ? st : ok();
+}
+
+moe_status moe_experts_gate_up_gather(const moe_experts* ex, const void* x, int64_t T, const uint32_t* row_src,
+                                      int32_t top_k, const uint32_t* offsets, int64_t rows, void* h,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_stage_args(ex, x, offsets, rows, h, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (top_k < 1 || T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "need top_k >= 1, T >= 0, T*top_k < 2^32-1");
+  if (rows > T * top_k) return fail(MOE_ERR_SHAPE, "rows must not exceed T * top_k");
+  if (rows > 0 && row_src == nullptr) return fail(MOE_ERR_NULL, "row_src must be non-NULL");
+  if (rows == 0) return ok();
+  const moe::TcGather gather{x, row_src, top_k, T};
+  st = run_stage(ex, true, nullptr, &gather, offsets, rows, h, workspace, static_cast<cudaStream_t>(stream));
   return st != MOE_OK ? st : ok();
 }
 
@@ -398,7 +421,7 @@ moe_status moe_experts_down(const moe_experts* ex, const void* h, const uint32_t
   moe_status st = check_stage_args(ex, h, offsets, rows, y_dispatched, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
-  st = run_stage(ex, false, h, offsets, rows, y_dispatched, workspace, static_cast<cudaStream_t>(stream));
+  st = run_stage(ex, false, h, nullptr, offsets, rows, y_dispatched, workspace, static_cast<cudaStream_t>(stream));
   return st != MOE_OK ? st : ok();
 }
 

@@ -15,11 +15,13 @@ namespace {
 
 constexpr int SB_M = 64, SB_N = 64, SB_K = 16, SB_THREADS = 256;
 
+// Gather mode (gate/up only, row_src != nullptr): row r of the A operand is
+// a[(row_src[r] / top_k) * K ...], the token's row of x.
 template <bool GATE_UP>
 __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
-    const float* __restrict__ a, const uint32_t* __restrict__ offsets, int E,
-    const float* __restrict__ w0, const float* __restrict__ w1, int64_t K, int64_t N,
-    int64_t rows_total, float* __restrict__ out) {
+    const float* __restrict__ a, const uint32_t* __restrict__ row_src, int top_k, int64_t a_rows,
+    const uint32_t* __restrict__ offsets, int E, const float* __restrict__ w0, const float* __restrict__ w1,
+    int64_t K, int64_t N, int64_t rows_total, float* __restrict__ out) {
   __shared__ uint32_t tile_start[ROUTE_MAX_E + 1];
   __shared__ float As[SB_K][SB_M + 4];
   __shared__ float B0s[SB_K][SB_N + 4];
@@ -46,12 +48,18 @@ __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
 
   const int lr = threadIdx.x / 4;        // 0..63: row of the A / B tile this thread loads
   const int lk = (threadIdx.x % 4) * 4;  // 0,4,8,12: first k of its 4 loads
+  const float* a_row = nullptr;          // this thread's A row, or nullptr for zeros
+  if (lr < tc.rows) {
+    int64_t src = static_cast<int64_t>(tc.row0) + lr;
+    if (row_src != nullptr) src = row_src[src] / static_cast<uint32_t>(top_k);
+    if (src < a_rows) a_row = a + src * K;
+  }
   for (int64_t k0 = 0; k0 < K; k0 += SB_K) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int64_t kk = k0 + lk + q;
       const bool kin = kk < K;
-      As[lk + q][lr] = (kin && lr < tc.rows) ? a[(static_cast<int64_t>(tc.row0) + lr) * K + kk] : 0.0f;
+      As[lk + q][lr] = (kin && a_row != nullptr) ? a_row[kk] : 0.0f;
       const int64_t n = n0 + lr;
       B0s[lk + q][lr] = (kin && n < N) ? wg[n * K + kk] : 0.0f;
       if constexpr (GATE_UP) B1s[lk + q][lr] = (kin && n < N) ? wu[n * K + kk] : 0.0f;
@@ -101,18 +109,23 @@ int64_t tile_bound(int64_t rows, int E, int bm, int64_t n_tiles) {
 
 }  // namespace
 
-cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const uint32_t* offsets, int E,
-                                    int64_t rows, const float* w0, const float* w1, int64_t H,
-                                    int64_t I, float* out, cudaStream_t stream) {
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather,
+                                    const uint32_t* offsets, int E, int64_t rows, const float* w0,
+                                    const float* w1, int64_t H, int64_t I, float* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
+  if (gather != nullptr && !gate_up) return cudaErrorInvalidValue;
+  const float* src = gather != nullptr ? static_cast<const float*>(gather->x) : a;
+  const uint32_t* row_src = gather != nullptr ? gather->row_src : nullptr;
+  const int top_k = gather != nullptr ? gather->top_k : 1;
+  const int64_t a_rows = gather != nullptr ? gather->x_rows : rows;
   if (gate_up) {
     const int64_t g = tile_bound(rows, E, SB_M, (I + SB_N - 1) / SB_N);
     experts_simt_kernel<true><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        a, offsets, E, w0, w1, H, I, rows, out);
+        src, row_src, top_k, a_rows, offsets, E, w0, w1, H, I, rows, out);
   } else {
     const int64_t g = tile_bound(rows, E, SB_M, (H + SB_N - 1) / SB_N);
     experts_simt_kernel<false><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        a, offsets, E, w0, nullptr, I, H, rows, out);
+        a, nullptr, 1, rows, offsets, E, w0, nullptr, I, H, rows, out);
   }
   return cudaGetLastError();
 }

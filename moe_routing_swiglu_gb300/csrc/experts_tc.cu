@@ -69,7 +69,10 @@ constexpr int ROW_BYTES = BK * 2;             // 128 B per row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;       // 16 KB per weight tile
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
+constexpr int NUM_LOAD_WARPS = 4;             // token-row loaders of the gather mode
+constexpr int FIRST_LOAD_WARP = 2 + NUM_EPI_WARPS;
+template <bool GATHER>
+constexpr int num_threads() { return 32 * (2 + NUM_EPI_WARPS + (GATHER ? NUM_LOAD_WARPS : 0)); }
 constexpr int XPOSE_BYTES = 32 * 32 * 2;      // per-warp transpose buffer
 constexpr int STAGE_SMEM = 192 * 1024;        // shared memory given to pipeline stages
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
@@ -113,6 +116,7 @@ constexpr uint32_t ST_EPI_TMEM_FULL = 0x14;
 constexpr uint32_t ST_MMA_DRAIN = 0x15;
 constexpr uint32_t ST_PRODUCER_DRAIN = 0x16;
 constexpr uint32_t ST_TILE_RING = 0x17;
+constexpr uint32_t ST_LOADER_EMPTY = 0x18;
 constexpr uint32_t ST_SELFTEST = 0x100;
 
 struct TcArgs {
@@ -126,6 +130,12 @@ struct TcArgs {
   uint32_t rows_total;      // rows of the token and output matrices
   uint32_t tile_cap;        // host bound on the tile count
   uint32_t* status;
+  // Gather mode (K3 only): token row r of a tile is x[row_src[r] / top_k].
+  const uint8_t* gx;        // x [x_rows, K], 16-bit, rows of k_bytes
+  const uint32_t* row_src;  // [rows_total]
+  int top_k;
+  uint32_t x_rows;
+  int k_bytes;              // K * 2
 };
 
 // SiLU(g) = g * sigmoid(g), sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
@@ -138,8 +148,8 @@ __device__ __forceinline__ float silu_f32(float g) {
 
 // Tensor maps: a0/a1 weight tiles (128-row boxes: K3 gate/up, K4 down rows
 // n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes.
-template <typename T, bool GATE_UP, int TBM>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <typename T, bool GATE_UP, int TBM, bool GATHER>
+__global__ void __launch_bounds__(num_threads<GATHER>(), 1)
     experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
                       const __grid_constant__ CUtensorMap tm_b128,
@@ -167,12 +177,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // Gather mode: the producer's expect_tx arrival plus one cp.async
+      // arrival per loader thread.
+      mbar_init(&full[s], GATHER ? 1 + 32 * NUM_LOAD_WARPS : 1);
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < RING; ++r) {
       mbar_init(&tile_full[r], 1);
-      mbar_init(&tile_empty[r], NUM_EPI_WARPS);
+      mbar_init(&tile_empty[r], NUM_EPI_WARPS + (GATHER ? NUM_LOAD_WARPS : 0));
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int n_tok = (tc.rows + 15) & ~15;        // N of this tile
         const int n128 = n_tok >> 7;                   // 128-row boxes
         const int n16 = (n_tok & 127) >> 4;            // then 16-row boxes
-        const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + n_tok * ROW_BYTES);
+        const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + (GATHER ? 0 : n_tok * ROW_BYTES));
         const int wrow0 = GATE_UP ? tc.n * BM : tc.n * (2 * BM);
         const int wrow1 = GATE_UP ? tc.n * BM : tc.n * (2 * BM) + BM;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -237,12 +249,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_3d(st, &tm_a0, &full[stage], k0, wrow0, tc.e);
           tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], k0, wrow1, tc.e);
-          uint8_t* b_dst = st + 2 * A_BYTES;
-          int r = 0;
-          for (int b = 0; b < n128; ++b, r += 128)
-            tma_load_2d(b_dst + r * ROW_BYTES, &tm_b128, &full[stage], k0, static_cast<int>(tc.row0) + r);
-          for (int b = 0; b < n16; ++b, r += 16)
-            tma_load_2d(b_dst + r * ROW_BYTES, &tm_b16, &full[stage], k0, static_cast<int>(tc.row0) + r);
+          if (!GATHER) {
+            uint8_t* b_dst = st + 2 * A_BYTES;
+            int r = 0;
+            for (int b = 0; b < n128; ++b, r += 128)
+              tma_load_2d(b_dst + r * ROW_BYTES, &tm_b128, &full[stage], k0, static_cast<int>(tc.row0) + r);
+            for (int b = 0; b < n16; ++b, r += 16)
+              tma_load_2d(b_dst + r * ROW_BYTES, &tm_b16, &full[stage], k0, static_cast<int>(tc.row0) + r);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -296,6 +310,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
+          // Token rows written by the loaders' cp.async (generic proxy) are
+          // read by the tensor cores (async proxy).
+          if (GATHER) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + C::SMEM_STAGES + stage * STAGE_BYTES);
           const uint32_t a1 = a0 + A_BYTES;
@@ -321,7 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait_bounded(drain, 0, nullptr, args.status, ST_MMA_DRAIN, WAIT_LIMIT_NS);
     }
     __syncwarp();
-  } else {
+  } else if (warp < FIRST_LOAD_WARP) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                    // 0..7
     const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
@@ -390,6 +407,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(&tile_empty[slot]);
       }
     }
+  } else if (GATHER) {
+    // ------------------------------------------------------------ token-row loaders (gather mode)
+    // Row r of a tile's token block is x[row_src[row0 + r] / top_k]. In each
+    // copy instruction lanes 8i..8i+7 move the eight 16-byte chunks of one
+    // 128-byte row slice (four whole rows per instruction), each chunk to its
+    // 128-byte-swizzle position (chunk ^ (row & 7)), the layout a TMA copy
+    // with 128-byte swizzle produces. Rows past the tile's rows up to its
+    // 16-row N are zero-filled.
+    constexpr int RPT = TBM / (4 * NUM_LOAD_WARPS);  // rows per thread per stage
+    const int lw = warp - FIRST_LOAD_WARP;
+    const int q = lane & 7;
+    const int rsub = lw * 4 + (lane >> 3);           // row = rsub + 16 * j
+    int stage = 0;
+    uint32_t phase = 0;
+    for (uint32_t it = 0;; ++it) {
+      const uint32_t slot = it % RING;
+      bool ok = mbar_wait_bounded(&tile_full[slot], (it / RING) & 1u, abort_flag, args.status,
+                                  ST_TILE_RING, WAIT_LIMIT_NS);
+      const uint32_t tile = ok ? static_cast<uint32_t>(ring[slot]) : static_cast<uint32_t>(TILE_END);
+      if (!__all_sync(FULL_MASK, ok) || tile == TILE_END) break;
+      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+      const int n_tok = (tc.rows + 15) & ~15;
+      const uint8_t* src[RPT];
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) {
+        const int r = rsub + 16 * j;
+        src[j] = nullptr;
+        if (r < tc.rows && tc.row0 + static_cast<uint32_t>(r) < args.rows_total) {
+          const uint32_t tok = args.row_src[tc.row0 + r] / static_cast<uint32_t>(args.top_k);
+          if (tok < args.x_rows) src[j] = args.gx + static_cast<int64_t>(tok) * args.k_bytes;
+        }
+      }
+      for (int kb = 0; kb < args.k_blocks; ++kb) {
+        ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status, ST_LOADER_EMPTY,
+                               WAIT_LIMIT_NS);
+        if (!__all_sync(FULL_MASK, ok)) break;
+        const uint32_t b = smem_u32(smem + C::SMEM_STAGES + stage * STAGE_BYTES + 2 * A_BYTES);
+        const int kbyte = kb * (BK * 2) + q * 16;
+        const bool kin = kbyte < args.k_bytes;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+          const int r = rsub + 16 * j;
+          if (r < n_tok) {
+            const uint32_t dst = b + static_cast<uint32_t>(r * ROW_BYTES + ((q ^ (r & 7)) << 4));
+            if (src[j] != nullptr && kin) cp_async_16(dst, src[j] + kbyte, 16);
+            else cp_async_16(dst, args.gx, 0);
+          }
+        }
+        cp_async_mbar_arrive_noinc(&full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tile_empty[slot]);
+    }
+    // No copy may land after the block has exited.
+    cp_async_wait_all();
   }
 
   tc_fence_before();
@@ -466,10 +543,10 @@ int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks, int tbm) {
   return t_blocks * n_wblocks;
 }
 
-template <typename T, bool GATE_UP, int TBM>
+template <typename T, bool GATE_UP, int TBM, bool GATHER = false>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b128,
                        const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream) {
-  auto kern = experts_tc_kernel<T, GATE_UP, TBM>;
+  auto kern = experts_tc_kernel<T, GATE_UP, TBM, GATHER>;
   constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -477,23 +554,26 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
   if (grid <= 0) return cudaSuccess;
   err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
   if (err != cudaSuccess) return err;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a0, a1, b128, b16, args);
+  kern<<<grid, num_threads<GATHER>(), SMEM_BYTES, stream>>>(a0, a1, b128, b16, args);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                         const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                         void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
+                         const TcGather* gather, const uint32_t* offsets, int E, int64_t rows, int64_t H,
+                         int64_t I, void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
                          const char** why) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
   if (err != cudaSuccess) return err;
   const int64_t K = gate_up ? H : I;
   const int64_t n_out = gate_up ? I : H;
-  CUtensorMap t128, t16;
-  if (!encode_2d(&t128, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 128) ||
-      !encode_2d(&t16, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 16)) {
+  // Token maps over the dense rows; the gather mode loads rows itself and
+  // passes the weight maps in their place (never dereferenced there).
+  CUtensorMap t128 = w.gate, t16 = w.gate;
+  if (gather == nullptr &&
+      (!encode_2d(&t128, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 128) ||
+       !encode_2d(&t16, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 16))) {
     *why = "cuTensorMapEncodeTiled rejected the token tensor map";
     return cudaErrorInvalidValue;
   }
@@ -505,7 +585,20 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   const bool small = rows <= 8 * static_cast<int64_t>(E);
   const int64_t cap = tile_bound(rows, E, nw, small ? 32 : 256);
   TcArgs args{offsets, out, sched, E, nw, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
-              static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status};
+              static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status,
+              nullptr, nullptr, 1, 0, static_cast<int>(K * 2)};
+  if (gather != nullptr) {
+    if (!gate_up) {
+      *why = "the gather mode applies to the gate/up stage only";
+      return cudaErrorInvalidValue;
+    }
+    args.gx = static_cast<const uint8_t*>(gather->x);
+    args.row_src = gather->row_src;
+    args.top_k = gather->top_k;
+    args.x_rows = static_cast<uint32_t>(gather->x_rows);
+    if (small) return launch_one<T, true, 32, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
+    return launch_one<T, true, 256, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
+  }
   if (small) {
     if (gate_up) return launch_one<T, true, 32>(w.gate, w.up, t128, t16, args, num_sms, stream);
     return launch_one<T, false, 32>(w.down, w.down, t128, t16, args, num_sms, stream);
@@ -531,14 +624,15 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
 }
 
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                              const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
-                              const char** why) {
+                              const TcGather* gather, const uint32_t* offsets, int E, int64_t rows,
+                              int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
+                              cudaStream_t stream, const char** why) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
-    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, sched, num_sms,
-                                       stream, why);
-  return launch_stage<__half>(w, dtype, gate_up, a, offsets, E, rows, H, I, out, sched, num_sms, stream, why);
+    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, gather, offsets, E, rows, H, I, out, sched,
+                                       num_sms, stream, why);
+  return launch_stage<__half>(w, dtype, gate_up, a, gather, offsets, E, rows, H, I, out, sched, num_sms,
+                              stream, why);
 }
 
 cudaError_t read_device_status(uint32_t* code, bool clear) {

@@ -51,9 +51,17 @@ cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint
 
 // ---- K7 FP32 experts on CUDA cores (experts_simt.cu). gate_up: a = x_dispatched
 // [rows, H], w0/w1 = gate/up, out = h [rows, I]; else a = h, w0 = down, out = y [rows, H].
-cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const uint32_t* offsets, int E,
-                                    int64_t rows, const float* w0, const float* w1, int64_t H,
-                                    int64_t I, float* out, cudaStream_t stream);
+// Gather mode of the gate/up stage (both expert paths): dispatched row r reads x[row_src[r] / top_k]
+// instead of row r of a materialised x_dispatched.
+struct TcGather {
+  const void* x;            // [x_rows, H]
+  const uint32_t* row_src;  // [rows]
+  int top_k;
+  int64_t x_rows;
+};
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather,
+                                    const uint32_t* offsets, int E, int64_t rows, const float* w0,
+                                    const float* w1, int64_t H, int64_t I, float* out, cudaStream_t stream);
 
 // ---- K3/K4 F16/BF16 experts on tcgen05 tensor cores (experts_tc.cu)
 struct TcWeights {
@@ -61,13 +69,18 @@ struct TcWeights {
 };
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,
                        int64_t E, int64_t H, int64_t I, TcWeights* out, const char** why);
-// gate_up: K3, a = x_dispatched [rows, H] -> out = h [rows, I]; else K4, a = h -> out = y [rows, H].
+// moe_forward gathers x rows in the gate/up stage for decode-sized batches
+// (at most 8 dispatched rows per expert on average, where the 32-token tiles
+// run) and materialises x_dispatched for larger ones.
+inline bool forward_gathers_rows(int64_t rows, int64_t E) { return rows <= 8 * E; }
+// gate_up: K3, a = x_dispatched [rows, H] (or gather != NULL) -> out = h [rows, I];
+// else K4, a = h -> out = y [rows, H].
 // sched: one uint32 of device memory for the tile counter (zeroed on the stream before the launch).
 constexpr size_t TC_SCHED_BYTES = 256;
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                              const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I,
-                              void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
-                              const char** why);
+                              const TcGather* gather, const uint32_t* offsets, int E, int64_t rows,
+                              int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
+                              cudaStream_t stream, const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 

@@ -5,7 +5,8 @@
 The inputs are the seeded synthetic workloads of ``workloads.py``; routing and
 dispatch run once to set up the stage's inputs, then the chosen stage runs
 ``--reps`` times back to back (stream-ordered) and the device is synchronised.
-Stages: route, dispatch, gate_up, down, combine, forward (moe_forward), and
+Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
+row_src), down, combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
 variant in ``workloads.GROUPED``).
 """
@@ -32,7 +33,8 @@ def main(argv=None):
     names.update(workloads.SMALL_CONFIGS)
     ap.add_argument("--workload", default="cfg2", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "gate_up", "down", "combine", "forward", "route_grouped"])
+                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "combine", "forward",
+                             "route_grouped"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     cfg = names[args.workload]
@@ -62,6 +64,8 @@ def main(argv=None):
             moe.moe_dispatch(idx, cfg.E, d["x"])
         elif args.stage == "gate_up":
             moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h)
+        elif args.stage == "gate_up_gather":
+            moe.moe_experts_gate_up_gather(ex, d["x"], disp.row_src, cfg.top_k, disp.offsets, out=h)
         elif args.stage == "down":
             moe.moe_experts_down(ex, h, disp.offsets, out=y)
         elif args.stage == "route_grouped":

@@ -168,6 +168,18 @@ def test_grouped_forward_rejects_bad_arguments(lib):
                                            None) == 1
 
 
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(ex=None), 1), (dict(offsets=None), 1), (dict(x=None), 1), (dict(ws=None), 6), (dict(ws=P(0x200010)), 5),
+])
+def test_gate_up_gather_rejects_bad_arguments(lib, kwargs, status):
+    """Checks that run before the handle is read (the rest need a real handle
+    and run in the GPU tests)."""
+    a = dict(ex=FAKE, x=FAKE, T=4, row_src=FAKE, k=2, offsets=FAKE, rows=8, h=FAKE, ws=P(0x200000))
+    a.update(kwargs)
+    assert lib.moe_experts_gate_up_gather(a["ex"], a["x"], a["T"], a["row_src"], a["k"], a["offsets"], a["rows"],
+                                          a["h"], a["ws"], 1 << 10, None) == status
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.moe_selftest_bounded_wait(0, None) == 2
     assert lib.moe_selftest_bounded_wait(10_000_001, None) == 2

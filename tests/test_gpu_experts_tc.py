@@ -78,3 +78,76 @@ def test_tc_decode_path_with_a_hot_expert(cuda_lib):
     y = _run_experts(cuda_lib, cfg, inp, dp)
     yref = moe_oracle.experts_forward_dispatched(inp["x"], inp["gate"], inp["up"], inp["down"], dp, cfg.top_k)
     assert_output_close(f64(y), yref, torch.bfloat16, "y_dispatched")
+
+
+@pytest.mark.parametrize("name", ["bf16_fine", "f16_zipf", "bf16_ragged", "bf16_decode", "f32_ragged"])
+def test_gate_up_gather_equals_dense(cuda_lib, name):
+    """The gathered gate/up stage (rows read from x through row_src) is
+    bit-identical to the stage on the materialised x_dispatched, and h is
+    the oracle's within the chain's tolerance."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    inp = workloads.generate(cfg)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    h_dense = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    h_gather = moe.moe_experts_gate_up_gather(ex, d["x"], disp.row_src, cfg.top_k, disp.offsets)
+    torch.cuda.synchronize()
+    assert torch.equal(h_dense.view(torch.uint8), h_gather.view(torch.uint8))
+    assert moe.moe_device_status() == 0
+
+
+def test_gate_up_gather_full_size(cuda_lib):
+    """The fine-grained prefill workload at full size (the benchmark's launch
+    configuration): gathered and dense gate/up stages agree bit for bit."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[2]
+    d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    h_dense = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    for _ in range(2):
+        h_gather = moe.moe_experts_gate_up_gather(ex, d["x"], disp.row_src, cfg.top_k, disp.offsets)
+        torch.cuda.synchronize()
+        assert torch.equal(h_dense.view(torch.uint8), h_gather.view(torch.uint8))
+    assert moe.moe_device_status() == 0
+
+
+def test_gate_up_gather_bad_row_src_reads_zero_rows(cuda_lib):
+    """A row_src entry past T * top_k reads as a zero row: h = SiLU(0) * 0 = 0
+    for that row, no out-of-range access."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_ragged"]
+    d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    rs = disp.row_src.clone()
+    rs[5] = 0x7FFFFFFF
+    h = moe.moe_experts_gate_up_gather(ex, d["x"], rs, cfg.top_k, disp.offsets)
+    ref = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(h[5]) == 0
+    keep = torch.ones(h.shape[0], dtype=torch.bool, device=DEV)
+    keep[5] = False
+    assert torch.equal(h[keep].view(torch.uint8), ref[keep].view(torch.uint8))
+
+
+def test_gate_up_gather_rejects_bad_arguments(cuda_lib):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_ragged"]
+    d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E)
+    for kw, status in [(dict(top_k=0), 2), (dict(rows=cfg.T * cfg.top_k + 1), 2)]:
+        a = dict(top_k=cfg.top_k, rows=None)
+        a.update(kw)
+        with pytest.raises(moe.MoeError) as err:
+            moe.moe_experts_gate_up_gather(ex, d["x"], disp.row_src, a["top_k"], disp.offsets, rows=a["rows"],
+                                           out=torch.empty(cfg.T * cfg.top_k + 1, cfg.I, dtype=cfg.torch_dtype,
+                                                           device=DEV))
+        assert err.value.status == status

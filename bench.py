@@ -19,7 +19,9 @@ Printed (rank 0, one JSON line): tokens/s, grouped-GEMM TFLOP/s against the
 measured BF16 peak, route+dispatch microseconds, the decode workload's HBM
 GB/s over the touched expert weights, the roofline of the dominant kernel,
 the end-to-end number through moe_forward with host buffers, the CPU oracle
-baseline, kernel launches and the SM clocks seen during the run. A second,
+baseline, kernel launches and the SM clocks seen during the run, and the
+grouped-GEMM TFLOP/s of the coarse BF16 and Zipf-skewed F16 prefill
+workloads (the two GEMM stages timed on their own). A second,
 shorter run of the same chain with the grouped sigmoid routing in place of
 the softmax routing reports its tokens/s and routing time.
 
@@ -245,12 +247,11 @@ class L2Flush:
 
     def __init__(self, dev):
         self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.r = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.acc = torch.empty((), dtype=torch.int64, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     def __call__(self):
         self.w.zero_()
-        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.acc)
+        torch.amax(self.r)  # a pure read (no converted copy), one small result
 
 
 def timed_steps(chain, stream, flush, steps, warmup):
@@ -340,6 +341,39 @@ def traffic_record(kernel_source: Path):
     return rec if rec.get("source_sha256") == sha else None
 
 
+def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
+    """Mean seconds of the gate/up and down GEMM stages on one workload
+    (routing and dispatch done once beforehand; L2 flushed before each
+    timed stage)."""
+    inp = workloads.generate(cfg)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    del inp
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    h = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    y = moe.moe_experts_down(ex, h, disp.offsets)
+    ws = torch.empty(moe.STAGE_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+    times = {"gate_up": [], "down": []}
+    for i in range(steps + 2):
+        for name in ("gate_up", "down"):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if name == "gate_up":
+                moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h, workspace=ws)
+            else:
+                moe.moe_experts_down(ex, h, disp.offsets, out=y, workspace=ws)
+            b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                times[name].append(a.elapsed_time(b) / 1e3)
+    assert moe.moe_device_status() == 0
+    del ex, d, h, y, disp
+    torch.cuda.empty_cache()
+    return float(np.mean(times["gate_up"])), float(np.mean(times["down"]))
+
+
 def cpu_baseline_prefill(inp, n_tokens=PREFILL.T):
     """The oracle, as it stands, on the first n_tokens of the prefill batch
     (by default the whole batch: a few seconds of CPU work on the host)."""
@@ -400,6 +434,15 @@ def run_ours(args, rank, world, local_rank):
     g_steps = min(args.steps, 200)
     g_stages, g_total = timed_steps(chain, stream, flush, g_steps, args.warmup)
     g_total = max_over_ranks(g_total, world, dev)
+    other_gemms = {}
+    for cid in (3, 5):
+        oc = workloads.CONFIGS[cid]
+        t_g, t_d = gemm_stage_times(moe, oc, dev, stream, flush, 5)
+        tf = oc.expert_flops / (t_g + t_d) / 1e12
+        peak = peaks["bf16_tflops"]  # F16 and BF16 share the dense tensor rate
+        other_gemms[oc.name] = {"tflops": round(tf, 1), "frac_peak": round(tf / peak, 4),
+                                "gate_up_us": round(t_g * 1e6, 1), "down_us": round(t_d * 1e6, 1),
+                                "flops": oc.expert_flops}
     clk = clocks.stop()
     assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
 
@@ -458,6 +501,7 @@ def run_ours(args, rank, world, local_rank):
                    "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),
                    "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
                    "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
+        "grouped_gemm_other_workloads": other_gemms,
         "sigmoid_grouped": {
             "workload": f"{c.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
                         f"{grouped_routing.selected_groups} selected, top-two group scores, scale "

@@ -22,3 +22,14 @@ from .moe_oracle import (  # noqa: F401
     silu,
     widen,
 )
+from .training import (  # noqa: F401
+    ExpertGrads,
+    RouterWeightOptions,
+    check_router_options,
+    combine_backward,
+    dispatch_backward,
+    experts_backward,
+    router_jacobian,
+    selected_router_backward,
+    selected_router_weights,
+)

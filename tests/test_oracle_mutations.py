@@ -166,3 +166,92 @@ def test_planted_routing_mistake_is_caught(name, monkeypatch):
         except Exception as exc:
             caught.append((pin.__name__, type(exc).__name__))
     assert caught, f"no pin catches the planted mistake {name!r}"
+
+
+# ---------------------------------------------------------------- training oracle
+from oracle import training as _training  # noqa: E402
+from tests.test_oracle_training_pins import TRAINING_PINS  # noqa: E402
+
+_jac = _training.router_jacobian
+_cb = _training.combine_backward
+_eb = _training.experts_backward
+_db = _training.dispatch_backward
+
+
+def _jac_without_softmax_cross_term(l64_row, idx_row, o):
+    if o.scoring != "softmax":
+        return _jac(l64_row, idx_row, o)
+    ex = np.exp(l64_row - l64_row.max())
+    P = ex / ex.sum()
+    J = np.zeros((idx_row.size, l64_row.size))
+    J[np.arange(idx_row.size), idx_row] = P[idx_row]        # drops -P_i P_m
+    if o.renormalize:
+        v = P[idx_row]
+        Z = v.sum()
+        J = (J * Z - np.outer(v, J.sum(axis=0))) / (Z * Z)
+    return J * float(o.scale)
+
+
+def _jac_ignoring_scale(l64_row, idx_row, o):
+    return _jac(l64_row, idx_row, dataclasses.replace(o, scale=1.0))
+
+
+def _jac_renorm_sign_flipped(l64_row, idx_row, o):
+    if not o.renormalize:
+        return _jac(l64_row, idx_row, o)
+    J0 = _jac(l64_row, idx_row, dataclasses.replace(o, renormalize=False, scale=1.0))
+    ex = np.exp(l64_row - l64_row.max())
+    P = ex / ex.sum() if o.scoring == "softmax" else 1 / (1 + np.exp(-l64_row))
+    v = P[idx_row]
+    Z = v.sum()
+    return (J0 * Z + np.outer(v, J0.sum(axis=0))) / (Z * Z) * float(o.scale)
+
+
+def _combine_backward_unweighted(y, inv, weights, grad_out, T, top_k):
+    return _cb(y, inv, np.ones_like(np.asarray(weights, dtype=np.float64)), grad_out, T, top_k)
+
+
+def _experts_backward_silu_for_derivative(x, gate, up, down, offsets, dexpert):
+    saved = _training._silu_grad
+    _training._silu_grad = _training._silu
+    try:
+        return _eb(x, gate, up, down, offsets, dexpert)
+    finally:
+        _training._silu_grad = saved
+
+
+def _experts_backward_swapped_gate_up(x, gate, up, down, offsets, dexpert):
+    g = _eb(x, up, gate, down, offsets, dexpert)
+    return _training.ExpertGrads(g.dx_dispatched, g.dup, g.dgate, g.ddown)
+
+
+def _dispatch_backward_mean(dinput, inv, T, top_k):
+    return _db(dinput, inv, T, top_k) / top_k
+
+
+TRAINING_MUTATIONS = {
+    "softmax_jacobian_without_cross_term": ("router_jacobian", _jac_without_softmax_cross_term),
+    "router_backward_ignores_scale": ("router_jacobian", _jac_ignoring_scale),
+    "renormalize_quotient_rule_sign": ("router_jacobian", _jac_renorm_sign_flipped),
+    "combine_backward_drops_weight": ("combine_backward", _combine_backward_unweighted),
+    "silu_used_for_its_derivative": ("experts_backward", _experts_backward_silu_for_derivative),
+    "gate_and_up_gradients_swapped": ("experts_backward", _experts_backward_swapped_gate_up),
+    "dispatch_backward_averages_slots": ("dispatch_backward", _dispatch_backward_mean),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TRAINING_MUTATIONS))
+def test_planted_training_mistake_is_caught(name, monkeypatch):
+    import oracle as pkg
+
+    attr, fn = TRAINING_MUTATIONS[name]
+    monkeypatch.setattr(_training, attr, fn)
+    if hasattr(pkg, attr):
+        monkeypatch.setattr(pkg, attr, fn)
+    caught = []
+    for pin in TRAINING_PINS:
+        try:
+            pin(pkg)
+        except Exception as exc:
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin catches the planted mistake {name!r}"

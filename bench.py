@@ -21,7 +21,9 @@ GB/s over the touched expert weights, the roofline of the dominant kernel,
 the end-to-end number through moe_forward with host buffers, the CPU oracle
 baseline, kernel launches and the SM clocks seen during the run, and the
 grouped-GEMM TFLOP/s of the coarse BF16 and Zipf-skewed F16 prefill
-workloads (the two GEMM stages timed on their own). A second,
+workloads (the two GEMM stages timed on their own), and one first-order
+training step (forward with the experts' cache, then combine, experts,
+dispatch and router backward) on the prefill workload. A second,
 shorter run of the same chain with the grouped sigmoid routing in place of
 the softmax routing reports its tokens/s and routing time.
 
@@ -374,6 +376,55 @@ def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
     return float(np.mean(times["gate_up"])), float(np.mean(times["down"]))
 
 
+def training_step_times(moe, cfg, dev, stream, flush, steps):
+    """One first-order training step on a workload (ruDNN user guide, section
+    12): forward (route, dispatch, training forward of the experts, combine)
+    then backward (combine backward, experts backward, dispatch backward,
+    router backward of the softmax weights). Returns mean seconds per stage
+    (forward, combine_backward, experts_backward, dispatch_backward,
+    router_backward)."""
+    inp = workloads.generate(cfg)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    del inp
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    g = torch.Generator().manual_seed(7)
+    grad_out = torch.randn(cfg.T, cfg.H, generator=g).to(cfg.torch_dtype).to(dev)
+    opts = moe.RouterWeightOptions("softmax", cfg.renormalize, 1.0)
+
+    def step(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        idx, w = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+        disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+        y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
+        moe.moe_combine(y, disp.inv, w)
+        rec(1)
+        dexp, dw = moe.moe_combine_backward(y, disp.inv, w, grad_out)
+        rec(2)
+        gr = moe.moe_experts_backward(ex, cache, dexp)
+        rec(3)
+        moe.moe_dispatch_backward(gr.dx_dispatched, disp.inv, cfg.T, cfg.top_k)
+        rec(4)
+        moe.moe_router_backward(d["logits"], idx, dw, opts)
+        rec(5)
+
+    for _ in range(2):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        step(ev)
+        torch.cuda.synchronize()
+        times.append([ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(5)])
+    assert moe.moe_device_status() == 0
+    del ex, d
+    torch.cuda.empty_cache()
+    return [float(x) for x in np.mean(np.array(times), axis=0)]
+
+
 def cpu_baseline_prefill(inp, n_tokens=PREFILL.T):
     """The oracle, as it stands, on the first n_tokens of the prefill batch
     (by default the whole batch: a few seconds of CPU work on the host)."""
@@ -434,6 +485,15 @@ def run_ours(args, rank, world, local_rank):
     g_steps = min(args.steps, 200)
     g_stages, g_total = timed_steps(chain, stream, flush, g_steps, args.warmup)
     g_total = max_over_ranks(g_total, world, dev)
+    tr = training_step_times(moe, PREFILL, dev, stream, flush, 5)
+    bwd_flops = 2 * PREFILL.expert_flops  # dgrad + wgrad: twice the forward's 6*T*k*H*I
+    training = {"workload": PREFILL.name, "us_per_step": round(sum(tr) * 1e6, 1),
+                "tokens_per_s": round(world * PREFILL.T / sum(tr), 1),
+                "forward_us": round(tr[0] * 1e6, 1), "combine_backward_us": round(tr[1] * 1e6, 1),
+                "experts_backward_us": round(tr[2] * 1e6, 1), "dispatch_backward_us": round(tr[3] * 1e6, 1),
+                "router_backward_us": round(tr[4] * 1e6, 1),
+                "experts_backward_tflops": round(bwd_flops / tr[2] / 1e12, 1),
+                "experts_backward_frac_bf16_peak": round(bwd_flops / tr[2] / 1e12 / peaks["bf16_tflops"], 4)}
     other_gemms = {}
     for cid in (3, 5):
         oc = workloads.CONFIGS[cid]
@@ -502,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
                    "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
                    "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
         "grouped_gemm_other_workloads": other_gemms,
+        "training_step": training,
         "sigmoid_grouped": {
             "workload": f"{c.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
                         f"{grouped_routing.selected_groups} selected, top-two group scores, scale "

@@ -341,6 +341,113 @@ moe_status moe_forward_sigmoid_grouped(const moe_experts* experts, const void* x
                                        uint32_t* indices_opt, void* weights_opt, void* workspace,
                                        size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * First-order training (ruDNN user guide, section 12). The backward runs in
+ * the order the guide gives: combine_backward -> experts backward (the
+ * forward cache's backward) -> dispatch_backward, and the FP32 dweights go
+ * to moe_router_backward for the logits gradient.
+ * ---------------------------------------------------------------------- */
+
+typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router_scoring;
+typedef enum { MOE_INDEX_U32 = 0, MOE_INDEX_I32 = 1, MOE_INDEX_I64 = 2 } moe_index_type;
+
+/* RouterWeightOptions: scoring, renormalize over the selected slots, and a
+ * finite positive scale applied last. */
+typedef struct {
+  int32_t scoring;      /* moe_router_scoring */
+  int32_t renormalize;  /* nonzero: divide by the sum over the slots */
+  float scale;
+} moe_router_weight_options;
+
+/*
+ * moe_router_weights - selected_router_weights: FP32 weights of a fixed
+ * selection. Softmax: the FP32 softmax over all E experts (as moe_route
+ * computes it) at each selected index; sigmoid: 1 / (1 + exp(-l)) of each
+ * selected logit. Then optional renormalize (slot-ordered FP32 sum), then
+ * times scale.
+ *
+ *   logits    device [T, E] in `dtype` (1 <= E <= 1024).
+ *   indices   device [T, top_k] in `index_type` (uint32, int32 or int64),
+ *             1 <= top_k <= min(E, 64). Repeated indices gather; any index
+ *             outside 0..E-1 makes the token's whole row NaN (no out-of-range
+ *             access, no host synchronisation).
+ *   weights   device [T, top_k] float out.
+ */
+moe_status moe_router_weights(const void* logits, moe_dtype dtype, int64_t T, int64_t E, const void* indices,
+                              moe_index_type index_type, int32_t top_k, const moe_router_weight_options* options,
+                              float* weights, void* stream);
+
+/*
+ * moe_router_backward - selected_router_backward: dlogits [T, E] in the
+ * logits dtype, the gradient of the moe_router_weights output (given as
+ * FP32 grad_weights [T, top_k]) with respect to the logits, for the fixed
+ * selection (the top-k itself, group choice and correction bias are not
+ * differentiated). Every entry of dlogits is written. Same checks as
+ * moe_router_weights; an invalid index makes the row of dlogits NaN.
+ */
+moe_status moe_router_backward(const void* logits, moe_dtype dtype, int64_t T, int64_t E, const void* indices,
+                               moe_index_type index_type, int32_t top_k, const moe_router_weight_options* options,
+                               const float* grad_weights, void* dlogits, void* stream);
+
+/*
+ * moe_experts_forward_training - forward_dispatched_training: the experts'
+ * forward that also keeps the cache the backward needs.
+ *
+ *   x_dispatched, offsets, rows   as in moe_experts_forward_dispatched.
+ *   h             device [rows, I] out: SiLU(g) * u in the dtype.
+ *   y_dispatched  device [rows, H] out.
+ *   cache_g, cache_u  device [rows, I] out: the pre-activations g = W_gate x
+ *                 and u = W_up x, rounded to the dtype.
+ *   workspace     at least 256 bytes, 256-byte aligned.
+ * y_dispatched and h are bit-identical to moe_experts_forward_dispatched's.
+ */
+moe_status moe_experts_forward_training(const moe_experts* experts, const void* x_dispatched,
+                                        const uint32_t* offsets, int64_t rows, void* h, void* y_dispatched,
+                                        void* cache_g, void* cache_u, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
+/*
+ * moe_combine_backward - combine_backward: for each token t and slot j with
+ * r = inv[t * top_k + j]: dexpert[r] = w[t, j] * grad_out[t] (rounded to the
+ * dtype) and dweights[t, j] = <grad_out[t], y[r]> (FP32). A slot whose inv
+ * entry is >= T * top_k gets a NaN dweight and writes no dexpert row;
+ * dexpert rows no slot points at are not written.
+ *
+ *   y_dispatched  device [T * top_k, H] in `dtype` (the forward's expert output).
+ *   weights       device [T, top_k] in `weights_dtype` (the forward's weights).
+ *   grad_out      device [T, H] in `dtype`.
+ *   dexpert       device [T * top_k, H] out in `dtype`.
+ *   dweights      device [T, top_k] float out.
+ */
+moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv, const void* weights,
+                                moe_dtype weights_dtype, const void* grad_out, int64_t T, int32_t top_k, int64_t H,
+                                void* dexpert, float* dweights, void* stream);
+
+/*
+ * moe_experts_backward - the forward cache's backward: from dexpert [rows, H]
+ * (dy), the dispatched input gradient dx_dispatched [rows, H] (dtype) and the
+ * FP32 weight gradients dgate, dup [E, I, H] and ddown [E, H, I] (every
+ * entry written; experts without rows get zeros):
+ *   dh = W_down^T dy; dg = dh * u * SiLU'(g); du = dh * SiLU(g);
+ *   dx = W_gate^T dg + W_up^T du; ddown = dy h^T; dgate = dg x^T; dup = du x^T.
+ *   workspace  moe_experts_backward_workspace_size(experts, rows) bytes,
+ *              256-byte aligned (dh in FP32, dg and du in the dtype).
+ */
+size_t moe_experts_backward_workspace_size(const moe_experts* experts, int64_t rows);
+moe_status moe_experts_backward(const moe_experts* experts, const void* x_dispatched, const uint32_t* offsets,
+                                int64_t rows, const void* h, const void* cache_g, const void* cache_u,
+                                const void* dexpert, void* dx_dispatched, float* dgate, float* dup, float* ddown,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_dispatch_backward - dispatch_backward: dx[t] = sum over slots j of
+ * dinput[inv[t * top_k + j]], added in slot order in FP32 and rounded to the
+ * dtype; the routing weight is not applied again. A token with an inv entry
+ * >= T * top_k gets a NaN row.
+ */
+moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* inv, int64_t T, int32_t top_k,
+                                 int64_t H, void* dx, void* stream);
+
 /*
  * moe_device_status - read (and clear, if `clear` is nonzero) the device
  * status word. The expert GEMM kernels bound every pipeline wait (about one

@@ -38,9 +38,26 @@ class GroupRoutingOptions(ctypes.Structure):
                          int(bool(renormalize)), float(scale))
 
 
+class RouterWeightOptions(ctypes.Structure):
+    """moe_router_weight_options (RouterWeightOptions of first-order training):
+    scoring ("softmax" or "sigmoid"), renormalize, scale."""
+    _fields_ = [("scoring", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+    def __init__(self, scoring="softmax", renormalize=True, scale=1.0):
+        code = {"softmax": 0, "sigmoid": 1}[scoring] if isinstance(scoring, str) else int(scoring)
+        super().__init__(code, int(bool(renormalize)), float(scale))
+
+
+_INDEX = {torch.int32: 1, torch.int64: 2}
+if hasattr(torch, "uint32"):
+    _INDEX[torch.uint32] = 0
+
+
 # Every entry point declared in include/moe.h: name -> (restype, argtypes).
 _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 _OPT = ctypes.POINTER(GroupRoutingOptions)
+_ROPT = ctypes.POINTER(RouterWeightOptions)
+_FP = ctypes.c_void_p
 SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -65,6 +82,15 @@ SIGNATURES = {
     "moe_route_sigmoid_grouped": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _OPT, _P, _P, _P, _P]),
     "moe_forward_sigmoid_grouped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _P, _OPT, _P, _P, _P, _P,
                                                    _SZ, _P]),
+    "moe_router_weights": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P]),
+    "moe_router_backward": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P,
+                                           _P]),
+    "moe_experts_forward_training": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_combine_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _I64, _I32, _I64, _P, _P,
+                                            _P]),
+    "moe_experts_backward_workspace_size": (_SZ, [_P, _I64]),
+    "moe_experts_backward": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _I32, _I64, _P, _P]),
     "moe_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _I32]),
     "moe_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _P]),
 }
@@ -380,6 +406,116 @@ def moe_forward_sigmoid_grouped(experts: Experts, x: torch.Tensor, logits: torch
                                            ctypes.byref(o), _ptr(res), _ptr(indices), _ptr(weights), _ptr(ws),
                                            ws.numel(), _stream(stream)))
     return res
+
+
+def _router_opts(options) -> RouterWeightOptions:
+    if isinstance(options, RouterWeightOptions):
+        return options
+    return RouterWeightOptions(options.scoring, options.renormalize, options.scale)
+
+
+def _index_type(indices: torch.Tensor) -> int:
+    if indices.dtype not in _INDEX:
+        raise MoeError(3, f"indices must be uint32, int32 or int64, not {indices.dtype}")
+    return _INDEX[indices.dtype]
+
+
+def moe_router_weights(logits: torch.Tensor, indices: torch.Tensor, options, *, out=None, stream=None):
+    """selected_router_weights: FP32 [T, top_k] weights of a fixed selection."""
+    lib = load_library()
+    _dev_tensor(logits, "logits")
+    _dev_tensor(indices, "indices")
+    T, E = logits.shape
+    k = indices.shape[1]
+    o = _router_opts(options)
+    w = out if out is not None else torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib.moe_router_weights(_ptr(logits), _dt(logits), T, E, _ptr(indices), _index_type(indices), k,
+                                  ctypes.byref(o), _ptr(w), _stream(stream)))
+    return w
+
+
+def moe_router_backward(logits: torch.Tensor, indices: torch.Tensor, grad_weights: torch.Tensor, options, *,
+                        out=None, stream=None):
+    """selected_router_backward: dlogits [T, E] in the logits dtype."""
+    lib = load_library()
+    for name, t in (("logits", logits), ("indices", indices), ("grad_weights", grad_weights)):
+        _dev_tensor(t, name)
+    if grad_weights.dtype != torch.float32:
+        raise MoeError(3, "grad_weights must be float32")
+    T, E = logits.shape
+    k = indices.shape[1]
+    o = _router_opts(options)
+    d = out if out is not None else torch.empty_like(logits)
+    _check(lib.moe_router_backward(_ptr(logits), _dt(logits), T, E, _ptr(indices), _index_type(indices), k,
+                                   ctypes.byref(o), _ptr(grad_weights), _ptr(d), _stream(stream)))
+    return d
+
+
+TrainingCache = namedtuple("TrainingCache", "x_dispatched offsets h g u")
+
+
+def moe_experts_forward_training(experts: Experts, x_dispatched: torch.Tensor, offsets: torch.Tensor,
+                                 workspace=None, stream=None):
+    """forward_dispatched_training: (y_dispatched [rows, H], cache) where the
+    cache holds what moe_experts_backward needs (h, g, u)."""
+    lib = load_library()
+    _dev_tensor(x_dispatched, "x_dispatched")
+    rows = x_dispatched.shape[0]
+    dev = x_dispatched.device
+    y = torch.empty(rows, experts.H, dtype=experts.dtype, device=dev)
+    h, g, u = (torch.empty(rows, experts.I, dtype=experts.dtype, device=dev) for _ in range(3))
+    ws = _workspace(STAGE_WORKSPACE_BYTES, dev, workspace)
+    _check(lib.moe_experts_forward_training(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows, _ptr(h),
+                                            _ptr(y), _ptr(g), _ptr(u), _ptr(ws), ws.numel(), _stream(stream)))
+    return y, TrainingCache(x_dispatched, offsets, h, g, u)
+
+
+ExpertGrads = namedtuple("ExpertGrads", "dx_dispatched dgate dup ddown")
+
+
+def moe_experts_backward(experts: Experts, cache: TrainingCache, dexpert: torch.Tensor, workspace=None,
+                         stream=None) -> ExpertGrads:
+    """cache.backward(dexpert): dx_dispatched [rows, H] and FP32 dgate, dup
+    [E, I, H] and ddown [E, H, I]."""
+    lib = load_library()
+    _dev_tensor(dexpert, "dexpert")
+    rows = cache.x_dispatched.shape[0]
+    dev = dexpert.device
+    dx = torch.empty(rows, experts.H, dtype=experts.dtype, device=dev)
+    dgate = torch.empty(experts.E, experts.I, experts.H, dtype=torch.float32, device=dev)
+    dup = torch.empty_like(dgate)
+    ddown = torch.empty(experts.E, experts.H, experts.I, dtype=torch.float32, device=dev)
+    ws = _workspace(lib.moe_experts_backward_workspace_size(experts.handle, rows), dev, workspace)
+    _check(lib.moe_experts_backward(experts.handle, _ptr(cache.x_dispatched), _ptr(cache.offsets), rows,
+                                    _ptr(cache.h), _ptr(cache.g), _ptr(cache.u), _ptr(dexpert), _ptr(dx),
+                                    _ptr(dgate), _ptr(dup), _ptr(ddown), _ptr(ws), ws.numel(), _stream(stream)))
+    return ExpertGrads(dx, dgate, dup, ddown)
+
+
+def moe_combine_backward(y_dispatched: torch.Tensor, inv: torch.Tensor, weights: torch.Tensor,
+                         grad_out: torch.Tensor, stream=None):
+    """combine_backward: (dexpert [rows, H] in y's dtype, dweights [T, top_k] FP32)."""
+    lib = load_library()
+    for name, t in (("y_dispatched", y_dispatched), ("inv", inv), ("weights", weights), ("grad_out", grad_out)):
+        _dev_tensor(t, name)
+    T, k = weights.shape
+    H = y_dispatched.shape[1]
+    dexp = torch.empty_like(y_dispatched)
+    dw = torch.empty(T, k, dtype=torch.float32, device=y_dispatched.device)
+    _check(lib.moe_combine_backward(_ptr(y_dispatched), _dt(y_dispatched), _ptr(inv), _ptr(weights), _dt(weights),
+                                    _ptr(grad_out), T, k, H, _ptr(dexp), _ptr(dw), _stream(stream)))
+    return dexp, dw
+
+
+def moe_dispatch_backward(dinput: torch.Tensor, inv: torch.Tensor, T: int, top_k: int, stream=None):
+    """dispatch_backward: dx [T, H], each token's dispatched rows added in slot order."""
+    lib = load_library()
+    _dev_tensor(dinput, "dinput")
+    _dev_tensor(inv, "inv")
+    H = dinput.shape[1]
+    dx = torch.empty(T, H, dtype=dinput.dtype, device=dinput.device)
+    _check(lib.moe_dispatch_backward(_ptr(dinput), _dt(dinput), _ptr(inv), T, top_k, H, _ptr(dx), _stream(stream)))
+    return dx
 
 
 def moe_device_status(clear: bool = True) -> int:

@@ -138,17 +138,18 @@ moe_status check_current_device(const moe_experts* ex) {
 // One expert GEMM stage: gate_up (x_dispatched, or x gathered through
 // row_src, -> h) or down (h -> y).
 moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const moe::TcGather* gather,
-                     const uint32_t* offsets, int64_t rows, void* out, void* sched, cudaStream_t s) {
+                     const uint32_t* offsets, int64_t rows, void* out, void* sched, cudaStream_t s,
+                     const moe::TcCache* cache = nullptr) {
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32) {
-    err = moe::launch_experts_simt_f32(gate_up, static_cast<const float*>(a), gather, offsets,
+    err = moe::launch_experts_simt_f32(gate_up, static_cast<const float*>(a), gather, cache, offsets,
                                        static_cast<int>(ex->E), rows,
                                        static_cast<const float*>(gate_up ? ex->gate : ex->down),
                                        static_cast<const float*>(gate_up ? ex->up : nullptr), ex->H,
                                        ex->I, static_cast<float*>(out), s);
   } else {
-    err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, gather, offsets, static_cast<int>(ex->E),
+    err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, gather, cache, offsets, static_cast<int>(ex->E),
                                  rows, ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why);
   }
   if (err != cudaSuccess) return cuda_fail(err, gate_up ? "gate/up GEMM launch" : "down GEMM launch", why);
@@ -502,6 +503,136 @@ moe_status moe_forward_sigmoid_grouped(const moe_experts* ex, const void* x, con
   };
   return forward_chain(ex, x, logits_dtype, T, p.k, out, indices_opt, weights_opt, workspace,
                        workspace_bytes, static_cast<cudaStream_t>(stream), route);
+}
+
+// ---------------------------------------------------------------- first-order training
+
+static moe_status check_router_weight_args(const void* logits, int dtype, int64_t T, int64_t E,
+                                           const void* indices, int index_type, int32_t top_k,
+                                           const moe_router_weight_options* o, moe::RouterParams* p) {
+  if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (index_type < MOE_INDEX_U32 || index_type > MOE_INDEX_I64)
+    return fail(MOE_ERR_DTYPE, "index type must be MOE_INDEX_U32, MOE_INDEX_I32 or MOE_INDEX_I64");
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  if (top_k < 1 || top_k > E || top_k > 64) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= min(E, 64)");
+  if (o == nullptr) return fail(MOE_ERR_NULL, "options must be non-NULL");
+  if (o->scoring != MOE_ROUTER_SOFTMAX && o->scoring != MOE_ROUTER_SIGMOID)
+    return fail(MOE_ERR_SHAPE, "scoring must be MOE_ROUTER_SOFTMAX or MOE_ROUTER_SIGMOID");
+  if (!(o->scale > 0.0f) || !(o->scale <= std::numeric_limits<float>::max()))
+    return fail(MOE_ERR_SHAPE, "scale must be finite and positive");
+  if (T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && (logits == nullptr || indices == nullptr)) return fail(MOE_ERR_NULL, "logits and indices must be non-NULL");
+  p->scoring = o->scoring;
+  p->renormalize = o->renormalize != 0;
+  p->scale = o->scale;
+  return MOE_OK;
+}
+
+moe_status moe_router_weights(const void* logits, moe_dtype dtype, int64_t T, int64_t E, const void* indices,
+                              moe_index_type index_type, int32_t top_k, const moe_router_weight_options* options,
+                              float* weights, void* stream) {
+  moe::RouterParams p{};
+  moe_status st = check_router_weight_args(logits, dtype, T, E, indices, index_type, top_k, options, &p);
+  if (st != MOE_OK) return st;
+  if (T > 0 && weights == nullptr) return fail(MOE_ERR_NULL, "weights must be non-NULL");
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_router_weights(logits, dtype, T, static_cast<int>(E), indices, index_type, top_k, p,
+                                               weights, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_weights launch");
+  return ok();
+}
+
+moe_status moe_router_backward(const void* logits, moe_dtype dtype, int64_t T, int64_t E, const void* indices,
+                               moe_index_type index_type, int32_t top_k, const moe_router_weight_options* options,
+                               const float* grad_weights, void* dlogits, void* stream) {
+  moe::RouterParams p{};
+  moe_status st = check_router_weight_args(logits, dtype, T, E, indices, index_type, top_k, options, &p);
+  if (st != MOE_OK) return st;
+  if (T > 0 && (grad_weights == nullptr || dlogits == nullptr))
+    return fail(MOE_ERR_NULL, "grad_weights and dlogits must be non-NULL");
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_router_backward(logits, dtype, T, static_cast<int>(E), indices, index_type, top_k,
+                                                p, grad_weights, dlogits, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_router_backward launch");
+  return ok();
+}
+
+moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv, const void* weights,
+                                moe_dtype weights_dtype, const void* grad_out, int64_t T, int32_t top_k, int64_t H,
+                                void* dexpert, float* dweights, void* stream) {
+  if (!dtype_valid(dtype) || !dtype_valid(weights_dtype)) return fail(MOE_ERR_DTYPE, "unknown dtype");
+  if (top_k < 1) return fail(MOE_ERR_TOP_K, "top_k must be >= 1");
+  if (H < 1 || T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "need H >= 1, T >= 0, T*top_k < 2^32-1");
+  if (T > 0 && (y_dispatched == nullptr || inv == nullptr || weights == nullptr || grad_out == nullptr ||
+                dexpert == nullptr || dweights == nullptr))
+    return fail(MOE_ERR_NULL, "every buffer must be non-NULL");
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_combine_backward(y_dispatched, dtype, inv, weights, weights_dtype, grad_out, T, top_k,
+                                                 H, dexpert, dweights, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_combine_backward launch");
+  return ok();
+}
+
+moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* inv, int64_t T, int32_t top_k,
+                                 int64_t H, void* dx, void* stream) {
+  if (!dtype_valid(dtype)) return fail(MOE_ERR_DTYPE, "unknown dtype");
+  if (top_k < 1) return fail(MOE_ERR_TOP_K, "top_k must be >= 1");
+  if (H < 1 || T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "need H >= 1, T >= 0, T*top_k < 2^32-1");
+  if (T > 0 && (dinput == nullptr || inv == nullptr || dx == nullptr))
+    return fail(MOE_ERR_NULL, "dinput, inv and dx must be non-NULL");
+  if (T == 0) return ok();
+  cudaError_t err = moe::launch_dispatch_backward(dinput, dtype, inv, T, top_k, H, dx, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch_backward launch");
+  return ok();
+}
+
+moe_status moe_experts_forward_training(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets,
+                                        int64_t rows, void* h, void* y_dispatched, void* cache_g, void* cache_u,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, y_dispatched, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (rows > 0 && (h == nullptr || cache_g == nullptr || cache_u == nullptr))
+    return fail(MOE_ERR_NULL, "h, cache_g and cache_u must be non-NULL");
+  if (ex->dtype != MOE_F32 && (!aligned16(h) || !aligned16(cache_g) || !aligned16(cache_u)))
+    return fail(MOE_ERR_ALIGNMENT, "h, cache_g and cache_u must be 16-byte aligned");
+  if (rows == 0) return ok();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe::TcCache cache{cache_g, cache_u};
+  st = run_stage(ex, true, x_dispatched, nullptr, offsets, rows, h, workspace, s, &cache);
+  if (st != MOE_OK) return st;
+  st = run_stage(ex, false, h, nullptr, offsets, rows, y_dispatched, workspace, s);
+  return st != MOE_OK ? st : ok();
+}
+
+size_t moe_experts_backward_workspace_size(const moe_experts* ex, int64_t rows) {
+  if (ex == nullptr || rows < 0) return 0;
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(ex->I);
+  return align_up(n * 4 + 1, 256) + 2 * align_up(n * dtype_size(ex->dtype) + 1, 256);
+}
+
+moe_status moe_experts_backward(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets, int64_t rows,
+                                const void* h, const void* cache_g, const void* cache_u, const void* dexpert,
+                                void* dx_dispatched, float* dgate, float* dup, float* ddown, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, dx_dispatched, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (dgate == nullptr || dup == nullptr || ddown == nullptr)
+    return fail(MOE_ERR_NULL, "dgate, dup and ddown must be non-NULL");
+  if (rows > 0 && (h == nullptr || cache_g == nullptr || cache_u == nullptr || dexpert == nullptr))
+    return fail(MOE_ERR_NULL, "h, cache_g, cache_u and dexpert must be non-NULL");
+  if (workspace_bytes < moe_experts_backward_workspace_size(ex, rows))
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_experts_backward_workspace_size()");
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(ex->I);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t dh_bytes = align_up(n * 4 + 1, 256);
+  const size_t d_bytes = align_up(n * dtype_size(ex->dtype) + 1, 256);
+  moe::TrainBuffers b{x_dispatched, h, cache_g, cache_u, dexpert, ex->gate, ex->up, ex->down,
+                      reinterpret_cast<float*>(ws), ws + dh_bytes, ws + dh_bytes + d_bytes, dx_dispatched,
+                      dgate, dup, ddown};
+  cudaError_t err = moe::launch_experts_backward(ex->dtype, b, offsets, static_cast<int>(ex->E), rows, ex->H, ex->I,
+                                                 static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_experts_backward launch");
+  return ok();
 }
 
 moe_status moe_device_status(uint32_t* code, int32_t clear) {

@@ -10,6 +10,11 @@
 // atomics, so the result does not depend on scheduling. A slot whose inv
 // entry is INVALID_ROW (an index >= E at dispatch), or any entry >= T*k,
 // makes its token's row NaN instead of reading out of range.
+//
+// The same kernel without weights is dispatch_backward (ruDNN user guide,
+// section 12): dx[t, :] = sum_j dinput[inv[t*k + j], :], the dispatched rows'
+// gradients added back onto their token in slot order, with no routing
+// weight applied again.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -40,7 +45,7 @@ __device__ __forceinline__ void store_vec(T* p, const float (&v)[Vec<T>::N]) {
   *reinterpret_cast<uint4*>(p) = raw;
 }
 
-template <typename T, typename TW, bool VEC>
+template <typename T, typename TW, bool VEC, bool WEIGHTED>
 __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
                                                       const uint32_t* __restrict__ inv,
                                                       const TW* __restrict__ w, int64_t T_tokens,
@@ -59,7 +64,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
       const uint32_t r = inv[t * k + j];
       s_row[j] = r < rows ? r : 0u;           // an invalid entry reads row 0 ...
-      s_w[j] = to_f32(w[t * k + j]);
+      s_w[j] = WEIGHTED ? to_f32(w[t * k + j]) : 1.0f;
       if (r >= rows) s_bad = 1;               // ... and the whole row becomes NaN
     }
     __syncthreads();
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
   }
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool WEIGHTED = true>
 cudaError_t launch_combine_t(const void* y, const uint32_t* inv, const void* w, int64_t T_tokens,
                              int k, int64_t H, void* out, cudaStream_t stream) {
   const int blocks = static_cast<int>(T_tokens < 65536 ? T_tokens : 65536);
@@ -115,11 +120,11 @@ cudaError_t launch_combine_t(const void* y, const uint32_t* inv, const void* w, 
   const int64_t per_thread = vec ? Vec<T>::N : 1;
   while (threads > 32 && static_cast<int64_t>(threads / 2) * per_thread >= H) threads /= 2;
   if (vec) {
-    combine_kernel<T, TW, true><<<blocks, threads, 0, stream>>>(
+    combine_kernel<T, TW, true, WEIGHTED><<<blocks, threads, 0, stream>>>(
         static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
         static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
   } else {
-    combine_kernel<T, TW, false><<<blocks, threads, 0, stream>>>(
+    combine_kernel<T, TW, false, WEIGHTED><<<blocks, threads, 0, stream>>>(
         static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
         static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
   }
@@ -149,6 +154,16 @@ cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint
       return launch_combine_w<__half>(y_dispatched, inv, weights, weights_dtype, T, top_k, H, out, stream);
     default:
       return launch_combine_w<__nv_bfloat16>(y_dispatched, inv, weights, weights_dtype, T, top_k, H, out, stream);
+  }
+}
+
+cudaError_t launch_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* inv, int64_t T,
+                                     int top_k, int64_t H, void* dx, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  switch (dtype) {
+    case MOE_F32: return launch_combine_t<float, float, false>(dinput, inv, nullptr, T, top_k, H, dx, stream);
+    case MOE_F16: return launch_combine_t<__half, float, false>(dinput, inv, nullptr, T, top_k, H, dx, stream);
+    default: return launch_combine_t<__nv_bfloat16, float, false>(dinput, inv, nullptr, T, top_k, H, dx, stream);
   }
 }
 

@@ -21,7 +21,8 @@ template <bool GATE_UP>
 __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
     const float* __restrict__ a, const uint32_t* __restrict__ row_src, int top_k, int64_t a_rows,
     const uint32_t* __restrict__ offsets, int E, const float* __restrict__ w0, const float* __restrict__ w1,
-    int64_t K, int64_t N, int64_t rows_total, float* __restrict__ out) {
+    int64_t K, int64_t N, int64_t rows_total, float* __restrict__ out, float* __restrict__ out_g,
+    float* __restrict__ out_u) {
   __shared__ uint32_t tile_start[ROUTE_MAX_E + 1];
   __shared__ float As[SB_K][SB_M + 4];
   __shared__ float B0s[SB_K][SB_N + 4];
@@ -96,7 +97,13 @@ __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
       const int64_t n = n0 + tx * 4 + j;
       if (n >= N) continue;
       float v = acc0[i][j];
-      if constexpr (GATE_UP) v = v / (1.0f + expf(-v)) * acc1[i][j];
+      if constexpr (GATE_UP) {
+        if (out_g != nullptr) {  // training: keep the pre-activations
+          out_g[(static_cast<int64_t>(tc.row0) + r) * N + n] = v;
+          out_u[(static_cast<int64_t>(tc.row0) + r) * N + n] = acc1[i][j];
+        }
+        v = v / (1.0f + expf(-v)) * acc1[i][j];
+      }
       dst[n] = v;
     }
   }
@@ -109,11 +116,11 @@ int64_t tile_bound(int64_t rows, int E, int bm, int64_t n_tiles) {
 
 }  // namespace
 
-cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather,
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather, const TcCache* cache,
                                     const uint32_t* offsets, int E, int64_t rows, const float* w0,
                                     const float* w1, int64_t H, int64_t I, float* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  if (gather != nullptr && !gate_up) return cudaErrorInvalidValue;
+  if ((gather != nullptr || cache != nullptr) && !gate_up) return cudaErrorInvalidValue;
   const float* src = gather != nullptr ? static_cast<const float*>(gather->x) : a;
   const uint32_t* row_src = gather != nullptr ? gather->row_src : nullptr;
   const int top_k = gather != nullptr ? gather->top_k : 1;
@@ -121,11 +128,13 @@ cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather
   if (gate_up) {
     const int64_t g = tile_bound(rows, E, SB_M, (I + SB_N - 1) / SB_N);
     experts_simt_kernel<true><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        src, row_src, top_k, a_rows, offsets, E, w0, w1, H, I, rows, out);
+        src, row_src, top_k, a_rows, offsets, E, w0, w1, H, I, rows, out,
+        cache != nullptr ? static_cast<float*>(cache->g) : nullptr,
+        cache != nullptr ? static_cast<float*>(cache->u) : nullptr);
   } else {
     const int64_t g = tile_bound(rows, E, SB_M, (H + SB_N - 1) / SB_N);
     experts_simt_kernel<false><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        a, nullptr, 1, rows, offsets, E, w0, nullptr, I, H, rows, out);
+        a, nullptr, 1, rows, offsets, E, w0, nullptr, I, H, rows, out, nullptr, nullptr);
   }
   return cudaGetLastError();
 }

@@ -136,6 +136,9 @@ struct TcArgs {
   int top_k;
   uint32_t x_rows;
   int k_bytes;              // K * 2
+  // Training mode (K3 only): the pre-activations g and u, [rows, I] each.
+  void* out_g;
+  void* out_u;
 };
 
 // SiLU(g) = g * sigmoid(g), sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
@@ -370,14 +373,17 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
         tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0), v0);
         tmem_ld_32x32b_x32(t_lane + C::D1 + static_cast<uint32_t>(c0), v1);
         tmem_ld_wait();
-#pragma unroll
-        for (int blk = 0; blk < (GATE_UP ? 1 : 2); ++blk) {
+        // K3 writes h, and in training mode also the pre-activations g and u
+        // (the forward cache); K4 writes its two 128-column blocks.
+        const int n_blk = GATE_UP ? (args.out_g != nullptr ? 3 : 1) : 2;
+        for (int blk = 0; blk < n_blk; ++blk) {
           // Lane = output column, j = token: write column-major, read token rows.
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             float val;
             if (GATE_UP) {
-              val = silu_f32(__uint_as_float(v0[j])) * __uint_as_float(v1[j]);
+              const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
+              val = blk == 0 ? silu_f32(gv) * uv : (blk == 1 ? gv : uv);
             } else {
               val = __uint_as_float(blk == 0 ? v0[j] : v1[j]);
             }
@@ -385,7 +391,8 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
             xp[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
           }
           __syncwarp();
-          const int64_t col = colA + (blk == 0 ? 0 : BM) + rd_part * 8;
+          const int64_t col = colA + ((GATE_UP || blk == 0) ? 0 : BM) + rd_part * 8;
+          void* out_base = !GATE_UP || blk == 0 ? args.out : (blk == 1 ? args.out_g : args.out_u);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int j = p * 8 + rd_tok;
@@ -393,7 +400,7 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
             const int t_in = c0 + j;
             if (t_in < tc.rows && tc.row0 + static_cast<uint32_t>(t_in) < args.rows_total &&
                 col + 8 <= args.n_out) {
-              T* dst = static_cast<T*>(args.out) + (static_cast<int64_t>(tc.row0) + t_in) * args.n_out + col;
+              T* dst = static_cast<T*>(out_base) + (static_cast<int64_t>(tc.row0) + t_in) * args.n_out + col;
               *reinterpret_cast<uint4*>(dst) = row;
             }
           }
@@ -560,8 +567,8 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
 
 template <typename T>
 cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                         const TcGather* gather, const uint32_t* offsets, int E, int64_t rows, int64_t H,
-                         int64_t I, void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
+                         const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E, int64_t rows,
+                         int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
                          const char** why) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
@@ -586,7 +593,15 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   const int64_t cap = tile_bound(rows, E, nw, small ? 32 : 256);
   TcArgs args{offsets, out, sched, E, nw, static_cast<int>((K + BK - 1) / BK), static_cast<int>(n_out),
               static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status,
-              nullptr, nullptr, 1, 0, static_cast<int>(K * 2)};
+              nullptr, nullptr, 1, 0, static_cast<int>(K * 2), nullptr, nullptr};
+  if (cache != nullptr) {
+    if (!gate_up) {
+      *why = "the pre-activation cache belongs to the gate/up stage";
+      return cudaErrorInvalidValue;
+    }
+    args.out_g = cache->g;
+    args.out_u = cache->u;
+  }
   if (gather != nullptr) {
     if (!gate_up) {
       *why = "the gather mode applies to the gate/up stage only";
@@ -624,14 +639,14 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
 }
 
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                              const TcGather* gather, const uint32_t* offsets, int E, int64_t rows,
-                              int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
+                              const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E,
+                              int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
                               cudaStream_t stream, const char** why) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
-    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, gather, offsets, E, rows, H, I, out, sched,
+    return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, gather, cache, offsets, E, rows, H, I, out, sched,
                                        num_sms, stream, why);
-  return launch_stage<__half>(w, dtype, gate_up, a, gather, offsets, E, rows, H, I, out, sched, num_sms,
+  return launch_stage<__half>(w, dtype, gate_up, a, gather, cache, offsets, E, rows, H, I, out, sched, num_sms,
                               stream, why);
 }
 

@@ -59,7 +59,12 @@ struct TcGather {
   int top_k;
   int64_t x_rows;
 };
-cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather,
+// Training forward: the gate/up stage also writes the pre-activations.
+struct TcCache {
+  void* g;  // [rows, I]
+  void* u;  // [rows, I]
+};
+cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather* gather, const TcCache* cache,
                                     const uint32_t* offsets, int E, int64_t rows, const float* w0,
                                     const float* w1, int64_t H, int64_t I, float* out, cudaStream_t stream);
 
@@ -78,10 +83,48 @@ inline bool forward_gathers_rows(int64_t rows, int64_t E) { return rows <= 8 * E
 // sched: one uint32 of device memory for the tile counter (zeroed on the stream before the launch).
 constexpr size_t TC_SCHED_BYTES = 256;
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
-                              const TcGather* gather, const uint32_t* offsets, int E, int64_t rows,
-                              int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
+                              const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E,
+                              int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
                               cudaStream_t stream, const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
+
+// ---- first-order training (train_router.cu, train_experts.cu, combine.cu)
+struct RouterParams {
+  int scoring;      // 0 softmax, 1 sigmoid
+  int renormalize;
+  float scale;
+};
+// index_type: 0 uint32, 1 int32, 2 int64
+cudaError_t launch_router_weights(const void* logits, moe_dtype dtype, int64_t T, int E, const void* indices,
+                                  int index_type, int top_k, const RouterParams& p, float* weights,
+                                  cudaStream_t stream);
+cudaError_t launch_router_backward(const void* logits, moe_dtype dtype, int64_t T, int E, const void* indices,
+                                   int index_type, int top_k, const RouterParams& p, const float* grad_weights,
+                                   void* dlogits, cudaStream_t stream);
+cudaError_t launch_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                                    const void* weights, moe_dtype weights_dtype, const void* grad_out, int64_t T,
+                                    int top_k, int64_t H, void* dexpert, float* dweights, cudaStream_t stream);
+cudaError_t launch_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* inv, int64_t T,
+                                     int top_k, int64_t H, void* dx, cudaStream_t stream);
+struct TrainBuffers {
+  const void* x;     // x_dispatched [rows, H]
+  const void* h;     // [rows, I]
+  const void* g;     // [rows, I]
+  const void* u;     // [rows, I]
+  const void* dy;    // dexpert [rows, H]
+  const void* gate;  // [E, I, H]
+  const void* up;    // [E, I, H]
+  const void* down;  // [E, H, I]
+  float* dh;         // scratch [rows, I]
+  void* dg;          // scratch [rows, I]
+  void* du;          // scratch [rows, I]
+  void* dx;          // out [rows, H]
+  float* dgate;      // out [E, I, H]
+  float* dup;        // out [E, I, H]
+  float* ddown;      // out [E, H, I]
+};
+cudaError_t launch_experts_backward(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,
+                                    int64_t rows, int64_t H, int64_t I, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 
 }  // namespace moe

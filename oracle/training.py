@@ -188,14 +188,27 @@ class ExpertGrads:
     dgate: np.ndarray          # [E, I, H]
     dup: np.ndarray            # [E, I, H]
     ddown: np.ndarray          # [E, H, I]
+    # The same sums over |terms| (|dg| |W_gate| + |du| |W_up|, |dg|^T |x|, ...):
+    # the scale a rounding error of each sum is measured against.
+    dx_abs: np.ndarray | None = None
+    dgate_abs: np.ndarray | None = None
+    dup_abs: np.ndarray | None = None
+    ddown_abs: np.ndarray | None = None
 
 
-def experts_backward(x_dispatched, gate, up, down, offsets, dexpert) -> ExpertGrads:
+def experts_backward(x_dispatched, gate, up, down, offsets, dexpert, cache=None) -> ExpertGrads:
     """Backward of y_r = W_down[e] (SiLU(W_gate[e] x_r) * (W_up[e] x_r)) over the
     dispatched rows of each expert (f64 from the dtype-rounded inputs):
     dh = dy W_down, dW_down = dy^T h, dg = dh * u * SiLU'(g), du = dh * SiLU(g),
-    dx = dg W_gate + du W_up, dW_gate = dg^T x, dW_up = du^T x."""
+    dx = dg W_gate + du W_up, dW_gate = dg^T x, dW_up = du^T x.
+
+    ``cache`` = (g, u, h) [rows, I] each: the forward cache the backward
+    consumes (cache.backward of the pages); without it g, u and h are
+    recomputed from x in f64."""
     x = widen(x_dispatched)
+    cg = cu = ch = None
+    if cache is not None:
+        cg, cu, ch = (widen(c) if isinstance(c, torch.Tensor) else np.asarray(c, dtype=np.float64) for c in cache)
     dy = widen(dexpert) if isinstance(dexpert, torch.Tensor) else np.asarray(dexpert, dtype=np.float64)
     Wg, Wu, Wd = widen(gate), widen(up), widen(down)
     E, I, H = Wg.shape
@@ -204,14 +217,18 @@ def experts_backward(x_dispatched, gate, up, down, offsets, dexpert) -> ExpertGr
     dWg = np.zeros((E, I, H))
     dWu = np.zeros((E, I, H))
     dWd = np.zeros((E, H, I))
+    ab = [np.zeros_like(x), np.zeros((E, I, H)), np.zeros((E, I, H)), np.zeros((E, H, I))]
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
         if hi <= lo:
             continue
         X, dY = x[lo:hi], dy[lo:hi]
-        G = X @ Wg[e].T
-        U = X @ Wu[e].T
-        Hh = _silu(G) * U
+        if cache is None:
+            G = X @ Wg[e].T
+            U = X @ Wu[e].T
+            Hh = _silu(G) * U
+        else:
+            G, U, Hh = cg[lo:hi], cu[lo:hi], ch[lo:hi]
         dH = dY @ Wd[e]
         dWd[e] = dY.T @ Hh
         dG = dH * U * _silu_grad(G)
@@ -219,7 +236,11 @@ def experts_backward(x_dispatched, gate, up, down, offsets, dexpert) -> ExpertGr
         dx[lo:hi] = dG @ Wg[e] + dU @ Wu[e]
         dWg[e] = dG.T @ X
         dWu[e] = dU.T @ X
-    return ExpertGrads(dx, dWg, dWu, dWd)
+        ab[0][lo:hi] = np.abs(dG) @ np.abs(Wg[e]) + np.abs(dU) @ np.abs(Wu[e])
+        ab[1][e] = np.abs(dG).T @ np.abs(X)
+        ab[2][e] = np.abs(dU).T @ np.abs(X)
+        ab[3][e] = np.abs(dY).T @ np.abs(Hh)
+    return ExpertGrads(dx, dWg, dWu, dWd, *ab)
 
 
 def dispatch_backward(dinput, inv, T: int, top_k: int):

@@ -180,6 +180,38 @@ def test_gate_up_gather_rejects_bad_arguments(lib, kwargs, status):
                                           a["h"], a["ws"], 1 << 10, None) == status
 
 
+def _rw(lib, logits=FAKE, dtype=2, T=4, E=8, idx=FAKE, itype=1, k=2, scoring=0, scale=1.0, out=FAKE,
+        opts=True):
+    o = moe.RouterWeightOptions(scoring, True, scale)
+    return lib.moe_router_weights(logits, dtype, T, E, idx, itype, k, ctypes.byref(o) if opts else None, out, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(out=None), 1), (dict(opts=False), 1),
+    (dict(dtype=5), 3), (dict(itype=3), 3), (dict(itype=-1), 3),
+    (dict(E=0), 2), (dict(E=1025), 2), (dict(T=-1), 2),
+    (dict(k=0), 4), (dict(k=9), 4), (dict(k=65, E=100), 4),
+    (dict(scoring=2), 2), (dict(scale=0.0), 2), (dict(scale=float("inf")), 2),
+])
+def test_router_weights_rejects_bad_arguments(lib, kwargs, status):
+    assert _rw(lib, **kwargs) == status
+
+
+def test_training_entry_points_reject_null_buffers(lib):
+    o = moe.RouterWeightOptions("sigmoid", False, 1.0)
+    assert lib.moe_router_backward(FAKE, 2, 4, 8, FAKE, 1, 2, ctypes.byref(o), None, FAKE, None) == 1
+    assert lib.moe_router_backward(FAKE, 2, 0, 8, None, 1, 2, ctypes.byref(o), None, None, None) == 0
+    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, 2, None, 4, 2, 64, FAKE, FAKE, None) == 1
+    assert lib.moe_combine_backward(FAKE, 9, FAKE, FAKE, 2, FAKE, 4, 2, 64, FAKE, FAKE, None) == 3
+    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, 2, FAKE, 4, 0, 64, FAKE, FAKE, None) == 4
+    assert lib.moe_dispatch_backward(None, 2, FAKE, 4, 2, 64, FAKE, None) == 1
+    assert lib.moe_dispatch_backward(FAKE, 2, FAKE, 4, 2, 0, FAKE, None) == 2
+    assert lib.moe_experts_forward_training(None, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 10, None) == 1
+    assert lib.moe_experts_backward(None, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    1 << 10, None) == 1
+    assert lib.moe_experts_backward_workspace_size(None, 4) == 0
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.moe_selftest_bounded_wait(0, None) == 2
     assert lib.moe_selftest_bounded_wait(10_000_001, None) == 2

@@ -1,0 +1,228 @@
+"""GPU parity of first-order training (ruDNN user guide, section 12) against
+the training oracle, through the C ABI: router weights and their gradient,
+the training forward's cache, combine backward, the experts' backward and
+dispatch backward."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle import moe_oracle
+from tests.parity import assert_nan_positions_equal, f64, u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+Opt = oracle.RouterWeightOptions
+VARIANTS = [Opt("softmax", False, 1.0), Opt("softmax", True, 1.0), Opt("sigmoid", False, 1.5),
+            Opt("sigmoid", True, 2.5)]
+_ULP = {torch.float32: 2.0 ** -23, torch.float16: 2.0 ** -10, torch.bfloat16: 2.0 ** -7}
+
+
+def _router_inputs(T, E, k, dtype, seed, idx_dtype=torch.int32):
+    g = torch.Generator().manual_seed(seed)
+    l = (torch.randn(T, E, generator=g) * 2).to(dtype)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)])
+    idx[1, 1] = idx[1, 0]                      # a repeated index gathers twice
+    idx[2, 0] = E + 3                          # an invalid index: NaN row
+    gw = torch.randn(T, k, generator=g)
+    return l, idx.to(idx_dtype), gw
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 6), (128, 8), (200, 64), (1024, 7)])
+def test_router_weights_and_backward_parity(cuda_lib, dtype, E, k):
+    moe = cuda_lib
+    T = 97
+    l, idx, gw = _router_inputs(T, E, k, dtype, E * 31 + k)
+    for i, o in enumerate(VARIANTS):
+        it = [torch.int32, torch.int64, torch.int32, torch.int64][i]
+        w = moe.moe_router_weights(l.to(DEV), idx.to(it).to(DEV), o)
+        d = moe.moe_router_backward(l.to(DEV), idx.to(it).to(DEV), gw.to(DEV), o)
+        torch.cuda.synchronize()
+        w32, _ = oracle.selected_router_weights(l, idx.numpy(), o)
+        d64, _ = oracle.selected_router_backward(l, idx.numpy(), gw, o)
+        gwv = f64(w)
+        assert_nan_positions_equal(gwv, w32.astype(np.float64), "router weights")
+        fin = np.isfinite(w32)
+        rel = np.abs(gwv[fin] - w32[fin]) / np.maximum(np.abs(w32[fin]), 1e-30)
+        assert rel.max() <= 1e-6, f"{o}: weight rel error {rel.max():.3e}"
+        gd = f64(d)
+        assert_nan_positions_equal(gd, d64, "dlogits")
+        rows = np.isfinite(d64).all(axis=1)
+        bound = 4e-6 * o.scale * np.abs(gw.numpy().astype(np.float64)).sum(axis=1)[rows][:, None]
+        err = np.abs(gd[rows] - d64[rows])
+        assert (err <= _ULP[dtype] * np.abs(d64[rows]) + bound + 1e-30).all(), \
+            f"{o}: dlogits error {err.max():.3e} (bound {bound.max():.3e})"
+
+
+def test_router_sigmoid_backward_is_local(cuda_lib):
+    """Sigmoid scoring: logits outside the selection get an exact zero gradient."""
+    moe = cuda_lib
+    l, idx, gw = _router_inputs(64, 40, 5, torch.float32, 3)
+    idx[2, 0] = 0
+    d = moe.moe_router_backward(l.to(DEV), idx.to(DEV), gw.to(DEV), Opt("sigmoid", True, 1.0)).cpu()
+    mask = torch.zeros(64, 40, dtype=torch.bool)
+    mask.scatter_(1, idx.long(), True)
+    assert (d[~mask] == 0).all()
+
+
+def _small_training_case(name, seed=5):
+    cfg = workloads.SMALL_CONFIGS[name]
+    inp = workloads.generate(cfg)
+    rt = moe_oracle.route(inp["logits"], cfg.top_k, cfg.renormalize)
+    dp = moe_oracle.dispatch(rt.indices, cfg.E)
+    xd = inp["x"][torch.from_numpy(dp.row_src.astype(np.int64) // cfg.top_k)]
+    g = torch.Generator().manual_seed(seed)
+    dy = (torch.randn(cfg.T * cfg.top_k, cfg.H, generator=g) * 0.5).to(cfg.torch_dtype)
+    return cfg, inp, rt, dp, xd, dy
+
+
+# Gradient tolerance: each gradient entry is a sum, and its rounding error is
+# measured against the sum of |terms| (the oracle returns it): the F32 path
+# computes every step in FP32 (2e-5 covers FP32 sums of up to a few thousand
+# terms); the 16-bit paths round g, u, h, dg and du to the dtype once each on
+# the way, a few 2^-9 relative, so 2e-2 as in the forward outputs' bar.
+GRAD_TOL = {torch.float32: 2e-5, torch.float16: 2e-2, torch.bfloat16: 2e-2}
+
+
+def _grad_close(got, ref, abs_terms, dtype, what):
+    assert_nan_positions_equal(got, ref, what)
+    fin = np.isfinite(ref)
+    err = np.abs(got[fin] - ref[fin])
+    bound = GRAD_TOL[dtype] * abs_terms[fin] + 1e-30
+    worst = np.argmax(err / bound) if err.size else 0
+    assert (err <= bound).all(), (f"{what}: error {err.flat[worst]:.3e} against sum |terms| "
+                                  f"{abs_terms[fin].flat[worst]:.3e}")
+
+
+@pytest.mark.parametrize("name", ["f32_ragged", "bf16_ragged", "bf16_fine", "f16_zipf", "bf16_decode"])
+def test_experts_training_forward_and_backward_parity(cuda_lib, name):
+    moe = cuda_lib
+    cfg, inp, rt, dp, xd, dy = _small_training_case(name)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    offs = torch.from_numpy(dp.offsets.astype(np.int64)).to(torch.int32).to(DEV)
+    xdd = xd.to(DEV).contiguous()
+    y, cache = moe.moe_experts_forward_training(ex, xdd, offs)
+    y_ref = moe.moe_experts_forward_dispatched(ex, xdd, offs)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.uint8), y_ref.view(torch.uint8))
+    # The cached pre-activation g is the oracle's W_gate x (one rounding).
+    gref = np.zeros((xd.shape[0], cfg.I))
+    gabs = np.zeros((xd.shape[0], cfg.I))
+    for e in range(cfg.E):
+        lo, hi = int(dp.offsets[e]), int(dp.offsets[e + 1])
+        gref[lo:hi] = f64(xd[lo:hi]) @ f64(inp["gate"][e]).T
+        gabs[lo:hi] = np.abs(f64(xd[lo:hi])) @ np.abs(f64(inp["gate"][e])).T
+    _grad_close(f64(cache.g), gref, gabs, cfg.torch_dtype, "cache g")
+
+    gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
+    torch.cuda.synchronize()
+    # cache.backward consumes the cache the forward produced (checked above).
+    ref = oracle.experts_backward(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy,
+                                  cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
+    n = int(dp.offsets[-1])
+    _grad_close(f64(gr.dx_dispatched)[:n], ref.dx_dispatched[:n], ref.dx_abs[:n], cfg.torch_dtype, "dx_dispatched")
+    _grad_close(f64(gr.dgate), ref.dgate, ref.dgate_abs, cfg.torch_dtype, "dgate")
+    _grad_close(f64(gr.dup), ref.dup, ref.dup_abs, cfg.torch_dtype, "dup")
+    _grad_close(f64(gr.ddown), ref.ddown, ref.ddown_abs, cfg.torch_dtype, "ddown")
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["f32_contract", "bf16_fine", "f16_zipf", "bf16_ragged"])
+def test_combine_and_dispatch_backward_parity(cuda_lib, name):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    inp = workloads.generate(cfg, weights=False)
+    rt = moe_oracle.route(inp["logits"], cfg.top_k, cfg.renormalize)
+    dp = moe_oracle.dispatch(rt.indices, cfg.E)
+    g = torch.Generator().manual_seed(17)
+    n = cfg.T * cfg.top_k
+    y = torch.randn(n, cfg.H, generator=g).to(cfg.torch_dtype)
+    go = torch.randn(cfg.T, cfg.H, generator=g).to(cfg.torch_dtype)
+    w = torch.from_numpy(rt.weights).to(cfg.torch_dtype)
+    inv = torch.from_numpy(dp.inv.astype(np.int64)).to(torch.int32)
+    dexp, dw = moe.moe_combine_backward(y.to(DEV), inv.to(DEV), w.to(DEV), go.to(DEV))
+    torch.cuda.synchronize()
+    ref_dexp, ref_dw = oracle.combine_backward(y, dp.inv, f64(w), go, cfg.T, cfg.top_k)
+    used = int(dp.offsets[-1])
+    got = f64(dexp)[:used]
+    ref = ref_dexp[:used]
+    assert_nan_positions_equal(got, ref, "dexpert")
+    fin = np.isfinite(ref)
+    # one rounding of the exact FP32 product to the dtype (half a subnormal
+    # step near zero for f16)
+    tiny = 2.0 ** -25 if cfg.torch_dtype == torch.float16 else 1e-30
+    assert (np.abs(got[fin] - ref[fin]) <= _ULP[cfg.torch_dtype] * np.abs(ref[fin]) + tiny).all()
+    gdw = f64(dw)
+    assert_nan_positions_equal(gdw, ref_dw, "dweights")
+    fin = np.isfinite(ref_dw)
+    scale = (np.abs(f64(go))[:, None, :] * np.abs(f64(y))[dp.inv.astype(np.int64).reshape(cfg.T, cfg.top_k) % n]).sum(-1)
+    assert (np.abs(gdw[fin] - ref_dw[fin]) <= 1e-5 * scale[fin] + 1e-30).all()
+
+    dx = moe.moe_dispatch_backward(dexp, inv.to(DEV), cfg.T, cfg.top_k)
+    torch.cuda.synchronize()
+    ref_dx = oracle.dispatch_backward(dexp.cpu(), dp.inv, cfg.T, cfg.top_k)
+    gdx = f64(dx)
+    assert_nan_positions_equal(gdx, ref_dx, "dx")
+    fin = np.isfinite(ref_dx)
+    assert (np.abs(gdx[fin] - ref_dx[fin]) <= _ULP[cfg.torch_dtype] * np.abs(ref_dx[fin]) * 1.0000001 + tiny).all()
+
+
+def test_dispatch_backward_invalid_slot_gives_nan_row(cuda_lib):
+    moe = cuda_lib
+    idx = torch.tensor([[0, 1], [1, 9], [2, 0]], dtype=torch.int32)   # token 1 holds an invalid index
+    d = moe.moe_dispatch(idx.to(DEV), 3)
+    dinput = torch.randn(6, 8).to(torch.bfloat16).to(DEV)
+    dx = moe.moe_dispatch_backward(dinput, d.inv, 3, 2).cpu().float()
+    assert torch.isnan(dx[1]).all() and torch.isfinite(dx[0]).all() and torch.isfinite(dx[2]).all()
+
+
+def test_whole_training_step_matches_oracle(cuda_lib):
+    """One whole first-order step on the reduced fine-grained workload:
+    route -> dispatch -> training forward; then combine backward -> experts
+    backward -> dispatch backward, and the router gradient of the FP32
+    dweights (softmax, renormalize); every stage checked against the oracle
+    on the inputs that stage received on the GPU."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_fine"]
+    inp = workloads.generate(cfg)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, w = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
+    g = torch.Generator().manual_seed(23)
+    go = (torch.randn(cfg.T, cfg.H, generator=g)).to(cfg.torch_dtype)
+    dexp, dw = moe.moe_combine_backward(y, disp.inv, w, go.to(DEV))
+    gr = moe.moe_experts_backward(ex, cache, dexp)
+    dx = moe.moe_dispatch_backward(gr.dx_dispatched, disp.inv, cfg.T, cfg.top_k)
+    o = Opt("softmax", True, 1.0)
+    dl = moe.moe_router_backward(d["logits"], idx, dw, o)
+    torch.cuda.synchronize()
+
+    rt = moe_oracle.route(inp["logits"], cfg.top_k, cfg.renormalize)
+    dp = moe_oracle.dispatch(rt.indices, cfg.E)
+    assert np.array_equal(u32(idx), rt.indices)
+    assert np.array_equal(u32(disp.inv), dp.inv)
+    # Each stage against the oracle on the GPU's inputs to that stage.
+    xd = inp["x"][torch.from_numpy(dp.row_src.astype(np.int64) // cfg.top_k)]
+    ref_dexp, ref_dw = oracle.combine_backward(y.cpu(), dp.inv, rt.weights, go, cfg.T, cfg.top_k)
+    ref_gr = oracle.experts_backward(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dexp.cpu(),
+                                     cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
+    ref_dx = oracle.dispatch_backward(gr.dx_dispatched.cpu(), dp.inv, cfg.T, cfg.top_k)
+    ref_dl, _ = oracle.selected_router_backward(inp["logits"], rt.indices, dw.cpu(), o)
+    dw_abs = (np.abs(f64(go))[:, None, :] * np.abs(f64(y))[dp.inv.astype(np.int64).reshape(cfg.T, cfg.top_k)]).sum(-1)
+    _grad_close(f64(dw), ref_dw, dw_abs, torch.float32, "dweights")
+    n = cfg.T * cfg.top_k
+    _grad_close(f64(gr.dx_dispatched)[:n], ref_gr.dx_dispatched[:n], ref_gr.dx_abs[:n], cfg.torch_dtype,
+                "dx_dispatched")
+    for name in ("dgate", "dup", "ddown"):
+        _grad_close(f64(getattr(gr, name)), getattr(ref_gr, name), getattr(ref_gr, name + "_abs"), cfg.torch_dtype,
+                    name)
+    dx_abs = oracle.dispatch_backward(np.abs(f64(gr.dx_dispatched)), dp.inv, cfg.T, cfg.top_k)
+    _grad_close(f64(dx), ref_dx, dx_abs, cfg.torch_dtype, "dx")
+    dl_abs = o.scale * np.abs(f64(dw)).sum(axis=1, keepdims=True) * np.ones((1, cfg.E))
+    _grad_close(f64(dl), ref_dl, dl_abs, cfg.torch_dtype, "dlogits")
+    assert moe.moe_device_status() == 0

@@ -607,7 +607,7 @@ moe_status moe_experts_forward_training(const moe_experts* ex, const void* x_dis
 size_t moe_experts_backward_workspace_size(const moe_experts* ex, int64_t rows) {
   if (ex == nullptr || rows < 0) return 0;
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(ex->I);
-  return align_up(n * 4 + 1, 256) + 2 * align_up(n * dtype_size(ex->dtype) + 1, 256);
+  return align_up(n * 4 + 1, 256) + 2 * align_up(n * dtype_size(ex->dtype) + 1, 256) + moe::TC_SCHED_BYTES;
 }
 
 moe_status moe_experts_backward(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets, int64_t rows,
@@ -629,9 +629,17 @@ moe_status moe_experts_backward(const moe_experts* ex, const void* x_dispatched,
   moe::TrainBuffers b{x_dispatched, h, cache_g, cache_u, dexpert, ex->gate, ex->up, ex->down,
                       reinterpret_cast<float*>(ws), ws + dh_bytes, ws + dh_bytes + d_bytes, dx_dispatched,
                       dgate, dup, ddown};
-  cudaError_t err = moe::launch_experts_backward(ex->dtype, b, offsets, static_cast<int>(ex->E), rows, ex->H, ex->I,
-                                                 static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return cuda_fail(err, "moe_experts_backward launch");
+  cudaError_t err;
+  const char* why = nullptr;
+  if (ex->dtype == MOE_F32 || rows == 0) {
+    err = moe::launch_experts_backward(ex->dtype, b, offsets, static_cast<int>(ex->E), rows, ex->H, ex->I,
+                                       static_cast<cudaStream_t>(stream));
+  } else {
+    uint32_t* sched = reinterpret_cast<uint32_t*>(ws + dh_bytes + 2 * d_bytes);
+    err = moe::launch_experts_backward_tc(ex->dtype, b, offsets, static_cast<int>(ex->E), rows, ex->H, ex->I, sched,
+                                          ex->num_sms, static_cast<cudaStream_t>(stream), &why);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "moe_experts_backward launch", why);
   return ok();
 }
 

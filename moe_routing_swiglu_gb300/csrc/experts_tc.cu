@@ -650,6 +650,10 @@ cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up,
                               stream, why);
 }
 
+cudaError_t device_status_ptr(uint32_t** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_moe_device_status);
+}
+
 cudaError_t read_device_status(uint32_t* code, bool clear) {
   cudaError_t err = cudaDeviceSynchronize();
   if (err != cudaSuccess) return err;

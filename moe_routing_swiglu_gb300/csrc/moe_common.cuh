@@ -300,12 +300,31 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// MN-major operand with 128-byte swizzle: atoms of 8 K-rows x 128 B (64
+// 16-bit MN elements), as a TMA box {64 (MN, inner), rows (K)} lays them out;
+// `lbo` is the byte distance between MN-adjacent atoms (the next 64 MN
+// elements), `sbo` between K-adjacent atoms (the next 8 K-rows).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16: FP32 accumulator (bits 4-5
 // = 1), A and B format (bits 7-9 and 10-12: 0 = F16, 1 = BF16), both operands
 // K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with A (bit 15) and / or B (bit 16) MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_major(bool bf16, int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f16(bf16, M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 }  // namespace moe

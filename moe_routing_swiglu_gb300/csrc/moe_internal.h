@@ -87,6 +87,8 @@ cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up,
                               int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
                               cudaStream_t stream, const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
+// Device address of the status word the bounded waits report into.
+cudaError_t device_status_ptr(uint32_t** p);
 
 // ---- first-order training (train_router.cu, train_experts.cu, combine.cu)
 struct RouterParams {
@@ -123,8 +125,17 @@ struct TrainBuffers {
   float* dup;        // out [E, I, H]
   float* ddown;      // out [E, H, I]
 };
+// CUDA-core backward (every dtype; the F32 path).
 cudaError_t launch_experts_backward(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,
                                     int64_t rows, int64_t H, int64_t I, cudaStream_t stream);
+// dg = dh * u * SiLU'(g), du = dh * SiLU(g) over n elements, rounded to the dtype.
+cudaError_t launch_silu_backward(moe_dtype dtype, const float* dh, const void* g, const void* u, int64_t n,
+                                 void* dg, void* du, cudaStream_t stream);
+// Tensor-core backward (F16/BF16): dgrad and wgrad grouped GEMMs on tcgen05
+// (experts_bwd_tc.cu); sched is one uint32 of device memory.
+cudaError_t launch_experts_backward_tc(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,
+                                       int64_t rows, int64_t H, int64_t I, uint32_t* sched, int num_sms,
+                                       cudaStream_t stream, const char** why);
 cudaError_t launch_bounded_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 
 }  // namespace moe

@@ -11,9 +11,11 @@
 //   ddown[e] += dy h^T, dgate[e] += dg x^T, dup[e] += du x^T  (wgrad GEMMs,
 //   K = the expert's rows)
 // SiLU'(g) = s (1 + g (1 - s)) with s the logistic function of g.
-// The GEMMs accumulate in FP32 on CUDA cores (64 x 64 output tiles, 4 x 4 per
-// thread), for every dtype; dh stays FP32, dg and du are rounded to the dtype
-// like the forward's activations, the weight gradients are FP32.
+// Here the GEMMs accumulate in FP32 on CUDA cores (64 x 64 output tiles, 4 x 4
+// per thread): the F32 experts' path (no TF32, as in the forward); F16/BF16
+// run them on the tensor cores (experts_bwd_tc.cu) and share the SiLU
+// backward below. dh stays FP32, dg and du are rounded to the dtype like the
+// forward's activations, the weight gradients are FP32.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -27,30 +29,74 @@ constexpr int CB_MAX_K = 1024;
 // One block per token: dexpert[inv[t,j]] = w[t,j] * dout[t] and
 // dweights[t,j] = <dout[t], y[inv[t,j]]> (FP32, a fixed reduction tree). A
 // slot whose inv entry is out of range gets a NaN dweight and no dexpert row.
-template <typename T, typename TW>
+// Each thread owns NV consecutive columns (16-byte vectors when the rows are
+// 16-byte multiples); slots are taken in groups of 8.
+template <typename T, int NV>
+struct VecIO {
+  static __device__ __forceinline__ void load(const T* p, float (&v)[NV]) {
+    if constexpr (NV * sizeof(T) == 16) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(p);
+      const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = to_f32(e[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = to_f32(p[i]);
+    }
+  }
+  static __device__ __forceinline__ void store(T* p, const float (&v)[NV]) {
+    if constexpr (NV * sizeof(T) == 16) {
+      uint4 raw;
+      T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) e[i] = from_f32<T>(v[i]);
+      *reinterpret_cast<uint4*>(p) = raw;
+    } else {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) p[i] = from_f32<T>(v[i]);
+    }
+  }
+};
+
+template <typename T, typename TW, int NV>
 __global__ void __launch_bounds__(256) combine_backward_kernel(
     const T* __restrict__ y, const uint32_t* __restrict__ inv, const TW* __restrict__ w,
     const T* __restrict__ dout, int64_t T_tokens, int k, int64_t H, uint32_t rows, T* __restrict__ dexpert,
     float* __restrict__ dweights) {
   __shared__ float s_part[8][8];  // [slot in group][warp]
+  __shared__ uint32_t s_row[8];
+  __shared__ float s_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const float qnan = __int_as_float(0x7FC00000);
   for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
     for (int j0 = 0; j0 < k; j0 += 8) {
       const int nj = k - j0 < 8 ? k - j0 : 8;
+      __syncthreads();
+      if (threadIdx.x < nj) {
+        s_row[threadIdx.x] = inv[t * k + j0 + threadIdx.x];
+        s_w[threadIdx.x] = to_f32(w[t * k + j0 + threadIdx.x]);
+      }
+      __syncthreads();
       float part[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) part[q] = 0.0f;
-      for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
-        const float go = to_f32(dout[t * H + c]);
+      for (int64_t c = static_cast<int64_t>(threadIdx.x) * NV; c < H; c += static_cast<int64_t>(blockDim.x) * NV) {
+        float go[NV];
+        VecIO<T, NV>::load(dout + t * H + c, go);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (q < nj) {
-            const uint32_t r = inv[t * k + j0 + q];
+            const uint32_t r = s_row[q];
             if (r < rows) {
-              part[q] = fmaf(go, to_f32(y[static_cast<int64_t>(r) * H + c]), part[q]);
-              dexpert[static_cast<int64_t>(r) * H + c] = from_f32<T>(to_f32(w[t * k + j0 + q]) * go);
+              float yv[NV], dv[NV];
+              VecIO<T, NV>::load(y + static_cast<int64_t>(r) * H + c, yv);
+#pragma unroll
+              for (int i = 0; i < NV; ++i) {
+                part[q] = fmaf(go[i], yv[i], part[q]);
+                dv[i] = s_w[q] * go[i];
+              }
+              VecIO<T, NV>::store(dexpert + static_cast<int64_t>(r) * H + c, dv);
             }
           }
         }
@@ -64,12 +110,10 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(
       }
       __syncthreads();
       if (threadIdx.x < nj) {
-        float s = 0.0f;
-        for (int wi = 0; wi < nwarps; ++wi) s += s_part[threadIdx.x][wi];
-        const uint32_t r = inv[t * k + j0 + threadIdx.x];
-        dweights[t * k + j0 + threadIdx.x] = r < rows ? s : qnan;
+        float sum = 0.0f;
+        for (int wi = 0; wi < nwarps; ++wi) sum += s_part[threadIdx.x][wi];
+        dweights[t * k + j0 + threadIdx.x] = s_row[threadIdx.x] < rows ? sum : qnan;
       }
-      __syncthreads();
     }
   }
 }
@@ -277,9 +321,18 @@ template <typename T, typename TW>
 cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const void* w, const void* dout, int64_t T_tokens,
                                int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s) {
   const int blocks = static_cast<int>(T_tokens < 65536 ? T_tokens : 65536);
-  combine_backward_kernel<T, TW><<<blocks, 256, 0, s>>>(
-      static_cast<const T*>(y), inv, static_cast<const TW*>(w), static_cast<const T*>(dout), T_tokens, k, H,
-      static_cast<uint32_t>(T_tokens * k), static_cast<T*>(dexpert), dweights);
+  constexpr int NV = 16 / static_cast<int>(sizeof(T));
+  const bool vec = (H * static_cast<int64_t>(sizeof(T))) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dout) % 16 == 0 && reinterpret_cast<uintptr_t>(dexpert) % 16 == 0;
+  const auto* yp = static_cast<const T*>(y);
+  const auto* wp = static_cast<const TW*>(w);
+  const auto* dp = static_cast<const T*>(dout);
+  auto* ep = static_cast<T*>(dexpert);
+  const uint32_t rows = static_cast<uint32_t>(T_tokens * k);
+  if (vec)
+    combine_backward_kernel<T, TW, NV><<<blocks, 256, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
+  else
+    combine_backward_kernel<T, TW, 1><<<blocks, 256, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
   return cudaGetLastError();
 }
 
@@ -312,6 +365,29 @@ cudaError_t launch_combine_backward(const void* y_dispatched, moe_dtype dtype, c
       return combine_backward_w<__nv_bfloat16>(y_dispatched, inv, weights, weights_dtype, grad_out, T, top_k, H,
                                                dexpert, dweights, stream);
   }
+}
+
+cudaError_t launch_silu_backward(moe_dtype dtype, const float* dh, const void* g, const void* u, int64_t n,
+                                 void* dg, void* du, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(n / 256 + 1 < 152 * 16 ? n / 256 + 1 : 152 * 16);
+  switch (dtype) {
+    case MOE_F32:
+      silu_backward_kernel<float><<<blocks, 256, 0, stream>>>(dh, static_cast<const float*>(g),
+                                                              static_cast<const float*>(u), n,
+                                                              static_cast<float*>(dg), static_cast<float*>(du));
+      break;
+    case MOE_F16:
+      silu_backward_kernel<__half><<<blocks, 256, 0, stream>>>(dh, static_cast<const __half*>(g),
+                                                               static_cast<const __half*>(u), n,
+                                                               static_cast<__half*>(dg), static_cast<__half*>(du));
+      break;
+    default:
+      silu_backward_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+          dh, static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(u), n,
+          static_cast<__nv_bfloat16*>(dg), static_cast<__nv_bfloat16*>(du));
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_experts_backward(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,

@@ -188,8 +188,9 @@ class ExpertGrads:
     dgate: np.ndarray          # [E, I, H]
     dup: np.ndarray            # [E, I, H]
     ddown: np.ndarray          # [E, H, I]
-    # The same sums over |terms| (|dg| |W_gate| + |du| |W_up|, |dg|^T |x|, ...):
-    # the scale a rounding error of each sum is measured against.
+    # The same sums over |terms| carried through the chain (|dy| |W_down| for
+    # dh, then |dh| |u| |SiLU'(g)|, ...): the scale a rounding error of each
+    # entry is measured against.
     dx_abs: np.ndarray | None = None
     dgate_abs: np.ndarray | None = None
     dup_abs: np.ndarray | None = None
@@ -236,9 +237,14 @@ def experts_backward(x_dispatched, gate, up, down, offsets, dexpert, cache=None)
         dx[lo:hi] = dG @ Wg[e] + dU @ Wu[e]
         dWg[e] = dG.T @ X
         dWu[e] = dU.T @ X
-        ab[0][lo:hi] = np.abs(dG) @ np.abs(Wg[e]) + np.abs(dU) @ np.abs(Wu[e])
-        ab[1][e] = np.abs(dG).T @ np.abs(X)
-        ab[2][e] = np.abs(dU).T @ np.abs(X)
+        # |.| carried through the chain: each entry's sum of |terms|, with the
+        # intermediate gradients replaced by their own |term| sums.
+        dH_abs = np.abs(dY) @ np.abs(Wd[e])
+        dG_abs = dH_abs * np.abs(U) * np.abs(_silu_grad(G))
+        dU_abs = dH_abs * np.abs(_silu(G))
+        ab[0][lo:hi] = dG_abs @ np.abs(Wg[e]) + dU_abs @ np.abs(Wu[e])
+        ab[1][e] = dG_abs.T @ np.abs(X)
+        ab[2][e] = dU_abs.T @ np.abs(X)
         ab[3][e] = np.abs(dY).T @ np.abs(Hh)
     return ExpertGrads(dx, dWg, dWu, dWd, *ab)
 

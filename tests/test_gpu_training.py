@@ -226,3 +226,35 @@ def test_whole_training_step_matches_oracle(cuda_lib):
     dl_abs = o.scale * np.abs(f64(dw)).sum(axis=1, keepdims=True) * np.ones((1, cfg.E))
     _grad_close(f64(dl), ref_dl, dl_abs, cfg.torch_dtype, "dlogits")
     assert moe.moe_device_status() == 0
+
+
+def test_experts_backward_full_size_sampled_experts(cuda_lib):
+    """The fine-grained prefill workload at full size (the benchmark's launch
+    configuration): the tensor-core backward against the oracle on three
+    sampled experts (their rows, weights and gradients cut out of the full
+    problem), including the expert with the most rows."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[2]
+    inp = workloads.generate(cfg)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, w = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
+    g = torch.Generator().manual_seed(29)
+    dy = (torch.randn(cfg.T * cfg.top_k, cfg.H, generator=g) * 0.5).to(cfg.torch_dtype)
+    gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
+    torch.cuda.synchronize()
+    offs = u32(disp.offsets).astype(np.int64)
+    counts = np.diff(offs)
+    for e in sorted({0, 77, int(np.argmax(counts))}):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        sub_off = np.array([0, hi - lo])
+        ref = oracle.experts_backward(cache.x_dispatched[lo:hi].cpu(), inp["gate"][e:e + 1], inp["up"][e:e + 1],
+                                      inp["down"][e:e + 1], sub_off, dy[lo:hi],
+                                      cache=(cache.g[lo:hi].cpu(), cache.u[lo:hi].cpu(), cache.h[lo:hi].cpu()))
+        _grad_close(f64(gr.dx_dispatched[lo:hi]), ref.dx_dispatched, ref.dx_abs, cfg.torch_dtype, f"dx (expert {e})")
+        _grad_close(f64(gr.dgate[e:e + 1]), ref.dgate, ref.dgate_abs, cfg.torch_dtype, f"dgate (expert {e})")
+        _grad_close(f64(gr.dup[e:e + 1]), ref.dup, ref.dup_abs, cfg.torch_dtype, f"dup (expert {e})")
+        _grad_close(f64(gr.ddown[e:e + 1]), ref.ddown, ref.ddown_abs, cfg.torch_dtype, f"ddown (expert {e})")
+    assert moe.moe_device_status() == 0

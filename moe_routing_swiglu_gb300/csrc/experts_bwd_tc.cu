@@ -67,19 +67,23 @@ struct BwdCfg {
   static constexpr int N_A = (MODE == WGRAD_D) ? 1 : 2;                // MMAs per k-step
   static constexpr int B_BYTES = DGRAD ? TBM * 128 : (WN / 64) * BOX;  // B operand per stage
   static constexpr int STAGE_BYTES = N_A * A_BYTES + B_BYTES;
-  static constexpr int STAGES = STAGE_SMEM / STAGE_BYTES;
+  // WGRAD keeps 32 KB for its FP32 output transposes.
+  static constexpr int STAGES = (DGRAD ? STAGE_SMEM : STAGE_SMEM - 32 * 1024) / STAGE_BYTES >= 3
+                                    ? (DGRAD ? STAGE_SMEM : STAGE_SMEM - 32 * 1024) / STAGE_BYTES
+                                    : 3;
   static constexpr int ACC_N = DGRAD ? TBM : WN;                       // accumulator columns per MMA
   static constexpr int ACC = (N_A * ACC_N * 2 <= static_cast<int>(TMEM_COLS)) ? 2 : 1;
   static constexpr uint32_t ACC_COLS = TMEM_COLS / ACC;
   static constexpr uint32_t D1 = ACC_N;                                // second accumulator
   static constexpr int SMEM_STAGES = 0;
+  static constexpr int XPOSE_WARP = DGRAD ? XPOSE_BYTES : 32 * 33 * 4;  // per epilogue warp
   static constexpr int SMEM_XPOSE = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_BYTES;
+  static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_WARP;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
   static constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
   static constexpr int SMEM_TILES = SMEM_MISC + 16;
-  static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
+  static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + (DGRAD ? 4 * (ROUTE_MAX_E + 1) : 0);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -366,7 +370,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;
     const int quad = warp & 3;
     const int half = ew >> 2;
-    uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * XPOSE_BYTES);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * C::XPOSE_WARP);
+    float* xf = reinterpret_cast<float*>(smem + C::SMEM_XPOSE + ew * C::XPOSE_WARP);  // WGRAD: [32][33]
     const int rd_tok = lane >> 2;
     const int rd_part = lane & 3;
     for (uint32_t it = 0;; ++it) {
@@ -426,8 +431,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
-        // lane = output row m, TMEM column = output column n; FP32 [E, M, N].
-        const int64_t m = static_cast<int64_t>(w.mb) * BM + quad * 32 + lane;
+        // TMEM lane = output row m, column = output n; FP32 [E, M, N]. Each
+        // 32 x 32 block goes through a padded shared transpose (row r at
+        // r * 33: conflict-free both ways) so that every store instruction
+        // writes one output row's 32 consecutive floats.
+        const int64_t m_base = static_cast<int64_t>(w.mb) * BM + quad * 32;
         const bool empty_expert = w.kb_count == 0;
         for (int c0 = 32 * half; c0 < WN; c0 += 64) {
           for (int blk = 0; blk < C::N_A; ++blk) {
@@ -439,20 +447,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;
             }
-            const int64_t n = static_cast<int64_t>(w.nb) * WN + c0;
-            if (m < args.m_out) {
-              float* o = static_cast<float*>(blk == 0 ? args.out0 : args.out1) +
-                         (static_cast<int64_t>(w.e) * args.m_out + m) * args.n_out + n;
-              if (n + 32 <= args.n_out) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  *reinterpret_cast<uint4*>(o + 4 * q) =
-                      make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-              } else {
-                for (int j = 0; j < 32; ++j)
-                  if (n + j < args.n_out) o[j] = __uint_as_float(v[j]);
-              }
-            }
+            for (int j = 0; j < 32; ++j) xf[lane * 33 + j] = __uint_as_float(v[j]);
+            __syncwarp();
+            const int64_t n = static_cast<int64_t>(w.nb) * WN + c0 + lane;
+            float* ob = static_cast<float*>(blk == 0 ? args.out0 : args.out1) +
+                        static_cast<int64_t>(w.e) * args.m_out * args.n_out;
+            const int rows_here = static_cast<int>(args.m_out - m_base < 32 ? args.m_out - m_base : 32);
+            if (n < args.n_out)
+              for (int r = 0; r < rows_here; ++r) ob[(m_base + r) * args.n_out + n] = xf[r * 33 + lane];
+            __syncwarp();
           }
         }
       }

@@ -8,7 +8,8 @@ dispatch run once to set up the stage's inputs, then the chosen stage runs
 Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
 row_src), down, combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
-variant in ``workloads.GROUPED``).
+variant in ``workloads.GROUPED``), and backward (the experts' backward of
+first-order training on a random output gradient).
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="cfg2", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
                     choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "combine", "forward",
-                             "route_grouped"])
+                             "route_grouped", "backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     cfg = names[args.workload]
@@ -56,6 +57,10 @@ def main(argv=None):
         bias = None if bias is None else bias.to(dev)
         opts = moe.GroupRoutingOptions(r.top_k, r.groups, r.selected_groups, r.group_top_two, r.renormalize,
                                        r.scale)
+    if args.stage == "backward":
+        _, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
+        g = torch.Generator().manual_seed(7)
+        dy = torch.randn(cfg.T * cfg.top_k, cfg.H, generator=g).to(cfg.torch_dtype).to(dev)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         if args.stage == "route":
@@ -70,6 +75,8 @@ def main(argv=None):
             moe.moe_experts_down(ex, h, disp.offsets, out=y)
         elif args.stage == "route_grouped":
             moe.moe_route_sigmoid_grouped(d["logits"], bias, opts, indices=idx, weights=w)
+        elif args.stage == "backward":
+            moe.moe_experts_backward(ex, cache, dy)
         elif args.stage == "combine":
             moe.moe_combine(y, disp.inv, w)
         else:

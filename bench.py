@@ -6,12 +6,13 @@
 
 One step is one pass of the whole chain over one batch of the BF16
 fine-grained prefill workload (T=4096, H=2048, I=768, E=128, top_k=8,
-renormalize), inputs resident in HBM. The step's C-ABI calls are captured
-once in a CUDA graph; each timed step is one replay bracketed by CUDA events
-on the launching stream, and L2 is flushed between steps outside the events
+renormalize), inputs resident in HBM. One moe_forward call is captured once
+in a CUDA graph; each timed step is one replay bracketed by CUDA events on
+the launching stream, and L2 is flushed between steps outside the events
 (a 256 MiB write, then a 256 MiB read so the flush's dirty lines are written
 back before the step). The per-stage times come from a second run that
-launches the calls directly with events between the stages. Under torchrun each
+launches the split C-ABI calls (route, dispatch, gate/up, down, combine)
+directly with events between the stages. Under torchrun each
 rank runs its own batch (weak scaling, replicated experts, no collective on
 the data path); the time is the maximum over ranks.
 
@@ -56,7 +57,6 @@ PREFILL = workloads.CONFIGS[2]
 DECODE = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 7  # route, dispatch count + scatter + gather, gate/up GEMM, down GEMM, combine
-# (plus one 4-byte memset node before each GEMM that resets its tile counter)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -237,6 +237,15 @@ class Chain:
         if rc:
             raise RuntimeError("a C-ABI call failed: " + lib.moe_last_error().decode())
 
+    def forward(self, stream):
+        """The whole chain as one moe_forward call (what a user runs)."""
+        c, lib, P = self.cfg, self.lib, self.moe._ptr
+        rc = lib.moe_forward(self.ex.handle, P(self.d["x"]), P(self.d["logits"]), self.dt, c.T, c.top_k,
+                             int(c.renormalize), P(self.out), P(self.idx), P(self.w), P(self.fws), self.fws.numel(),
+                             ctypes.c_void_p(stream.cuda_stream))
+        if rc:
+            raise RuntimeError("moe_forward failed: " + lib.moe_last_error().decode())
+
     def touched_experts(self) -> int:
         return int((self.counts.cpu() > 0).sum())
 
@@ -274,18 +283,18 @@ def timed_steps(chain, stream, flush, steps, warmup):
 
 
 def capture_step(chain):
-    """The step's C-ABI calls captured once into a CUDA graph (the same
-    kernels and memsets, replayed without host launch overhead)."""
+    """One moe_forward call captured into a CUDA graph (the same kernels,
+    replayed without host launch overhead)."""
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
         for _ in range(2):
-            chain.step(side)
+            chain.forward(side)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        chain.step(torch.cuda.current_stream())
+        chain.forward(torch.cuda.current_stream())
     torch.cuda.synchronize()
     return g
 
@@ -479,6 +488,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_s, h2d, d2h = e2e_steps(chain, stream, flush, min(args.steps, 20))
     e2e_s = max_over_ranks(e2e_s, world, dev)
     dec_stages, dec_total = timed_steps(decode, stream, flush, min(args.steps, 50), args.warmup)
+    dec_graph = capture_step(decode)
+    dec_graph_total = timed_graph_steps(dec_graph, stream, flush, min(args.steps, 200), args.warmup)
     grouped_cfg, grouped_routing = workloads.GROUPED["bf16_prefill_grouped"]
     assert grouped_cfg is PREFILL
     chain.use_grouped_routing(grouped_routing)
@@ -536,7 +547,7 @@ def run_ours(args, rank, world, local_rank):
     d = DECODE
     dec_touched = decode.touched_experts()
     dec_bytes = dec_touched * 3 * d.I * d.H * es
-    dec_fwd = float(dec_total) / min(args.steps, 50)
+    dec_fwd = float(dec_graph_total) / min(args.steps, 200)
     dec_exp = float(dec_stages[2] + dec_stages[3])
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
@@ -551,11 +562,13 @@ def run_ours(args, rank, world, local_rank):
         "route_dispatch_us": {"route": round(t_route * 1e6, 2), "dispatch": round(t_disp * 1e6, 2),
                               "total": round((t_route + t_disp) * 1e6, 2)},
         "combine_us": round(t_comb * 1e6, 2),
-        "timing": {"value": f"{args.steps} CUDA-graph replays of the step (its {KERNELS_PER_STEP} kernels and 2 memsets), "
-                            "one event pair around each replay",
+        "timing": {"value": f"{args.steps} CUDA-graph replays of one moe_forward call (its {KERNELS_PER_STEP} "
+                            "kernels), one event pair around each replay",
                    "stages": f"{stage_steps} steps launched directly with events between the stages "
                              f"({stage_total / stage_steps * 1e6:.1f} us per step including the events)"},
         "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
+                   "timing": "CUDA-graph replays of the decode step (forward); experts_us from the staged run",
+                   "frac_hbm_forward": round(dec_bytes / dec_fwd / 1e9 / peaks["hbm_gbs"], 4),
                    "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dec_touched,
                    "touched_weight_bytes": dec_bytes,
                    "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),

@@ -139,7 +139,7 @@ moe_status check_current_device(const moe_experts* ex) {
 // row_src, -> h) or down (h -> y).
 moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const moe::TcGather* gather,
                      const uint32_t* offsets, int64_t rows, void* out, void* sched, cudaStream_t s,
-                     const moe::TcCache* cache = nullptr) {
+                     const moe::TcCache* cache = nullptr, bool sched_zeroed = false) {
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32) {
@@ -150,7 +150,8 @@ moe_status run_stage(const moe_experts* ex, bool gate_up, const void* a, const m
                                        ex->I, static_cast<float*>(out), s);
   } else {
     err = moe::launch_experts_tc(ex->tc, ex->dtype, gate_up, a, gather, cache, offsets, static_cast<int>(ex->E),
-                                 rows, ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why);
+                                 rows, ex->H, ex->I, out, static_cast<uint32_t*>(sched), ex->num_sms, s, &why,
+                                 sched_zeroed);
   }
   if (err != cudaSuccess) return cuda_fail(err, gate_up ? "gate/up GEMM launch" : "down GEMM launch", why);
   return MOE_OK;
@@ -209,15 +210,18 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   // reads each dispatched row straight from x through row_src. Larger
   // batches: dispatch also writes x_dispatched, which the GEMM streams with
   // TMA (faster there than gathering rows from every weight tile).
+  // The dispatch's scatter kernel zeroes the two GEMMs' tile counters, so
+  // the chain is kernels only (each launched as a dependent of the previous).
+  uint32_t* sched = reinterpret_cast<uint32_t*>(ws + L.sched);
   cudaError_t err = route(indices, weights, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
   err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
-                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s);
+                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched);
   if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
   const moe::TcGather gather{x, row_src, top_k, T};
-  st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, ws + L.sched, s);
+  st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, sched, s, nullptr, true);
   if (st != MOE_OK) return st;
-  st = run_stage(ex, false, h, nullptr, offsets, rows, yd, ws + L.sched, s);
+  st = run_stage(ex, false, h, nullptr, offsets, rows, yd, sched + 1, s, nullptr, true);
   if (st != MOE_OK) return st;
   err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward combine launch");

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
   __shared__ uint32_t s_row[COMBINE_MAX_K];
   __shared__ float s_w[COMBINE_MAX_K];
   __shared__ int s_bad;
+  grid_dependency_wait();
   const float qnan = __int_as_float(0x7FC00000);
   for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
     __syncthreads();
@@ -119,16 +120,10 @@ cudaError_t launch_combine_t(const void* y, const uint32_t* inv, const void* w, 
   int threads = 256;
   const int64_t per_thread = vec ? Vec<T>::N : 1;
   while (threads > 32 && static_cast<int64_t>(threads / 2) * per_thread >= H) threads /= 2;
-  if (vec) {
-    combine_kernel<T, TW, true, WEIGHTED><<<blocks, threads, 0, stream>>>(
-        static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
-        static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
-  } else {
-    combine_kernel<T, TW, false, WEIGHTED><<<blocks, threads, 0, stream>>>(
-        static_cast<const T*>(y), inv, static_cast<const TW*>(w), T_tokens, k, H,
-        static_cast<uint32_t>(T_tokens * k), static_cast<T*>(out));
-  }
-  return cudaGetLastError();
+  auto kern = vec ? combine_kernel<T, TW, true, WEIGHTED> : combine_kernel<T, TW, false, WEIGHTED>;
+  return launch_dependent(kern, dim3(blocks), dim3(threads), 0, stream, static_cast<const T*>(y), inv,
+                          static_cast<const TW*>(w), T_tokens, k, H, static_cast<uint32_t>(T_tokens * k),
+                          static_cast<T*>(out));
 }
 
 template <typename T>

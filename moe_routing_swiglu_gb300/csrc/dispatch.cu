@@ -5,8 +5,8 @@
 // the optional x_dispatched copy below serves the split API.
 //
 // The flat slots f = t*k + j are cut into chunks of DISPATCH_CHUNK; two
-// launches make the layout stable (row order inside an expert = ascending f)
-// without atomics on the output:
+// launches (one when a single chunk holds every slot) make the layout stable
+// (row order inside an expert = ascending f) without atomics on the output:
 //   1. count:   per-chunk expert histogram          -> scratch[c][e]
 //   2. scatter: every chunk block re-derives what it needs from all chunks'
 //               histograms (expert totals -> exclusive scan -> offsets; the
@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const uint32_t* __r
                                                              int64_t n, int E,
                                                              uint32_t* __restrict__ hist) {
   __shared__ uint32_t h[ROUTE_MAX_E];
+  grid_dependency_wait();
   constexpr int PER = DISPATCH_CHUNK / 256;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK;
   uint32_t e_reg[PER];
@@ -48,15 +49,19 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const uint32_t* __r
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = h[e];
 }
 
+// SINGLE: one chunk holds every slot (n <= DISPATCH_CHUNK, decode-sized
+// batches): the block counts its own slots, so no count launch is needed.
+template <bool SINGLE>
 __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     const uint32_t* __restrict__ indices, int64_t n, int E, int nchunks,
     const uint32_t* __restrict__ hist, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets,
-    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv) {
+    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv, uint32_t* __restrict__ zero_words) {
   __shared__ uint32_t wh[SCATTER_WARPS][ROUTE_MAX_E];
   __shared__ uint32_t first[ROUTE_MAX_E];   // first row of this chunk per expert
   __shared__ uint32_t tot[ROUTE_MAX_E];
   __shared__ uint32_t warp_sums[SCATTER_WARPS];
   constexpr int STEPS = SLOTS_PER_WARP / 32;
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK +
                      static_cast<int64_t>(warp) * SLOTS_PER_WARP;
@@ -66,18 +71,35 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     const int64_t f = w0 + 32 * i + lane;
     e_reg[i] = f < n ? indices[f] : 0xFFFFFFFFu;
   }
-  // expert totals over all chunks and this chunk's offset from earlier chunks
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    uint32_t before = 0, all = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t v = hist[static_cast<int64_t>(c) * E + e];
-      before += c < static_cast<int>(blockIdx.x) ? v : 0u;
-      all += v;
-    }
-    first[e] = before;
-    tot[e] = all;
-  }
   for (int e = lane; e < E; e += 32) wh[warp][e] = 0;
+  if constexpr (SINGLE) {
+    // this block's own histogram is the total; nothing comes before it
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < STEPS; ++i)
+      if (e_reg[i] < static_cast<uint32_t>(E)) atomicAdd(&wh[warp][e_reg[i]], 1u);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      uint32_t all = 0;
+#pragma unroll
+      for (int w = 0; w < SCATTER_WARPS; ++w) all += wh[w][e];
+      first[e] = 0;
+      tot[e] = all;
+      counts[e] = all;
+    }
+  } else {
+    // expert totals over all chunks and this chunk's offset from earlier chunks
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      uint32_t before = 0, all = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const uint32_t v = hist[static_cast<int64_t>(c) * E + e];
+        before += c < static_cast<int>(blockIdx.x) ? v : 0u;
+        all += v;
+      }
+      first[e] = before;
+      tot[e] = all;
+    }
+  }
   __syncthreads();
   // exclusive scan of the totals over experts: warp w scans experts [w*E/8 ...)
   {
@@ -98,9 +120,11 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     }
     if (lane == 0) warp_sums[warp] = carry;
   }
+  if constexpr (!SINGLE) {
 #pragma unroll
-  for (int i = 0; i < STEPS; ++i)
-    if (e_reg[i] < static_cast<uint32_t>(E)) atomicAdd(&wh[warp][e_reg[i]], 1u);
+    for (int i = 0; i < STEPS; ++i)
+      if (e_reg[i] < static_cast<uint32_t>(E)) atomicAdd(&wh[warp][e_reg[i]], 1u);
+  }
   __syncthreads();
   {
     const int per = (E + SCATTER_WARPS - 1) / SCATTER_WARPS;
@@ -120,9 +144,11 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
       uint32_t all = 0;
       for (int w = 0; w < SCATTER_WARPS; ++w) all += warp_sums[w];
       offsets[E] = all;
+      // The tile counters of the expert GEMMs that follow in moe_forward.
+      if (zero_words != nullptr) zero_words[0] = zero_words[1] = 0u;
     }
   }
-  if (blockIdx.x == 0) {
+  if (!SINGLE && blockIdx.x == 0) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       uint32_t all = 0;
       for (int c = 0; c < nchunks; ++c) all += hist[static_cast<int64_t>(c) * E + e];
@@ -154,6 +180,7 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
 
 // With no slots at all the scatter kernel has no blocks: write zero counts/offsets.
 __global__ void dispatch_empty_kernel(int E, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets) {
+  grid_dependency_wait();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     if (e < E) counts[e] = 0;
     offsets[e] = 0;
@@ -167,6 +194,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const VecT* __rest
                                                               const uint32_t* __restrict__ offsets,
                                                               int E, int k, int64_t vec_per_row,
                                                               VecT* __restrict__ xd) {
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int64_t rows = offsets[E];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -217,17 +245,23 @@ size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, uint32_t* zero_words) {
   const int64_t n = T * top_k;
   const int nchunks = static_cast<int>((n + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
   uint32_t* hist = static_cast<uint32_t*>(scratch);
-  if (nchunks > 0) {
-    dispatch_count_kernel<<<nchunks, 256, 0, stream>>>(indices, n, E, hist);
-    dispatch_scatter_kernel<<<nchunks, SCATTER_WARPS * 32, 0, stream>>>(indices, n, E, nchunks, hist, counts,
-                                                                        offsets, row_src, inv);
+  cudaError_t err = cudaSuccess;
+  if (nchunks == 1) {
+    err = launch_dependent(dispatch_scatter_kernel<true>, dim3(1), dim3(SCATTER_WARPS * 32), 0, stream, indices, n, E,
+                           1, hist, counts, offsets, row_src, inv, zero_words);
+  } else if (nchunks > 1) {
+    err = launch_dependent(dispatch_count_kernel, dim3(nchunks), dim3(256), 0, stream, indices, n, E, hist);
+    if (err == cudaSuccess)
+      err = launch_dependent(dispatch_scatter_kernel<false>, dim3(nchunks), dim3(SCATTER_WARPS * 32), 0, stream,
+                             indices, n, E, nchunks, hist, counts, offsets, row_src, inv, zero_words);
   } else {
     dispatch_empty_kernel<<<1, 256, 0, stream>>>(E, counts, offsets);
   }
+  if (err != cudaSuccess) return err;
   if (x_dispatched != nullptr && n > 0) {
     const int64_t row_bytes = H * static_cast<int64_t>(dtype_size(dtype));
     const int64_t blocks64 = (n + 7) / 8;
@@ -235,18 +269,19 @@ cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k
     const bool vec16 = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
                        reinterpret_cast<uintptr_t>(x_dispatched) % 16 == 0;
     if (vec16) {
-      dispatch_gather_kernel<uint4><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint4*>(x), row_src, offsets, E, top_k, row_bytes / 16,
-          static_cast<uint4*>(x_dispatched));
+      err = launch_dependent(dispatch_gather_kernel<uint4>, dim3(blocks), dim3(256), 0, stream,
+                             static_cast<const uint4*>(x), row_src, offsets, E, top_k, row_bytes / 16,
+                             static_cast<uint4*>(x_dispatched));
     } else if (dtype == MOE_F32) {
-      dispatch_gather_kernel<float><<<blocks, 256, 0, stream>>>(
-          static_cast<const float*>(x), row_src, offsets, E, top_k, H,
-          static_cast<float*>(x_dispatched));
+      err = launch_dependent(dispatch_gather_kernel<float>, dim3(blocks), dim3(256), 0, stream,
+                             static_cast<const float*>(x), row_src, offsets, E, top_k, H,
+                             static_cast<float*>(x_dispatched));
     } else {
-      dispatch_gather_kernel<uint16_t><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint16_t*>(x), row_src, offsets, E, top_k, H,
-          static_cast<uint16_t*>(x_dispatched));
+      err = launch_dependent(dispatch_gather_kernel<uint16_t>, dim3(blocks), dim3(256), 0, stream,
+                             static_cast<const uint16_t*>(x), row_src, offsets, E, top_k, H,
+                             static_cast<uint16_t*>(x_dispatched));
     }
+    if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }

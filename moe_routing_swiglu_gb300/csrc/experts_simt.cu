@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
   __shared__ float As[SB_K][SB_M + 4];
   __shared__ float B0s[SB_K][SB_N + 4];
   __shared__ float B1s[GATE_UP ? SB_K : 1][SB_N + 4];
+  grid_dependency_wait();
   const int n_tiles = static_cast<int>((N + SB_N - 1) / SB_N);
   if (threadIdx.x < 32) build_tile_prefix(offsets, E, SB_M, n_tiles, tile_start);
   __syncthreads();
@@ -127,14 +128,16 @@ cudaError_t launch_experts_simt_f32(bool gate_up, const float* a, const TcGather
   const int64_t a_rows = gather != nullptr ? gather->x_rows : rows;
   if (gate_up) {
     const int64_t g = tile_bound(rows, E, SB_M, (I + SB_N - 1) / SB_N);
-    experts_simt_kernel<true><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        src, row_src, top_k, a_rows, offsets, E, w0, w1, H, I, rows, out,
-        cache != nullptr ? static_cast<float*>(cache->g) : nullptr,
-        cache != nullptr ? static_cast<float*>(cache->u) : nullptr);
+    return launch_dependent(experts_simt_kernel<true>, dim3(static_cast<unsigned>(g)), dim3(SB_THREADS), 0, stream,
+                            src, row_src, top_k, a_rows, offsets, E, w0, w1, H, I, rows, out,
+                            cache != nullptr ? static_cast<float*>(cache->g) : nullptr,
+                            cache != nullptr ? static_cast<float*>(cache->u) : nullptr);
   } else {
     const int64_t g = tile_bound(rows, E, SB_M, (H + SB_N - 1) / SB_N);
-    experts_simt_kernel<false><<<static_cast<unsigned>(g), SB_THREADS, 0, stream>>>(
-        a, nullptr, 1, rows, offsets, E, w0, nullptr, I, H, rows, out, nullptr, nullptr);
+    return launch_dependent(experts_simt_kernel<false>, dim3(static_cast<unsigned>(g)), dim3(SB_THREADS), 0, stream,
+                            a, static_cast<const uint32_t*>(nullptr), 1, rows, offsets, E, w0,
+                            static_cast<const float*>(nullptr), I, H, rows, out, static_cast<float*>(nullptr),
+                            static_cast<float*>(nullptr));
   }
   return cudaGetLastError();
 }

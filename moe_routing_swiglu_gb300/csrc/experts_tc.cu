@@ -203,11 +203,14 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
     tma_prefetch_desc(&tm_b16);
   }
   __syncwarp();
-  if (warp == 0) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks, tile_start);
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
+  // Everything above touches only this CTA's shared memory and TMEM; from
+  // here on the kernel reads what earlier kernels wrote (offsets, rows).
+  grid_dependency_wait();
+  if (warp == 0) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks, tile_start);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -552,24 +555,26 @@ int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks, int tbm) {
 
 template <typename T, bool GATE_UP, int TBM, bool GATHER = false>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b128,
-                       const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream,
+                       bool sched_zeroed) {
   auto kern = experts_tc_kernel<T, GATE_UP, TBM, GATHER>;
   constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int grid = static_cast<int>(args.tile_cap < static_cast<uint32_t>(num_sms) ? args.tile_cap : num_sms);
   if (grid <= 0) return cudaSuccess;
-  err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
-  if (err != cudaSuccess) return err;
-  kern<<<grid, num_threads<GATHER>(), SMEM_BYTES, stream>>>(a0, a1, b128, b16, args);
-  return cudaGetLastError();
+  if (!sched_zeroed) {
+    err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return err;
+  }
+  return launch_dependent(kern, dim3(grid), dim3(num_threads<GATHER>()), SMEM_BYTES, stream, a0, a1, b128, b16, args);
 }
 
 template <typename T>
 cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                          const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E, int64_t rows,
                          int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms, cudaStream_t stream,
-                         const char** why) {
+                         const char** why, bool sz) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
   if (err != cudaSuccess) return err;
@@ -611,15 +616,15 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
     args.row_src = gather->row_src;
     args.top_k = gather->top_k;
     args.x_rows = static_cast<uint32_t>(gather->x_rows);
-    if (small) return launch_one<T, true, 32, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
-    return launch_one<T, true, 256, true>(w.gate, w.up, t128, t16, args, num_sms, stream);
+    if (small) return launch_one<T, true, 32, true>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
+    return launch_one<T, true, 256, true>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
   }
   if (small) {
-    if (gate_up) return launch_one<T, true, 32>(w.gate, w.up, t128, t16, args, num_sms, stream);
-    return launch_one<T, false, 32>(w.down, w.down, t128, t16, args, num_sms, stream);
+    if (gate_up) return launch_one<T, true, 32>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
+    return launch_one<T, false, 32>(w.down, w.down, t128, t16, args, num_sms, stream, sz);
   }
-  if (gate_up) return launch_one<T, true, 256>(w.gate, w.up, t128, t16, args, num_sms, stream);
-  return launch_one<T, false, 256>(w.down, w.down, t128, t16, args, num_sms, stream);
+  if (gate_up) return launch_one<T, true, 256>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
+  return launch_one<T, false, 256>(w.down, w.down, t128, t16, args, num_sms, stream, sz);
 }
 
 }  // namespace
@@ -641,13 +646,13 @@ bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_d
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E,
                               int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
-                              cudaStream_t stream, const char** why) {
+                              cudaStream_t stream, const char** why, bool sched_zeroed) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
     return launch_stage<__nv_bfloat16>(w, dtype, gate_up, a, gather, cache, offsets, E, rows, H, I, out, sched,
-                                       num_sms, stream, why);
+                                       num_sms, stream, why, sched_zeroed);
   return launch_stage<__half>(w, dtype, gate_up, a, gather, cache, offsets, E, rows, H, I, out, sched, num_sms,
-                              stream, why);
+                              stream, why, sched_zeroed);
 }
 
 cudaError_t device_status_ptr(uint32_t** p) {

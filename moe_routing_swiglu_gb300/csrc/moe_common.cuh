@@ -60,6 +60,15 @@ __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code) {
   if (status != nullptr) atomicCAS(status, 0u, code);
 }
 
+// ---------------------------------------------------------------- dependent launches
+
+// Wait until the kernel this one depends on (the previous kernel in the
+// stream) has completed and its writes are visible. Kernels launched with
+// programmatic stream serialization (launch_dependent below) may start before
+// their predecessor finishes: they call this before reading anything it
+// wrote or writing anything it reads. Returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- grouped-GEMM tile plan
 
 // Tiles of a grouped GEMM: expert e owns ceil(count_e / bm) row tiles times

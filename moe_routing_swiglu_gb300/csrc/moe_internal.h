@@ -8,9 +8,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
+
+// Launch `kernel` with programmatic stream serialization: its blocks may be
+// scheduled (and run their prologue) while the previous kernel in the stream
+// finishes; the kernel calls grid_dependency_wait() before touching that
+// kernel's data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- K1 routing (route.cu)
 constexpr int ROUTE_MAX_E = 1024;
@@ -39,10 +61,12 @@ size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k);
 // the current device (set up on first use per device).
 constexpr size_t NOALLOC_DISPATCH_SCRATCH_BYTES = size_t{1} << 20;
 cudaError_t noalloc_dispatch_scratch(void** ptr);
+// zero_words (optional): two uint32 the scatter kernel sets to 0 (moe_forward's
+// GEMM tile counters, so the GEMMs need no memset).
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                            cudaStream_t stream);
+                            cudaStream_t stream, uint32_t* zero_words = nullptr);
 
 // ---- K5 combine (combine.cu)
 cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
@@ -85,7 +109,7 @@ constexpr size_t TC_SCHED_BYTES = 256;
 cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up, const void* a,
                               const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E,
                               int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
-                              cudaStream_t stream, const char** why);
+                              cudaStream_t stream, const char** why, bool sched_zeroed = false);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 // Device address of the status word the bounded waits report into.
 cudaError_t device_status_ptr(uint32_t** p);

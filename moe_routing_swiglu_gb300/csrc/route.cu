@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(const TL* __res
                                                                  TL* __restrict__ weights,
                                                                  float* __restrict__ weights32) {
   __shared__ __align__(16) float e_sm[ROUTE_WARPS][32 * V];
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   float* my_e = e_sm[threadIdx.x >> 5];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -176,13 +177,13 @@ cudaError_t launch_route_t(const void* logits, int64_t T, int E, int k, bool ren
   const TL* lg = static_cast<const TL*>(logits);
   TL* w = static_cast<TL*>(weights);
   const int r = renorm ? 1 : 0;
-  if (E <= 32) route_kernel<TL, 1><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  else if (E <= 64) route_kernel<TL, 2><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  else if (E <= 128) route_kernel<TL, 4><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  else if (E <= 256) route_kernel<TL, 8><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  else if (E <= 512) route_kernel<TL, 16><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  else route_kernel<TL, 32><<<blocks, threads, 0, stream>>>(lg, T, E, k, r, indices, w, w32);
-  return cudaGetLastError();
+  auto kern = route_kernel<TL, 32>;
+  if (E <= 32) kern = route_kernel<TL, 1>;
+  else if (E <= 64) kern = route_kernel<TL, 2>;
+  else if (E <= 128) kern = route_kernel<TL, 4>;
+  else if (E <= 256) kern = route_kernel<TL, 8>;
+  else if (E <= 512) kern = route_kernel<TL, 16>;
+  return launch_dependent(kern, dim3(blocks), dim3(threads), 0, stream, lg, T, E, k, r, indices, w, w32);
 }
 
 }  // namespace

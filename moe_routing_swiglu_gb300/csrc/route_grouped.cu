@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(GR_WARPS * 32)
   __shared__ float bias_sm[ROUTE_MAX_E];
   __shared__ uint8_t grp_sm[ROUTE_MAX_E];
   __shared__ __align__(16) float c_sm[GR_WARPS][32 * V];
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   float* my_c = c_sm[threadIdx.x >> 5];
 
@@ -317,13 +318,13 @@ cudaError_t launch_t(const void* logits, int64_t T, int E, const float* bias, co
   const int blocks = static_cast<int>(want < 65535 * 8 ? want : 65535 * 8);
   const TL* lg = static_cast<const TL*>(logits);
   TL* w = static_cast<TL*>(weights);
-  if (E <= 32) route_grouped_kernel<TL, 1><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  else if (E <= 64) route_grouped_kernel<TL, 2><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  else if (E <= 128) route_grouped_kernel<TL, 4><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  else if (E <= 256) route_grouped_kernel<TL, 8><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  else if (E <= 512) route_grouped_kernel<TL, 16><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  else route_grouped_kernel<TL, 32><<<blocks, threads, 0, stream>>>(lg, bias, T, E, p, indices, w, w32);
-  return cudaGetLastError();
+  auto kern = route_grouped_kernel<TL, 32>;
+  if (E <= 32) kern = route_grouped_kernel<TL, 1>;
+  else if (E <= 64) kern = route_grouped_kernel<TL, 2>;
+  else if (E <= 128) kern = route_grouped_kernel<TL, 4>;
+  else if (E <= 256) kern = route_grouped_kernel<TL, 8>;
+  else if (E <= 512) kern = route_grouped_kernel<TL, 16>;
+  return launch_dependent(kern, dim3(blocks), dim3(threads), 0, stream, lg, bias, T, E, p, indices, w, w32);
 }
 
 }  // namespace

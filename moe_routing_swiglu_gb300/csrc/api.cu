@@ -207,9 +207,11 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   void* xd = gather_rows ? nullptr : ws + L.xd;
 
   // Decode-sized batches: dispatch writes the maps only and the gate/up GEMM
-  // reads each dispatched row straight from x through row_src. Larger
-  // batches: dispatch also writes x_dispatched, which the GEMM streams with
-  // TMA (faster there than gathering rows from every weight tile).
+  // gathers each dispatched row straight from x through row_src (TMA row
+  // gathers). Larger batches: dispatch also writes x_dispatched, which the
+  // GEMM streams with 128-row TMA boxes (a row gather costs about as much
+  // TMA time as a whole box, so gathering every weight tile's 256 rows is
+  // slower there than the extra copy).
   // The dispatch's scatter kernel zeroes the two GEMMs' tile counters, so
   // the chain is kernels only (each launched as a dependent of the previous).
   uint32_t* sched = reinterpret_cast<uint32_t*>(ws + L.sched);
@@ -226,6 +228,12 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward combine launch");
   return ok();
+}
+
+// FP32 dh scratch of moe_experts_backward: the F32 path's dgrad writes it;
+// the tensor-core path turns dh into dg and du in the dgrad epilogue.
+size_t backward_dh_bytes(const moe_experts* ex, size_t n) {
+  return ex->dtype == MOE_F32 ? align_up(n * 4 + 1, 256) : 0;
 }
 
 }  // namespace
@@ -611,7 +619,7 @@ moe_status moe_experts_forward_training(const moe_experts* ex, const void* x_dis
 size_t moe_experts_backward_workspace_size(const moe_experts* ex, int64_t rows) {
   if (ex == nullptr || rows < 0) return 0;
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(ex->I);
-  return align_up(n * 4 + 1, 256) + 2 * align_up(n * dtype_size(ex->dtype) + 1, 256) + moe::TC_SCHED_BYTES;
+  return backward_dh_bytes(ex, n) + 2 * align_up(n * dtype_size(ex->dtype) + 1, 256) + moe::TC_SCHED_BYTES;
 }
 
 moe_status moe_experts_backward(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets, int64_t rows,
@@ -628,11 +636,11 @@ moe_status moe_experts_backward(const moe_experts* ex, const void* x_dispatched,
     return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_experts_backward_workspace_size()");
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(ex->I);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t dh_bytes = align_up(n * 4 + 1, 256);
+  const size_t dh_bytes = backward_dh_bytes(ex, n);
   const size_t d_bytes = align_up(n * dtype_size(ex->dtype) + 1, 256);
   moe::TrainBuffers b{x_dispatched, h, cache_g, cache_u, dexpert, ex->gate, ex->up, ex->down,
-                      reinterpret_cast<float*>(ws), ws + dh_bytes, ws + dh_bytes + d_bytes, dx_dispatched,
-                      dgate, dup, ddown};
+                      dh_bytes > 0 ? reinterpret_cast<float*>(ws) : nullptr, ws + dh_bytes, ws + dh_bytes + d_bytes,
+                      dx_dispatched, dgate, dup, ddown};
   cudaError_t err;
   const char* why = nullptr;
   if (ex->dtype == MOE_F32 || rows == 0) {

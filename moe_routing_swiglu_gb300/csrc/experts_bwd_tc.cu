@@ -3,7 +3,9 @@
 //
 // With dy the gradient of the dispatched rows' outputs (ruDNN user guide,
 // section 12, cache.backward):
-//   DGRAD_H   dh[r, i] = sum_h W_down[e][h][i] dy[r][h]        -> FP32 [rows, I]
+//   DGRAD_H   dh[r, i] = sum_h W_down[e][h][i] dy[r][h] (FP32, in TMEM), then
+//             in the epilogue dg = dh * u * SiLU'(g), du = dh * SiLU(g)
+//             from the cached g and u                           -> dtype [rows, I] x 2
 //   DGRAD_X   dx[r, h] = sum_i W_gate[e][i][h] dg[r][i]
 //                      + sum_i W_up[e][i][h]   du[r][i]        -> dtype [rows, H]
 //   WGRAD_D   ddown[e][h][i] = sum_{r in e} dy[r][h] h[r][i]   -> FP32 [E, H, I]
@@ -47,6 +49,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int XPOSE_BYTES = 32 * 32 * 2;
+constexpr int DH_PITCH = 36;                  // DGRAD_H: FP32 [16 tokens][36] staging rows
 constexpr int STAGE_SMEM = 192 * 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 constexpr uint32_t TILE_END = 0xFFFFFFFFu;
@@ -76,7 +79,8 @@ struct BwdCfg {
   static constexpr uint32_t ACC_COLS = TMEM_COLS / ACC;
   static constexpr uint32_t D1 = ACC_N;                                // second accumulator
   static constexpr int SMEM_STAGES = 0;
-  static constexpr int XPOSE_WARP = DGRAD ? XPOSE_BYTES : 32 * 33 * 4;  // per epilogue warp
+  static constexpr int XPOSE_WARP =                                      // per epilogue warp
+      MODE == DGRAD_H ? 16 * DH_PITCH * 4 : (DGRAD ? XPOSE_BYTES : 32 * 33 * 4);
   static constexpr int SMEM_XPOSE = STAGES * STAGE_BYTES;
   static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_WARP;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
@@ -92,8 +96,8 @@ struct BwdCfg {
 
 struct BwdArgs {
   const uint32_t* offsets;  // [E + 1]
-  void* out0;               // DGRAD: [rows, n_out]; WGRAD: [E, M, N] FP32
-  void* out1;               // WGRAD_GU: dup
+  void* out0;               // DGRAD: [rows, n_out] (DGRAD_H: dg); WGRAD: [E, M, N] FP32
+  void* out1;               // DGRAD_H: du; WGRAD_GU: dup
   uint32_t* sched;
   int E;
   int n_wblocks;            // DGRAD: output-channel blocks of 256; WGRAD: N blocks of 256
@@ -104,6 +108,8 @@ struct BwdArgs {
   uint32_t rows_total;
   uint32_t tile_cap;
   uint32_t* status;
+  const void* in_g;         // DGRAD_H: cached pre-activations g, u [rows, n_out]
+  const void* in_u;
 };
 
 template <typename T, int MODE>
@@ -387,7 +393,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(FULL_MASK, ok)) break;
       tc_fence_after();
       const uint32_t t_lane = tmem_base + acc * C::ACC_COLS + (static_cast<uint32_t>(quad * 32) << 16);
-      if (DGRAD) {
+      if (MODE == DGRAD_H) {
+        // lane = channel, TMEM column = token. Each 16-token half of a
+        // 32 x 32 block of dh goes through a padded FP32 staging tile (row j
+        // at j * 36 floats: conflict-free both ways); then lane (tok, part)
+        // takes 8 channels of one token, reads g and u with 16-byte loads and
+        // writes dg and du with 16-byte stores.
+        const int n_tok = (w.rows + 15) & ~15;
+        const int64_t chan0 = static_cast<int64_t>(w.nb) * (2 * BM) + quad * 32;
+        for (int c0 = 32 * half; c0 < n_tok; c0 += 64) {
+          for (int blk = 0; blk < 2; ++blk) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_lane + blk * C::D1 + static_cast<uint32_t>(c0), v);
+            tmem_ld_wait();
+            const int64_t col = chan0 + blk * BM + rd_part * 8;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xf[j * DH_PITCH + lane] = __uint_as_float(v[hh * 16 + j]);
+              __syncwarp();
+#pragma unroll
+              for (int p = 0; p < 2; ++p) {
+                const int j = p * 8 + rd_tok;
+                const int t_in = c0 + hh * 16 + j;
+                if (t_in < w.rows && col + 8 <= args.n_out) {
+                  const int64_t off = (static_cast<int64_t>(w.row0) + t_in) * args.n_out + col;
+                  const float4 d0 = *reinterpret_cast<const float4*>(xf + j * DH_PITCH + rd_part * 8);
+                  const float4 d1 = *reinterpret_cast<const float4*>(xf + j * DH_PITCH + rd_part * 8 + 4);
+                  const uint4 gq = *reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_g) + off);
+                  const uint4 uq = *reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_u) + off);
+                  const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                  const T* gv = reinterpret_cast<const T*>(&gq);
+                  const T* uv = reinterpret_cast<const T*>(&uq);
+                  uint32_t dgw[4], duw[4];
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    float g0, g1, u0, u1;
+                    silu_mul_backward(d[2 * q], to_f32(gv[2 * q]), to_f32(uv[2 * q]), &g0, &u0);
+                    silu_mul_backward(d[2 * q + 1], to_f32(gv[2 * q + 1]), to_f32(uv[2 * q + 1]), &g1, &u1);
+                    dgw[q] = pack2<T>(g0, g1);
+                    duw[q] = pack2<T>(u0, u1);
+                  }
+                  *reinterpret_cast<uint4*>(static_cast<T*>(args.out0) + off) =
+                      make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+                  *reinterpret_cast<uint4*>(static_cast<T*>(args.out1) + off) =
+                      make_uint4(duw[0], duw[1], duw[2], duw[3]);
+                }
+              }
+              __syncwarp();
+            }
+          }
+        }
+      } else if (DGRAD) {
         // lane = output channel, TMEM column = token of the block.
         const int n_tok = (w.rows + 15) & ~15;
         const int64_t chan0 = static_cast<int64_t>(w.nb) * (2 * BM) + quad * 32;
@@ -398,36 +455,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           for (int blk = 0; blk < 2; ++blk) {
             const int64_t chan = chan0 + blk * BM;
-            if (MODE == DGRAD_H) {
-              // FP32 rows: for each token the 32 lanes store 32 consecutive floats.
-              float* o = static_cast<float*>(args.out0);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int t_in = c0 + j;
-                if (t_in < w.rows && chan + lane < args.n_out)
-                  o[(static_cast<int64_t>(w.row0) + t_in) * args.n_out + chan + lane] =
-                      __uint_as_float(blk == 0 ? v0[j] : v1[j]);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const T hv = from_f32<T>(__uint_as_float(blk == 0 ? v0[j] : v1[j]));
-                xp[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
-              }
-              __syncwarp();
-              const int64_t col = chan + rd_part * 8;
-#pragma unroll
-              for (int p = 0; p < 4; ++p) {
-                const int j = p * 8 + rd_tok;
-                const uint4 row = *reinterpret_cast<const uint4*>(xp + j * 32 + rd_part * 8);
-                const int t_in = c0 + j;
-                if (t_in < w.rows && col + 8 <= args.n_out) {
-                  T* dst = static_cast<T*>(args.out0) + (static_cast<int64_t>(w.row0) + t_in) * args.n_out + col;
-                  *reinterpret_cast<uint4*>(dst) = row;
-                }
-              }
-              __syncwarp();
+            for (int j = 0; j < 32; ++j) {
+              const T hv = from_f32<T>(__uint_as_float(blk == 0 ? v0[j] : v1[j]));
+              xp[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
             }
+            __syncwarp();
+            const int64_t col = chan + rd_part * 8;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const int j = p * 8 + rd_tok;
+              const uint4 row = *reinterpret_cast<const uint4*>(xp + j * 32 + rd_part * 8);
+              const int t_in = c0 + j;
+              if (t_in < w.rows && col + 8 <= args.n_out) {
+                T* dst = static_cast<T*>(args.out0) + (static_cast<int64_t>(w.row0) + t_in) * args.n_out + col;
+                *reinterpret_cast<uint4*>(dst) = row;
+              }
+            }
+            __syncwarp();
           }
         }
       } else {
@@ -547,7 +592,8 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
   };
   const int64_t tok_blocks = rows / TBM + (rows < E ? rows : E);
   const uint32_t srows = static_cast<uint32_t>(rows);
-  // dh = dy W_down: A = W_down [E][H][I] (K = H, M = I), B = dy [rows][H]
+  // dh = dy W_down: A = W_down [E][H][I] (K = H, M = I), B = dy [rows][H];
+  // the epilogue turns dh into dg and du with the cached g and u.
   {
     if (!enc_weights_mn(&maps[0], dt, b.down, E, H, I) || !enc_rows(&maps[2], dt, b.dy, rows, H, 128) ||
         !enc_rows(&maps[3], dt, b.dy, rows, H, 16))
@@ -556,15 +602,9 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
     maps[4] = maps[2];
     maps[5] = maps[3];
     const int nw = static_cast<int>((I + 2 * BM - 1) / (2 * BM));
-    BwdArgs a{offsets, b.dh, nullptr, sched, E, nw, 0, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
-              0, srows, static_cast<uint32_t>(tok_blocks * nw), status};
+    BwdArgs a{offsets, b.dg, b.du, sched, E, nw, 0, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
+              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, b.g, b.u};
     err = launch_mode<T, DGRAD_H>(maps, a, num_sms, s);
-    if (err != cudaSuccess) return err;
-  }
-  // dg, du from dh and the cache
-  {
-    const int64_t n = rows * I;
-    err = launch_silu_backward(dt, b.dh, b.g, b.u, n, b.dg, b.du, s);
     if (err != cudaSuccess) return err;
   }
   // dx = dg W_gate + du W_up: A = W_gate / W_up [E][I][H] (K = I, M = H), B = dg / du [rows][I]

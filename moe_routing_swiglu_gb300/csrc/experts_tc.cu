@@ -37,6 +37,16 @@
 //                   FP32 (K3: SiLU(g)*u), transposes its 32 x 32 block
 //                   through a warp-private shared buffer and writes each
 //                   token's 64-byte runs with 16-byte stores.
+// Token rows reach shared memory in one of three ways (the template's LOAD):
+//   TOK_DENSE    TMA boxes of 128 and 16 rows over x_dispatched;
+//   TOK_GATHER4  TMA row gathers straight from x: row r of a tile is
+//                x[row_src[r] / top_k], four rows per tile::gather4 copy,
+//                issued by the lanes of warp 0 (decode-sized tiles of at
+//                most 32 rows; the dispatch then writes no x_dispatched);
+//   TOK_CPASYNC  the same gather by four extra loader warps with 16-byte
+//                cp.async copies into the swizzled layout (256-row tiles,
+//                where 64 row gathers per stage would keep the TMA unit
+//                busy far longer than one 128-row box).
 // Tiles: expert e has ceil(count_e / 256) token blocks times the weight
 // blocks; token blocks vary fastest and tiles are claimed in order, so the
 // CTAs that share a weight tile run together and read it from L2. The plan
@@ -69,10 +79,12 @@ constexpr int ROW_BYTES = BK * 2;             // 128 B per row per stage
 constexpr int A_BYTES = BM * ROW_BYTES;       // 16 KB per weight tile
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_LOAD_WARPS = 4;             // token-row loaders of the gather mode
+constexpr int NUM_LOAD_WARPS = 4;             // token-row loaders of the cp.async gather
 constexpr int FIRST_LOAD_WARP = 2 + NUM_EPI_WARPS;
-template <bool GATHER>
-constexpr int num_threads() { return 32 * (2 + NUM_EPI_WARPS + (GATHER ? NUM_LOAD_WARPS : 0)); }
+enum TokenLoad { TOK_DENSE = 0, TOK_CPASYNC = 1, TOK_GATHER4 = 2 };
+template <int LOAD>
+constexpr int num_threads() { return 32 * (2 + NUM_EPI_WARPS + (LOAD == TOK_CPASYNC ? NUM_LOAD_WARPS : 0)); }
+constexpr int BAD_WORDS = 8;                  // per ring slot: one flag bit per token row (256)
 constexpr int XPOSE_BYTES = 32 * 32 * 2;      // per-warp transpose buffer
 constexpr int STAGE_SMEM = 192 * 1024;        // shared memory given to pipeline stages
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
@@ -99,7 +111,8 @@ struct TcCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
   static constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
-  static constexpr int SMEM_TILES = SMEM_MISC + 16;
+  static constexpr int SMEM_BAD = SMEM_MISC + 16;                  // [RING][BAD_WORDS]
+  static constexpr int SMEM_TILES = SMEM_BAD + 4 * RING * BAD_WORDS;
   static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
@@ -130,7 +143,7 @@ struct TcArgs {
   uint32_t rows_total;      // rows of the token and output matrices
   uint32_t tile_cap;        // host bound on the tile count
   uint32_t* status;
-  // Gather mode (K3 only): token row r of a tile is x[row_src[r] / top_k].
+  // Gather modes (K3 only): token row r of a tile is x[row_src[r] / top_k].
   const uint8_t* gx;        // x [x_rows, K], 16-bit, rows of k_bytes
   const uint32_t* row_src;  // [rows_total]
   int top_k;
@@ -150,9 +163,10 @@ __device__ __forceinline__ float silu_f32(float g) {
 }
 
 // Tensor maps: a0/a1 weight tiles (128-row boxes: K3 gate/up, K4 down rows
-// n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes.
-template <typename T, bool GATE_UP, int TBM, bool GATHER>
-__global__ void __launch_bounds__(num_threads<GATHER>(), 1)
+// n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes
+// (TOK_GATHER4: b128 is x with a one-row box).
+template <typename T, bool GATE_UP, int TBM, int LOAD>
+__global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
                       const __grid_constant__ CUtensorMap tm_b128,
@@ -161,6 +175,7 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr int TB = TBM;
+  constexpr bool GATHER = LOAD == TOK_CPASYNC;  // loader warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::SMEM_BAR);
@@ -173,6 +188,7 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
   volatile uint32_t* ring = reinterpret_cast<volatile uint32_t*>(smem + C::SMEM_RING);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
+  volatile uint32_t* tile_bad = reinterpret_cast<volatile uint32_t*>(smem + C::SMEM_BAD);
   uint32_t* tile_start = reinterpret_cast<uint32_t*>(smem + C::SMEM_TILES);
 
   const int warp = threadIdx.x >> 5;
@@ -218,7 +234,126 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
   // The cap keeps a corrupt offsets array from producing an endless tile loop.
   const uint32_t total = min(tile_start[args.E], args.tile_cap);
 
-  if (warp == 0) {
+  if (warp == 0 && LOAD == TOK_GATHER4) {
+    // ------------------------------------------------------------ scheduler + TMA producer, row gathers
+    // Lane 0 claims tiles and issues the weight copies; lane l gathers the
+    // tile's rows 4 (l + 32 g) .. 4 (l + 32 g) + 3 for g < G4.
+    constexpr int G4 = (TBM / 4 + 31) / 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0;
+    bool ok = true;
+    for (uint32_t it = 0;; ++it) {
+      const uint32_t slot = it % RING;
+      uint32_t tile = TILE_END;
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&tile_empty[slot], ((it / RING) & 1u) ^ 1u, abort_flag, args.status, ST_TILE_RING,
+                               WAIT_LIMIT_NS);
+        if (ok) {
+          const uint32_t claimed = atomicAdd(args.sched, 1u);
+          tile = claimed < total ? claimed : TILE_END;
+        }
+      }
+      ok = __shfl_sync(FULL_MASK, ok ? 1 : 0, 0) != 0;
+      tile = __shfl_sync(FULL_MASK, tile, 0);
+      if (!ok) break;
+      if (tile == TILE_END) {
+        if (lane == 0) {
+          ring[slot] = TILE_END;
+          mbar_arrive(&tile_full[slot]);
+        }
+        break;
+      }
+      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+      const int n_tok = (tc.rows + 15) & ~15;
+      // Rows past the tile's rows (up to its 16-row N) read x row 0: their
+      // outputs are never written. A row whose token is out of range reads
+      // row 0 too and is flagged, and the epilogue writes zeros for it (the
+      // outputs of a zero x row).
+      int tok[G4][4];
+      uint32_t nib[G4];
+#pragma unroll
+      for (int g = 0; g < G4; ++g) {
+        nib[g] = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * (lane + 32 * g) + i;
+          uint32_t t = 0;
+          if (r < tc.rows && tc.row0 + static_cast<uint32_t>(r) < args.rows_total) {
+            t = args.row_src[tc.row0 + r] / static_cast<uint32_t>(args.top_k);
+            if (t >= args.x_rows) {
+              nib[g] |= 1u << i;
+              t = 0;
+            }
+          }
+          tok[g][i] = static_cast<int>(t);
+        }
+      }
+      // Flag word w holds rows 32 w .. 32 w + 31: lanes 8q .. 8q + 7 of
+      // gather g fill word 4 g + q, lane l at bits 4 (l % 8) ...
+#pragma unroll
+      for (int g = 0; g < G4; ++g) {
+        uint32_t wv = nib[g] << (4 * (lane & 7));
+        wv |= __shfl_xor_sync(FULL_MASK, wv, 1);
+        wv |= __shfl_xor_sync(FULL_MASK, wv, 2);
+        wv |= __shfl_xor_sync(FULL_MASK, wv, 4);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t word = __shfl_sync(FULL_MASK, wv, 8 * q);
+          if (lane == 0 && 4 * g + q < BAD_WORDS) tile_bad[slot * BAD_WORDS + 4 * g + q] = word;
+        }
+      }
+      if (lane == 0) {
+        ring[slot] = tile;
+        mbar_arrive(&tile_full[slot]);  // release: the ring entry and flags are visible to the waiters
+      }
+      const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + n_tok * ROW_BYTES);
+      const int n_gather = n_tok >> 2;
+      const int wrow = tc.n * BM;
+      for (int kb = 0; kb < args.k_blocks; ++kb) {
+        uint8_t* st = smem + C::SMEM_STAGES + stage * STAGE_BYTES;
+        const int k0 = kb * BK;
+        bool got = true;
+        if (lane == 0) {
+          got = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status, ST_PRODUCER_EMPTY,
+                                  WAIT_LIMIT_NS);
+          if (got) {
+            mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_3d(st, &tm_a0, &full[stage], k0, wrow, tc.e);
+            tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], k0, wrow, tc.e);
+          }
+        }
+        if (__shfl_sync(FULL_MASK, got ? 1 : 0, 0) == 0) {
+          ok = false;
+          break;
+        }
+        uint8_t* b_dst = st + 2 * A_BYTES;
+#pragma unroll
+        for (int g = 0; g < G4; ++g) {
+          const int gi = lane + 32 * g;
+          if (gi < n_gather)
+            tma_gather4(b_dst + gi * 4 * ROW_BYTES, &tm_b128, &full[stage], k0, tok[g][0], tok[g][1], tok[g][2],
+                        tok[g][3]);
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      // Let the copies already in flight land before the block can exit.
+      const uint32_t n_back = issued < STAGES ? issued : STAGES;
+      for (uint32_t i = 1; i <= n_back; ++i) {
+        const uint32_t n = issued - i;
+        mbar_wait_bounded(&full[n % STAGES], (n / STAGES) & 1u, nullptr, args.status, ST_PRODUCER_DRAIN,
+                          WAIT_LIMIT_NS);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -368,6 +503,7 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
       tc_fence_after();
       const int n_tok = (tc.rows + 15) & ~15;
       const uint32_t t_lane = tmem_base + acc * C::ACC_COLS + (static_cast<uint32_t>(quad * 32) << 16);
+      const volatile uint32_t* bad = tile_bad + slot * BAD_WORDS;  // TOK_GATHER4: rows to write as zeros
       // Output columns of this warp's 32 lanes (two blocks for K4).
       const int64_t colA = GATE_UP ? static_cast<int64_t>(tc.n) * BM + quad * 32
                                    : static_cast<int64_t>(tc.n) * (2 * BM) + quad * 32;
@@ -404,7 +540,8 @@ __global__ void __launch_bounds__(num_threads<GATHER>(), 1)
             if (t_in < tc.rows && tc.row0 + static_cast<uint32_t>(t_in) < args.rows_total &&
                 col + 8 <= args.n_out) {
               T* dst = static_cast<T*>(out_base) + (static_cast<int64_t>(tc.row0) + t_in) * args.n_out + col;
-              *reinterpret_cast<uint4*>(dst) = row;
+              const bool zero = LOAD == TOK_GATHER4 && ((bad[t_in >> 5] >> (t_in & 31)) & 1u) != 0;
+              *reinterpret_cast<uint4*>(dst) = zero ? make_uint4(0u, 0u, 0u, 0u) : row;
             }
           }
           __syncwarp();
@@ -553,11 +690,11 @@ int64_t tile_bound(int64_t rows, int E, int64_t n_wblocks, int tbm) {
   return t_blocks * n_wblocks;
 }
 
-template <typename T, bool GATE_UP, int TBM, bool GATHER = false>
+template <typename T, bool GATE_UP, int TBM, int LOAD = TOK_DENSE>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b128,
                        const CUtensorMap& b16, const TcArgs& args, int num_sms, cudaStream_t stream,
                        bool sched_zeroed) {
-  auto kern = experts_tc_kernel<T, GATE_UP, TBM, GATHER>;
+  auto kern = experts_tc_kernel<T, GATE_UP, TBM, LOAD>;
   constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -567,7 +704,7 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
     err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_dependent(kern, dim3(grid), dim3(num_threads<GATHER>()), SMEM_BYTES, stream, a0, a1, b128, b16, args);
+  return launch_dependent(kern, dim3(grid), dim3(num_threads<LOAD>()), SMEM_BYTES, stream, a0, a1, b128, b16, args);
 }
 
 template <typename T>
@@ -580,12 +717,15 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   if (err != cudaSuccess) return err;
   const int64_t K = gate_up ? H : I;
   const int64_t n_out = gate_up ? I : H;
-  // Token maps over the dense rows; the gather mode loads rows itself and
-  // passes the weight maps in their place (never dereferenced there).
+  // Token maps: 128- and 16-row boxes over the dense rows, or x with a
+  // one-row box for the row gathers (t16 is then never dereferenced).
   CUtensorMap t128 = w.gate, t16 = w.gate;
-  if (gather == nullptr &&
-      (!encode_2d(&t128, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 128) ||
-       !encode_2d(&t16, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 16))) {
+  const bool maps_ok =
+      gather == nullptr
+          ? encode_2d(&t128, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 128) &&
+                encode_2d(&t16, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(rows), 16)
+          : encode_2d(&t128, dtype, gather->x, static_cast<uint64_t>(K), static_cast<uint64_t>(gather->x_rows), 1);
+  if (!maps_ok) {
     *why = "cuTensorMapEncodeTiled rejected the token tensor map";
     return cudaErrorInvalidValue;
   }
@@ -616,8 +756,13 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
     args.row_src = gather->row_src;
     args.top_k = gather->top_k;
     args.x_rows = static_cast<uint32_t>(gather->x_rows);
-    if (small) return launch_one<T, true, 32, true>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
-    return launch_one<T, true, 256, true>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
+    // Decode-sized tiles (at most 32 rows): TMA row gathers, a few per
+    // stage. Prefill-sized tiles: 256 rows per stage are 64 row gathers,
+    // and the TMA unit spends about as long on one 4-row gather as on a
+    // whole 128-row box (gate/up at the prefill workload: 466 us with row
+    // gathers, 253 us with the cp.async loader warps).
+    if (small) return launch_one<T, true, 32, TOK_GATHER4>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
+    return launch_one<T, true, 256, TOK_CPASYNC>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);
   }
   if (small) {
     if (gate_up) return launch_one<T, true, 32>(w.gate, w.up, t128, t16, args, num_sms, stream, sz);

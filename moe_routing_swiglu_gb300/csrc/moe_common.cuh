@@ -32,6 +32,18 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(v);
 }
 
+// Backward of h = SiLU(g) * u for one element, given d = dL/dh (ruDNN user
+// guide, section 12, cache.backward; the textbook derivative SiLU'(g) =
+// s (1 + g (1 - s)), s = sigmoid(g)): dg = d * u * SiLU'(g), du = d * SiLU(g),
+// in FP32.
+__device__ __forceinline__ void silu_mul_backward(float d, float g, float u, float* dg, float* du) {
+  const float s = 1.0f / (1.0f + expf(-g));
+  const float silu = g * s;
+  const float dsilu = s * (1.0f + g * (1.0f - s));
+  *dg = d * u * dsilu;
+  *du = d * silu;
+}
+
 // Two FP32 values packed as one 32-bit pair of 16-bit floats (low half first).
 template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
@@ -217,6 +229,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, ui
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(desc), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Row gather: four rows r0..r3 of a 2-D tensor map whose box is one row high,
+// columns c0.. (the box width), landing as four consecutive box rows at
+// smem_dst. The swizzle follows the shared-memory address, so a destination
+// 512 bytes into a 1024-byte swizzle atom holds atom rows 4..7.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* desc, uint64_t* bar, int c0, int r0,
+                                            int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(desc), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 

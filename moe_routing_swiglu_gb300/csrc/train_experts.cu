@@ -125,12 +125,10 @@ __global__ void silu_backward_kernel(const float* __restrict__ dh, const T* __re
                                      const T* __restrict__ u, int64_t n, T* __restrict__ dg, T* __restrict__ du) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float gv = to_f32(g[i]), uv = to_f32(u[i]), d = dh[i];
-    const float s = 1.0f / (1.0f + expf(-gv));
-    const float silu = gv * s;
-    const float dsilu = s * (1.0f + gv * (1.0f - s));
-    dg[i] = from_f32<T>(d * uv * dsilu);
-    du[i] = from_f32<T>(d * silu);
+    float dgv, duv;
+    silu_mul_backward(dh[i], to_f32(g[i]), to_f32(u[i]), &dgv, &duv);
+    dg[i] = from_f32<T>(dgv);
+    du[i] = from_f32<T>(duv);
   }
 }
 

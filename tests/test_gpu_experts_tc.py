@@ -136,6 +136,35 @@ def test_gate_up_gather_bad_row_src_reads_zero_rows(cuda_lib):
     assert torch.equal(h[keep].view(torch.uint8), ref[keep].view(torch.uint8))
 
 
+def test_gate_up_gather_bad_rows_across_a_full_tile(cuda_lib):
+    """Out-of-range row_src entries spread over a 256-row token block and the
+    expert's next block (first and last rows, both sides of each 32-row
+    boundary) each give a zero row; every other row matches the dense stage
+    bit for bit (prefill workload, full size)."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[2]
+    d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    counts = disp.counts.cpu().numpy().astype(np.int64)
+    e = int(np.argmax(counts))
+    assert counts[e] > 256
+    o = int(disp.offsets[e].item())
+    local = [0, 3, 4, 31, 32, 63, 64, 127, 128, 129, 200, 255, 256, int(counts[e]) - 1]
+    bad = torch.tensor([o + j for j in local], dtype=torch.int64, device=DEV)
+    rs = disp.row_src.clone()
+    rs[bad] = (-16 - torch.arange(len(local), device=DEV)).to(rs.dtype)  # 2^32 - 16 - j as uint32
+    h = moe.moe_experts_gate_up_gather(ex, d["x"], rs, cfg.top_k, disp.offsets)
+    ref = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(h[bad]) == 0
+    keep = torch.ones(h.shape[0], dtype=torch.bool, device=DEV)
+    keep[bad] = False
+    assert torch.equal(h[keep].view(torch.uint8), ref[keep].view(torch.uint8))
+    assert moe.moe_device_status() == 0
+
+
 def test_gate_up_gather_rejects_bad_arguments(cuda_lib):
     moe = cuda_lib
     cfg = workloads.SMALL_CONFIGS["bf16_ragged"]

@@ -54,7 +54,11 @@ constexpr int STAGE_SMEM = 192 * 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 constexpr uint32_t TILE_END = 0xFFFFFFFFu;
 constexpr int TBM = 256;                      // DGRAD token block (N of the MMAs)
-constexpr int WN = 256;                       // WGRAD output columns per tile (N)
+// WGRAD output columns per tile (N). 128 for dgate/dup would let their two
+// accumulators fit TMEM twice (epilogue overlapping the next tile's MMAs),
+// but twice the tiles means twice the TMA operations per output byte on a
+// TMA unit the output stores also use: measured slower (536 vs 443 us).
+constexpr int WN = 256;
 
 constexpr uint32_t ST_PRODUCER_EMPTY = 0x21;
 constexpr uint32_t ST_MMA_FULL = 0x22;
@@ -80,7 +84,7 @@ struct BwdCfg {
   static constexpr uint32_t D1 = ACC_N;                                // second accumulator
   static constexpr int SMEM_STAGES = 0;
   static constexpr int XPOSE_WARP =                                      // per epilogue warp
-      MODE == DGRAD_H ? 16 * DH_PITCH * 4 : (DGRAD ? XPOSE_BYTES : 32 * 33 * 4);
+      MODE == DGRAD_H ? 16 * DH_PITCH * 4 : (DGRAD ? XPOSE_BYTES : 32 * 32 * 4);
   static constexpr int SMEM_XPOSE = STAGES * STAGE_BYTES;
   static constexpr int SMEM_BAR = SMEM_XPOSE + NUM_EPI_WARPS * XPOSE_WARP;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
@@ -110,6 +114,11 @@ struct BwdArgs {
   uint32_t* status;
   const void* in_g;         // DGRAD_H: cached pre-activations g, u [rows, n_out]
   const void* in_u;
+  // Nonzero: the A (B) maps view their 64-element atoms as one more dimension
+  // and one copy brings every atom of a k-block (DGRAD A: 4, WGRAD A: 2,
+  // WGRAD B: 4) instead of one copy per atom.
+  int merged_a;
+  int merged_b;
 };
 
 template <typename T, int MODE>
@@ -117,6 +126,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                   const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b0s,
                   const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b1s,
+                  const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
                   const BwdArgs args) {
   using C = BwdCfg<MODE>;
   constexpr bool DGRAD = C::DGRAD;
@@ -245,8 +255,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int k0 = (second ? kb - args.k_blocks : kb) * BK;
             const CUtensorMap* am = second ? &tm_a1 : &tm_a0;
             const int c0 = w.nb * (2 * BM);
+            if (args.merged_a) {
+              tma_load_4d(st, am, &full[stage], 0, k0, c0 / 64, w.e);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tma_load_3d(st + q * BOX, am, &full[stage], c0 + 64 * q, k0, w.e);
+              for (int q = 0; q < 4; ++q) tma_load_3d(st + q * BOX, am, &full[stage], c0 + 64 * q, k0, w.e);
+            }
             const CUtensorMap* b128 = second ? &tm_b1 : &tm_b0;
             const CUtensorMap* b16 = second ? &tm_b1s : &tm_b0s;
             uint8_t* b_dst = st + 2 * A_BYTES;
@@ -260,11 +274,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // B: activations [rows][N], four boxes for 256 columns.
             const int r0 = static_cast<int>(w.row0) + kb * BK;
             const int m0 = w.mb * BM, n0 = w.nb * WN;
-            for (int q = 0; q < 2; ++q) tma_load_2d(st + q * BOX, &tm_a0, &full[stage], m0 + 64 * q, r0);
-            if (C::N_A == 2)
-              for (int q = 0; q < 2; ++q) tma_load_2d(st + A_BYTES + q * BOX, &tm_a1, &full[stage], m0 + 64 * q, r0);
             uint8_t* b_dst = st + C::N_A * A_BYTES;
-            for (int q = 0; q < WN / 64; ++q) tma_load_2d(b_dst + q * BOX, &tm_b0, &full[stage], n0 + 64 * q, r0);
+            if (args.merged_a) {
+              tma_load_3d(st, &tm_a0, &full[stage], 0, r0, m0 / 64);
+              if (C::N_A == 2) tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], 0, r0, m0 / 64);
+            } else {
+              for (int q = 0; q < 2; ++q) tma_load_2d(st + q * BOX, &tm_a0, &full[stage], m0 + 64 * q, r0);
+              if (C::N_A == 2)
+                for (int q = 0; q < 2; ++q)
+                  tma_load_2d(st + A_BYTES + q * BOX, &tm_a1, &full[stage], m0 + 64 * q, r0);
+            }
+            if (args.merged_b) {
+              tma_load_3d(b_dst, &tm_b0, &full[stage], 0, r0, n0 / 64);
+            } else {
+              for (int q = 0; q < WN / 64; ++q) tma_load_2d(b_dst + q * BOX, &tm_b0, &full[stage], n0 + 64 * q, r0);
+            }
           }
           ++issued;
           if (++stage == STAGES) {
@@ -377,7 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quad = warp & 3;
     const int half = ew >> 2;
     uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * C::XPOSE_WARP);
-    float* xf = reinterpret_cast<float*>(smem + C::SMEM_XPOSE + ew * C::XPOSE_WARP);  // WGRAD: [32][33]
+    float* xf = reinterpret_cast<float*>(smem + C::SMEM_XPOSE + ew * C::XPOSE_WARP);
     const int rd_tok = lane >> 2;
     const int rd_part = lane & 3;
     for (uint32_t it = 0;; ++it) {
@@ -405,8 +429,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int blk = 0; blk < 2; ++blk) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_lane + blk * C::D1 + static_cast<uint32_t>(c0), v);
-            tmem_ld_wait();
             const int64_t col = chan0 + blk * BM + rd_part * 8;
+            // This lane's four (token, 8 channels) groups of g and u, loaded
+            // while the accumulator load is in flight.
+            uint4 gq[4], uq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int t_in = c0 + (i >> 1) * 16 + (i & 1) * 8 + rd_tok;
+              gq[i] = uq[i] = make_uint4(0u, 0u, 0u, 0u);
+              if (t_in < w.rows && col + 8 <= args.n_out) {
+                const int64_t off = (static_cast<int64_t>(w.row0) + t_in) * args.n_out + col;
+                gq[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_g) + off));
+                uq[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_u) + off));
+              }
+            }
+            tmem_ld_wait();
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -420,11 +457,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const int64_t off = (static_cast<int64_t>(w.row0) + t_in) * args.n_out + col;
                   const float4 d0 = *reinterpret_cast<const float4*>(xf + j * DH_PITCH + rd_part * 8);
                   const float4 d1 = *reinterpret_cast<const float4*>(xf + j * DH_PITCH + rd_part * 8 + 4);
-                  const uint4 gq = *reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_g) + off);
-                  const uint4 uq = *reinterpret_cast<const uint4*>(static_cast<const T*>(args.in_u) + off);
+                  const uint4 gv4 = gq[hh * 2 + p];
+                  const uint4 uv4 = uq[hh * 2 + p];
                   const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                  const T* gv = reinterpret_cast<const T*>(&gq);
-                  const T* uv = reinterpret_cast<const T*>(&uq);
+                  const T* gv = reinterpret_cast<const T*>(&gv4);
+                  const T* uv = reinterpret_cast<const T*>(&uv4);
                   uint32_t dgw[4], duw[4];
 #pragma unroll
                   for (int q = 0; q < 4; ++q) {
@@ -477,10 +514,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
         // TMEM lane = output row m, column = output n; FP32 [E, M, N]. Each
-        // 32 x 32 block goes through a padded shared transpose (row r at
-        // r * 33: conflict-free both ways) so that every store instruction
-        // writes one output row's 32 consecutive floats.
-        const int64_t m_base = static_cast<int64_t>(w.mb) * BM + quad * 32;
+        // 32 x 32 block is staged in the warp's 4 KB tile with the 128-byte
+        // swizzle (16-byte chunk q of row r at chunk q ^ (r % 8): conflict-
+        // free stores) and written by one TMA tensor store, which clips rows
+        // and columns past the expert's [M, N]. Lane 0 waits for the previous
+        // store to have read the tile before the warp rewrites it.
+        const int m_base = w.mb * BM + quad * 32;
         const bool empty_expert = w.kb_count == 0;
         for (int c0 = 32 * half; c0 < WN; c0 += 64) {
           for (int blk = 0; blk < C::N_A; ++blk) {
@@ -492,16 +531,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;
             }
+            // One staging tile per warp: the previous store must have read it
+            // (a second tile, letting two stores per warp be in flight, was
+            // slower: the stores then crowd the stage loads on the TMA unit).
+            const uint32_t xbuf = smem_u32(xf);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xf[lane * 33 + j] = __uint_as_float(v[j]);
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(xbuf + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                           v[4 * q + 3]);
+            fence_proxy_async_smem();
             __syncwarp();
-            const int64_t n = static_cast<int64_t>(w.nb) * WN + c0 + lane;
-            float* ob = static_cast<float*>(blk == 0 ? args.out0 : args.out1) +
-                        static_cast<int64_t>(w.e) * args.m_out * args.n_out;
-            const int rows_here = static_cast<int>(args.m_out - m_base < 32 ? args.m_out - m_base : 32);
-            if (n < args.n_out)
-              for (int r = 0; r < rows_here; ++r) ob[(m_base + r) * args.n_out + n] = xf[r * 33 + lane];
-            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(blk == 0 ? &tm_o0 : &tm_o1, xbuf, w.nb * WN + c0, m_base, w.e);
+              bulk_commit_group();
+            }
           }
         }
       }
@@ -512,6 +557,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(&tile_empty[slot]);
       }
     }
+    // The tensor stores read shared memory and write the gradients: both end
+    // before the block exits.
+    if (!DGRAD && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -542,7 +591,7 @@ bool enc(CUtensorMap* m, moe_dtype dt, const void* ptr, int rank, const cuuint64
          const cuuint32_t* box) {
   auto fn = encode_fn_bwd();
   if (fn == nullptr) return false;
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, dt == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank,
             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -555,6 +604,44 @@ bool enc_weights_mn(CUtensorMap* m, moe_dtype dt, const void* w, int64_t E, int6
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(M) * 2, static_cast<cuuint64_t>(K * M) * 2};
   const cuuint32_t box[3] = {64, 64, 1};
   return enc(m, dt, w, 3, dims, strides, box);
+}
+
+// FP32 weight gradient [E][M][N] as boxes {32 (N), 32 (M), 1}, 128-byte
+// swizzle (the epilogue's staging layout); rows and columns past [M, N] of an
+// expert are clipped by the store.
+bool enc_grad_out(CUtensorMap* m, const float* p, int64_t E, int64_t M, int64_t N) {
+  auto fn = encode_fn_bwd();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(M * N) * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [E][K][M] weights viewed as {64, K, M / 64, E} (the 64-element atoms of M
+// as a dimension of stride 128 B): box {64, 64, 4, 1} brings the four atoms
+// of a 256-channel block in one copy. Needs M % 64 == 0.
+bool enc_weights_mn_merged(CUtensorMap* m, moe_dtype dt, const void* w, int64_t E, int64_t K, int64_t M) {
+  if (M % 64 != 0) return false;
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M / 64),
+                              static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(M) * 2, 128, static_cast<cuuint64_t>(K * M) * 2};
+  const cuuint32_t box[4] = {64, 64, 4, 1};
+  return enc(m, dt, w, 4, dims, strides, box);
+}
+
+// [rows][C] activations viewed as {64, rows, C / 64}: box {64, 64, atoms}
+// brings `atoms` consecutive 64-element atoms of 64 rows in one copy. Needs
+// C % 64 == 0.
+bool enc_rows_merged(CUtensorMap* m, moe_dtype dt, const void* p, int64_t rows, int64_t C, uint32_t atoms) {
+  if (C % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(C / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2, 128};
+  const cuuint32_t box[3] = {64, 64, atoms};
+  return enc(m, dt, p, 3, dims, strides, box);
 }
 
 // [rows][C] activations as boxes {64 (C), box_rows}.
@@ -575,7 +662,7 @@ cudaError_t launch_mode(const CUtensorMap* maps, const BwdArgs& args, int num_sm
   if (grid <= 0) return cudaSuccess;
   err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
-  kern<<<grid, NUM_THREADS, SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], args);
+  kern<<<grid, NUM_THREADS, SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], args);
   return cudaGetLastError();
 }
 
@@ -585,7 +672,7 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
   uint32_t* status = nullptr;
   cudaError_t err = device_status_ptr(&status);
   if (err != cudaSuccess) return err;
-  CUtensorMap maps[6];
+  CUtensorMap maps[8];  // a0, a1, b0, b0s, b1, b1s, and the WGRAD outputs o0, o1
   auto fail_enc = [&]() {
     *why = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return cudaErrorInvalidValue;
@@ -595,50 +682,65 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
   // dh = dy W_down: A = W_down [E][H][I] (K = H, M = I), B = dy [rows][H];
   // the epilogue turns dh into dg and du with the cached g and u.
   {
-    if (!enc_weights_mn(&maps[0], dt, b.down, E, H, I) || !enc_rows(&maps[2], dt, b.dy, rows, H, 128) ||
+    const bool merged = enc_weights_mn_merged(&maps[0], dt, b.down, E, H, I);
+    if ((!merged && !enc_weights_mn(&maps[0], dt, b.down, E, H, I)) || !enc_rows(&maps[2], dt, b.dy, rows, H, 128) ||
         !enc_rows(&maps[3], dt, b.dy, rows, H, 16))
       return fail_enc();
     maps[1] = maps[0];
     maps[4] = maps[2];
     maps[5] = maps[3];
+    maps[6] = maps[7] = maps[0];
     const int nw = static_cast<int>((I + 2 * BM - 1) / (2 * BM));
     BwdArgs a{offsets, b.dg, b.du, sched, E, nw, 0, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
-              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, b.g, b.u};
+              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, b.g, b.u, merged ? 1 : 0, 0};
     err = launch_mode<T, DGRAD_H>(maps, a, num_sms, s);
     if (err != cudaSuccess) return err;
   }
   // dx = dg W_gate + du W_up: A = W_gate / W_up [E][I][H] (K = I, M = H), B = dg / du [rows][I]
   {
-    if (!enc_weights_mn(&maps[0], dt, b.gate, E, I, H) || !enc_weights_mn(&maps[1], dt, b.up, E, I, H) ||
+    const bool merged =
+        enc_weights_mn_merged(&maps[0], dt, b.gate, E, I, H) && enc_weights_mn_merged(&maps[1], dt, b.up, E, I, H);
+    if ((!merged && (!enc_weights_mn(&maps[0], dt, b.gate, E, I, H) || !enc_weights_mn(&maps[1], dt, b.up, E, I, H))) ||
         !enc_rows(&maps[2], dt, b.dg, rows, I, 128) || !enc_rows(&maps[3], dt, b.dg, rows, I, 16) ||
         !enc_rows(&maps[4], dt, b.du, rows, I, 128) || !enc_rows(&maps[5], dt, b.du, rows, I, 16))
       return fail_enc();
+    maps[6] = maps[7] = maps[0];
     const int nw = static_cast<int>((H + 2 * BM - 1) / (2 * BM));
     BwdArgs a{offsets, b.dx, nullptr, sched, E, nw, 0, static_cast<int>((I + BK - 1) / BK), static_cast<int>(H),
-              0, srows, static_cast<uint32_t>(tok_blocks * nw), status};
+              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, nullptr, nullptr, merged ? 1 : 0, 0};
     err = launch_mode<T, DGRAD_X>(maps, a, num_sms, s);
     if (err != cudaSuccess) return err;
   }
   // ddown[e] = dy^T h: A = dy [rows][H] (M = H), B = h [rows][I] (N = I)
   {
-    if (!enc_rows(&maps[0], dt, b.dy, rows, H, 64) || !enc_rows(&maps[2], dt, b.h, rows, I, 64)) return fail_enc();
+    const bool ma = enc_rows_merged(&maps[0], dt, b.dy, rows, H, 2);
+    const bool mb_ = enc_rows_merged(&maps[2], dt, b.h, rows, I, WN / 64);
+    if ((!ma && !enc_rows(&maps[0], dt, b.dy, rows, H, 64)) || (!mb_ && !enc_rows(&maps[2], dt, b.h, rows, I, 64)) ||
+        !enc_grad_out(&maps[6], b.ddown, E, H, I))
+      return fail_enc();
     maps[1] = maps[0];
     maps[3] = maps[4] = maps[5] = maps[2];
+    maps[7] = maps[6];
     const int mb = static_cast<int>((H + BM - 1) / BM), nb = static_cast<int>((I + WN - 1) / WN);
     BwdArgs a{offsets, b.ddown, nullptr, sched, E, nb, mb, 0, static_cast<int>(I), static_cast<int>(H), srows,
-              static_cast<uint32_t>(static_cast<int64_t>(E) * mb * nb), status};
+              static_cast<uint32_t>(static_cast<int64_t>(E) * mb * nb), status, nullptr, nullptr, ma ? 1 : 0,
+              mb_ ? 1 : 0};
     err = launch_mode<T, WGRAD_D>(maps, a, num_sms, s);
     if (err != cudaSuccess) return err;
   }
   // dgate[e], dup[e] = dg^T x, du^T x: A0 = dg, A1 = du [rows][I] (M = I), B = x [rows][H] (N = H)
   {
-    if (!enc_rows(&maps[0], dt, b.dg, rows, I, 64) || !enc_rows(&maps[1], dt, b.du, rows, I, 64) ||
-        !enc_rows(&maps[2], dt, b.x, rows, H, 64))
+    const bool ma = enc_rows_merged(&maps[0], dt, b.dg, rows, I, 2) && enc_rows_merged(&maps[1], dt, b.du, rows, I, 2);
+    const bool mb_ = enc_rows_merged(&maps[2], dt, b.x, rows, H, WN / 64);
+    if ((!ma && (!enc_rows(&maps[0], dt, b.dg, rows, I, 64) || !enc_rows(&maps[1], dt, b.du, rows, I, 64))) ||
+        (!mb_ && !enc_rows(&maps[2], dt, b.x, rows, H, 64)) || !enc_grad_out(&maps[6], b.dgate, E, I, H) ||
+        !enc_grad_out(&maps[7], b.dup, E, I, H))
       return fail_enc();
     maps[3] = maps[4] = maps[5] = maps[2];
     const int mb = static_cast<int>((I + BM - 1) / BM), nb = static_cast<int>((H + WN - 1) / WN);
     BwdArgs a{offsets, b.dgate, b.dup, sched, E, nb, mb, 0, static_cast<int>(H), static_cast<int>(I), srows,
-              static_cast<uint32_t>(static_cast<int64_t>(E) * mb * nb), status};
+              static_cast<uint32_t>(static_cast<int64_t>(E) * mb * nb), status, nullptr, nullptr, ma ? 1 : 0,
+              mb_ ? 1 : 0};
     err = launch_mode<T, WGRAD_GU>(maps, a, num_sms, s);
   }
   return err;

@@ -26,11 +26,13 @@ constexpr int TB_M = 64, TB_N = 64, TB_K = 16, TB_THREADS = 256;
 constexpr int CB_MAX_K = 1024;
 
 // ------------------------------------------------------------------ combine backward
-// One block per token: dexpert[inv[t,j]] = w[t,j] * dout[t] and
-// dweights[t,j] = <dout[t], y[inv[t,j]]> (FP32, a fixed reduction tree). A
-// slot whose inv entry is out of range gets a NaN dweight and no dexpert row.
-// Each thread owns NV consecutive columns (16-byte vectors when the rows are
-// 16-byte multiples); slots are taken in groups of 8.
+// One warp per token: dexpert[inv[t,j]] = w[t,j] * dout[t] and
+// dweights[t,j] = <dout[t], y[inv[t,j]]> (FP32: each lane's columns in order,
+// then a butterfly over the warp). A slot whose inv entry is out of range
+// gets a NaN dweight and no dexpert row. Lane l owns the NV-element vectors
+// at columns (l + 32 i) * NV (16-byte vectors when the rows are 16-byte
+// multiples); slots are taken in groups of 8. No shared memory and no block
+// barrier: the warps of a block stream their tokens independently.
 template <typename T, int NV>
 struct VecIO {
   static __device__ __forceinline__ void load(const T* p, float (&v)[NV]) {
@@ -59,60 +61,59 @@ struct VecIO {
 };
 
 template <typename T, typename TW, int NV>
-__global__ void __launch_bounds__(256) combine_backward_kernel(
+__global__ void __launch_bounds__(128) combine_backward_kernel(
     const T* __restrict__ y, const uint32_t* __restrict__ inv, const TW* __restrict__ w,
     const T* __restrict__ dout, int64_t T_tokens, int k, int64_t H, uint32_t rows, T* __restrict__ dexpert,
     float* __restrict__ dweights) {
-  __shared__ float s_part[8][8];  // [slot in group][warp]
-  __shared__ uint32_t s_row[8];
-  __shared__ float s_w[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const float qnan = __int_as_float(0x7FC00000);
-  for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T_tokens;
+       t += warps) {
     for (int j0 = 0; j0 < k; j0 += 8) {
       const int nj = k - j0 < 8 ? k - j0 : 8;
-      __syncthreads();
-      if (threadIdx.x < nj) {
-        s_row[threadIdx.x] = inv[t * k + j0 + threadIdx.x];
-        s_w[threadIdx.x] = to_f32(w[t * k + j0 + threadIdx.x]);
-      }
-      __syncthreads();
-      float part[8];
+      uint32_t r[8];
+      float wq[8], part[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) part[q] = 0.0f;
-      for (int64_t c = static_cast<int64_t>(threadIdx.x) * NV; c < H; c += static_cast<int64_t>(blockDim.x) * NV) {
+      for (int q = 0; q < 8; ++q) {
+        r[q] = q < nj ? inv[t * k + j0 + q] : 0xFFFFFFFFu;
+        wq[q] = q < nj ? to_f32(w[t * k + j0 + q]) : 0.0f;
+        part[q] = 0.0f;
+      }
+#pragma unroll 1
+      for (int64_t c = static_cast<int64_t>(lane) * NV; c < H; c += 32 * NV) {
         float go[NV];
         VecIO<T, NV>::load(dout + t * H + c, go);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          if (q < nj) {
-            const uint32_t r = s_row[q];
-            if (r < rows) {
-              float yv[NV], dv[NV];
-              VecIO<T, NV>::load(y + static_cast<int64_t>(r) * H + c, yv);
+          if (r[q] < rows) {
+            float yv[NV], dv[NV];
+            VecIO<T, NV>::load(y + static_cast<int64_t>(r[q]) * H + c, yv);
 #pragma unroll
-              for (int i = 0; i < NV; ++i) {
-                part[q] = fmaf(go[i], yv[i], part[q]);
-                dv[i] = s_w[q] * go[i];
-              }
-              VecIO<T, NV>::store(dexpert + static_cast<int64_t>(r) * H + c, dv);
+            for (int i = 0; i < NV; ++i) {
+              part[q] = fmaf(go[i], yv[i], part[q]);
+              dv[i] = wq[q] * go[i];
             }
+            VecIO<T, NV>::store(dexpert + static_cast<int64_t>(r[q]) * H + c, dv);
           }
         }
       }
+      // Butterfly over the warp: every lane ends with all eight sums.
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float v = part[q];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(FULL_MASK, v, off);
-        if (lane == 0) s_part[q][warp] = v;
+        for (int off = 16; off > 0; off >>= 1) part[q] += __shfl_xor_sync(FULL_MASK, part[q], off);
       }
-      __syncthreads();
-      if (threadIdx.x < nj) {
+      if (lane < nj) {
         float sum = 0.0f;
-        for (int wi = 0; wi < nwarps; ++wi) sum += s_part[threadIdx.x][wi];
-        dweights[t * k + j0 + threadIdx.x] = s_row[threadIdx.x] < rows ? sum : qnan;
+        uint32_t row = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q == lane) {
+            sum = part[q];
+            row = r[q];
+          }
+        dweights[t * k + j0 + lane] = row < rows ? sum : qnan;
       }
     }
   }
@@ -318,7 +319,8 @@ cudaError_t backward_t(const TrainBuffers& b, const uint32_t* offsets, int E, in
 template <typename T, typename TW>
 cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const void* w, const void* dout, int64_t T_tokens,
                                int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s) {
-  const int blocks = static_cast<int>(T_tokens < 65536 ? T_tokens : 65536);
+  const int64_t want = (T_tokens + 3) / 4;  // four tokens (warps) per block
+  const int blocks = static_cast<int>(want < 65536 ? want : 65536);
   constexpr int NV = 16 / static_cast<int>(sizeof(T));
   const bool vec = (H * static_cast<int64_t>(sizeof(T))) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(dout) % 16 == 0 && reinterpret_cast<uintptr_t>(dexpert) % 16 == 0;
@@ -328,9 +330,9 @@ cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const void* w
   auto* ep = static_cast<T*>(dexpert);
   const uint32_t rows = static_cast<uint32_t>(T_tokens * k);
   if (vec)
-    combine_backward_kernel<T, TW, NV><<<blocks, 256, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
+    combine_backward_kernel<T, TW, NV><<<blocks, 128, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
   else
-    combine_backward_kernel<T, TW, 1><<<blocks, 256, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
+    combine_backward_kernel<T, TW, 1><<<blocks, 128, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
   return cudaGetLastError();
 }
 

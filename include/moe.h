@@ -278,6 +278,34 @@ moe_status moe_forward(const moe_experts* experts, const void* x, const void* lo
                        size_t workspace_bytes, void* stream);
 
 /*
+ * moe_forward_host - moe_forward on host buffers: the inputs are copied from
+ * host memory into device staging in the workspace, the chain runs, and out
+ * is copied back to host memory. Every step is enqueued on `stream` (one
+ * cudaMemcpyAsync per copy, then the kernels); nothing synchronises the host.
+ *
+ *   x_host       host, [T, H] in the experts' dtype.
+ *   logits_host  host, [T, E] in `logits_dtype`.
+ *   out_host     host, [T, H] out in the experts' dtype.
+ *   indices_opt, weights_opt   device outputs as in moe_forward, or NULL.
+ *   workspace    device scratch of moe_forward_host_workspace_size(experts,
+ *                T, top_k, logits_dtype) bytes, 256-byte aligned.
+ *
+ * Same outputs as moe_forward on device copies of x and logits (bit for bit).
+ * With page-locked host buffers the copies are asynchronous: a caller that
+ * runs consecutive batches on two streams with two workspaces overlaps one
+ * batch's copies with the other's kernels. Pageable host memory works, but
+ * each copy then completes before the call returns. The host buffers stay
+ * owned by the caller; they must not be changed (x_host, logits_host) or read
+ * (out_host) until the stream has passed the call's work.
+ */
+size_t moe_forward_host_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k,
+                                       moe_dtype logits_dtype);
+moe_status moe_forward_host(const moe_experts* experts, const void* x_host, const void* logits_host,
+                            moe_dtype logits_dtype, int64_t T, int32_t top_k, int32_t renormalize,
+                            void* out_host, uint32_t* indices_opt, void* weights_opt, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * moe_group_routing_options - GroupRoutingOptions of the group-limited
  * sigmoid routing (ruDNN user guide, section 10).
  *

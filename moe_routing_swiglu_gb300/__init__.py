@@ -79,6 +79,8 @@ SIGNATURES = {
     "moe_combine": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _I64, _I32, _I64, _P, _P]),
     "moe_forward_workspace_size": (_SZ, [_P, _I64, _I32]),
     "moe_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_host_workspace_size": (ctypes.c_size_t, [_P, _I64, _I32, ctypes.c_int]),
+    "moe_forward_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_sigmoid_grouped": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _OPT, _P, _P, _P, _P]),
     "moe_forward_sigmoid_grouped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _P, _OPT, _P, _P, _P, _P,
                                                    _SZ, _P]),
@@ -351,6 +353,28 @@ def moe_forward(experts: Experts, x: torch.Tensor, logits: torch.Tensor, top_k: 
     _check(lib.moe_forward(experts.handle, _ptr(x), _ptr(logits), _dt(logits), T, top_k,
                            int(bool(renormalize)), _ptr(o), _ptr(indices), _ptr(weights), _ptr(ws),
                            ws.numel(), _stream(stream)))
+    return o
+
+
+def moe_forward_host(experts: Experts, x: torch.Tensor, logits: torch.Tensor, top_k: int, renormalize: bool, *,
+                     out=None, indices=None, weights=None, workspace=None, stream=None):
+    """moe_forward on host (CPU) tensors: x [T, H] and logits [T, E] are
+    copied to the device, the chain runs and out [T, H] is copied back, all
+    enqueued on the stream. Pin the host tensors (`pin_memory()`) for
+    asynchronous copies; the result is in `out` once the stream has passed
+    the call's work."""
+    lib = load_library()
+    for t, name in ((x, "x"), (logits, "logits")):
+        if t.is_cuda or not t.is_contiguous():
+            raise MoeError(2, f"{name} must be a contiguous host tensor")
+    T = x.shape[0]
+    o = out if out is not None else torch.empty(T, experts.H, dtype=experts.dtype).pin_memory()
+    if o.is_cuda or not o.is_contiguous():
+        raise MoeError(2, "out must be a contiguous host tensor")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ws = _workspace(lib.moe_forward_host_workspace_size(experts.handle, T, top_k, _dt(logits)), dev, workspace)
+    _check(lib.moe_forward_host(experts.handle, _ptr(x), _ptr(logits), _dt(logits), T, top_k, int(bool(renormalize)),
+                                _ptr(o), _ptr(indices), _ptr(weights), _ptr(ws), ws.numel(), _stream(stream)))
     return o
 
 

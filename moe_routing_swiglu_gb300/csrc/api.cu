@@ -230,6 +230,31 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   return ok();
 }
 
+// moe_forward_host's workspace: moe_forward's, then device staging for x,
+// logits and out, each 256-byte aligned.
+struct HostLayout {
+  size_t fwd, x, logits, out, total;
+  size_t x_bytes, logits_bytes, out_bytes;
+};
+
+HostLayout host_layout(const moe_experts* ex, int64_t T, int top_k, moe_dtype logits_dtype) {
+  HostLayout h{};
+  h.fwd = forward_layout(ex, T, top_k).total;
+  const size_t t = static_cast<size_t>(T);
+  h.x_bytes = t * static_cast<size_t>(ex->H) * dtype_size(ex->dtype);
+  h.logits_bytes = t * static_cast<size_t>(ex->E) * dtype_size(logits_dtype);
+  h.out_bytes = h.x_bytes;
+  size_t off = align_up(h.fwd, 256);
+  h.x = off;
+  off += align_up(h.x_bytes + 1, 256);
+  h.logits = off;
+  off += align_up(h.logits_bytes + 1, 256);
+  h.out = off;
+  off += align_up(h.out_bytes + 1, 256);
+  h.total = off;
+  return h;
+}
+
 // FP32 dh scratch of moe_experts_backward: the F32 path's dgrad writes it;
 // the tensor-core path turns dh into dg and du in the dgrad epilogue.
 size_t backward_dh_bytes(const moe_experts* ex, size_t n) {
@@ -472,6 +497,50 @@ moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
   };
   return forward_chain(ex, x, logits_dtype, T, top_k, out, indices_opt, weights_opt, workspace,
                        workspace_bytes, static_cast<cudaStream_t>(stream), route);
+}
+
+size_t moe_forward_host_workspace_size(const moe_experts* ex, int64_t T, int32_t top_k, moe_dtype logits_dtype) {
+  if (ex == nullptr || T < 0 || top_k < 1 || !slots_fit(T, top_k) || !dtype_valid(logits_dtype)) return 0;
+  return host_layout(ex, T, top_k, logits_dtype).total;
+}
+
+moe_status moe_forward_host(const moe_experts* ex, const void* x_host, const void* logits_host,
+                            moe_dtype logits_dtype, int64_t T, int32_t top_k, int32_t renormalize, void* out_host,
+                            uint32_t* indices_opt, void* weights_opt, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (ex == nullptr) return fail(MOE_ERR_NULL, "experts must be non-NULL");
+  if (!dtype_valid(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (top_k < 1 || top_k > ex->E) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= E");
+  if (T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && (x_host == nullptr || logits_host == nullptr || out_host == nullptr))
+    return fail(MOE_ERR_NULL, "x_host, logits_host and out_host must be non-NULL");
+  const HostLayout h = host_layout(ex, T, top_k, logits_dtype);
+  if (workspace == nullptr || workspace_bytes < h.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_forward_host_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  moe_status st = check_current_device(ex);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* dx = ws + h.x;
+  void* dl = ws + h.logits;
+  void* dout = ws + h.out;
+  st = check_route_args(dl, logits_dtype, T, ex->E, top_k, dl, dl);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(dx, x_host, h.x_bytes, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of x to the device");
+  err = cudaMemcpyAsync(dl, logits_host, h.logits_bytes, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of the logits to the device");
+  auto route = [&](uint32_t* indices, void* weights, cudaStream_t rs) {
+    return moe::launch_route(dl, logits_dtype, T, static_cast<int>(ex->E), top_k, renormalize != 0, indices,
+                             weights, nullptr, rs);
+  };
+  st = forward_chain(ex, dx, logits_dtype, T, top_k, dout, indices_opt, weights_opt, ws, h.fwd, s, route);
+  if (st != MOE_OK) return st;
+  err = cudaMemcpyAsync(out_host, dout, h.out_bytes, cudaMemcpyDeviceToHost, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of out to the host");
+  return ok();
 }
 
 moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_t T, int64_t E,

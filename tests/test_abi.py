@@ -115,6 +115,8 @@ def test_null_handles_are_rejected(lib):
     assert lib.moe_forward(None, FAKE, FAKE, 2, 4, 2, 1, FAKE, None, None, FAKE, 1 << 20, None) == 1
     assert lib.moe_experts_forward_dispatched(None, FAKE, FAKE, 4, FAKE, FAKE, 1 << 20, None) == 1
     assert lib.moe_forward_workspace_size(None, 4, 2) == 0
+    assert lib.moe_forward_host(None, FAKE, FAKE, 2, 4, 2, 1, FAKE, None, None, FAKE, 1 << 20, None) == 1
+    assert lib.moe_forward_host_workspace_size(None, 4, 2, 2) == 0
     assert lib.moe_experts_forward_dispatched_workspace_size(None, 4) == 0
     lib.moe_experts_destroy(None)
 

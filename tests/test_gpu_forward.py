@@ -138,3 +138,57 @@ def test_forward_workspace_too_small_is_rejected(cuda_lib):
     with pytest.raises(moe.MoeError) as err:
         moe.moe_forward(ex, d["x"], d["logits"], cfg.E + 1, True)
     assert err.value.status == 4
+
+
+@pytest.mark.parametrize("name", ["bf16_fine", "f16_zipf", "f32_contract"])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_equals_forward(cuda_lib, name, pinned):
+    """moe_forward_host (host x/logits in, host out back) gives moe_forward's
+    outputs bit for bit, with pinned and with pageable host memory."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS[name]
+    inp = workloads.generate(cfg)
+    out, idx, w, ex = _forward(moe, cfg, _device_inputs(inp))
+    hx, hl = inp["x"].contiguous(), inp["logits"].contiguous()
+    if pinned:
+        hx, hl = hx.pin_memory(), hl.pin_memory()
+    hout = torch.empty(cfg.T, cfg.H, dtype=cfg.torch_dtype)
+    if pinned:
+        hout = hout.pin_memory()
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    moe.moe_forward_host(ex, hx, hl, cfg.top_k, cfg.renormalize, out=hout, indices=idx2, weights=w2)
+    torch.cuda.synchronize()
+    assert torch.equal(hout.view(torch.uint8), out.cpu().view(torch.uint8))
+    assert torch.equal(idx2, idx) and torch.equal(w2.view(torch.uint8), w.view(torch.uint8))
+    assert moe.moe_device_status() == 0
+
+
+def test_forward_host_two_streams_pipelined(cuda_lib):
+    """Consecutive batches alternating over two streams and two workspaces
+    (one batch's copies overlapping the other's kernels), the prefill
+    workload at full size: every batch's host output equals moe_forward's."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[2]
+    base = workloads.generate(cfg)
+    d = _device_inputs(base)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    batches = []
+    for b in range(4):
+        g = torch.Generator().manual_seed(100 + b)
+        x = (torch.randn(cfg.T, cfg.H, generator=g)).to(cfg.torch_dtype).pin_memory()
+        lg = (torch.randn(cfg.T, cfg.E, generator=g)).to(cfg.torch_dtype).pin_memory()
+        batches.append((x, lg))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    nbytes = moe.load_library().moe_forward_host_workspace_size(ex.handle, cfg.T, cfg.top_k, moe._dt(batches[0][1]))
+    wss = [torch.empty(nbytes, dtype=torch.uint8, device=DEV) for _ in range(2)]
+    outs = [torch.empty(cfg.T, cfg.H, dtype=cfg.torch_dtype).pin_memory() for _ in range(4)]
+    for b, (x, lg) in enumerate(batches):
+        moe.moe_forward_host(ex, x, lg, cfg.top_k, cfg.renormalize, out=outs[b], workspace=wss[b % 2],
+                             stream=streams[b % 2])
+    torch.cuda.synchronize()
+    for b, (x, lg) in enumerate(batches):
+        ref = moe.moe_forward(ex, x.to(DEV), lg.to(DEV), cfg.top_k, cfg.renormalize)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[b].view(torch.uint8), ref.cpu().view(torch.uint8)), f"batch {b}"
+    assert moe.moe_device_status() == 0

@@ -446,7 +446,7 @@ def training_step_times(moe, cfg, dev, stream, flush, steps):
         y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
         moe.moe_combine(y, disp.inv, w)
         rec(1)
-        dexp, dw = moe.moe_combine_backward(y, disp.inv, w, grad_out)
+        dexp, dw = moe.moe_combine_backward(y, disp.inv, disp.row_src, w, grad_out)
         rec(2)
         gr = moe.moe_experts_backward(ex, cache, dexp)
         rec(3)

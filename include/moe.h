@@ -442,14 +442,20 @@ moe_status moe_experts_forward_training(const moe_experts* experts, const void* 
  * dexpert rows no slot points at are not written.
  *
  *   y_dispatched  device [T * top_k, H] in `dtype` (the forward's expert output).
+ *   inv, row_src  device [T * top_k] uint32, the two maps of moe_dispatch
+ *                 (slot -> row and row -> slot). The work runs in row order;
+ *                 a row r counts only when inv[row_src[r]] == r, so the
+ *                 entries of row_src past the dispatched rows may hold
+ *                 anything.
  *   weights       device [T, top_k] in `weights_dtype` (the forward's weights).
  *   grad_out      device [T, H] in `dtype`.
  *   dexpert       device [T * top_k, H] out in `dtype`.
  *   dweights      device [T, top_k] float out.
  */
-moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv, const void* weights,
-                                moe_dtype weights_dtype, const void* grad_out, int64_t T, int32_t top_k, int64_t H,
-                                void* dexpert, float* dweights, void* stream);
+moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                                const uint32_t* row_src, const void* weights, moe_dtype weights_dtype,
+                                const void* grad_out, int64_t T, int32_t top_k, int64_t H, void* dexpert,
+                                float* dweights, void* stream);
 
 /*
  * moe_experts_backward - the forward cache's backward: from dexpert [rows, H]

@@ -88,8 +88,8 @@ SIGNATURES = {
     "moe_router_backward": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P,
                                            _P]),
     "moe_experts_forward_training": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_combine_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _I64, _I32, _I64, _P, _P,
-                                            _P]),
+    "moe_combine_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P, _I64, _I32, _I64, _P,
+                                            _P, _P]),
     "moe_experts_backward_workspace_size": (_SZ, [_P, _I64]),
     "moe_experts_backward": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _I32, _I64, _P, _P]),
@@ -516,18 +516,22 @@ def moe_experts_backward(experts: Experts, cache: TrainingCache, dexpert: torch.
     return ExpertGrads(dx, dgate, dup, ddown)
 
 
-def moe_combine_backward(y_dispatched: torch.Tensor, inv: torch.Tensor, weights: torch.Tensor,
-                         grad_out: torch.Tensor, stream=None):
-    """combine_backward: (dexpert [rows, H] in y's dtype, dweights [T, top_k] FP32)."""
+def moe_combine_backward(y_dispatched: torch.Tensor, inv: torch.Tensor, row_src: torch.Tensor,
+                         weights: torch.Tensor, grad_out: torch.Tensor, stream=None):
+    """combine_backward: (dexpert [rows, H] in y's dtype, dweights [T, top_k]
+    FP32). inv and row_src are moe_dispatch's two maps."""
     lib = load_library()
-    for name, t in (("y_dispatched", y_dispatched), ("inv", inv), ("weights", weights), ("grad_out", grad_out)):
+    for name, t in (("y_dispatched", y_dispatched), ("inv", inv), ("row_src", row_src), ("weights", weights),
+                    ("grad_out", grad_out)):
         _dev_tensor(t, name)
     T, k = weights.shape
+    if inv.numel() != T * k or row_src.numel() != T * k:
+        raise MoeError(2, "inv and row_src must hold T * top_k entries")
     H = y_dispatched.shape[1]
     dexp = torch.empty_like(y_dispatched)
     dw = torch.empty(T, k, dtype=torch.float32, device=y_dispatched.device)
-    _check(lib.moe_combine_backward(_ptr(y_dispatched), _dt(y_dispatched), _ptr(inv), _ptr(weights), _dt(weights),
-                                    _ptr(grad_out), T, k, H, _ptr(dexp), _ptr(dw), _stream(stream)))
+    _check(lib.moe_combine_backward(_ptr(y_dispatched), _dt(y_dispatched), _ptr(inv), _ptr(row_src), _ptr(weights),
+                                    _dt(weights), _ptr(grad_out), T, k, H, _ptr(dexp), _ptr(dw), _stream(stream)))
     return dexp, dw
 
 

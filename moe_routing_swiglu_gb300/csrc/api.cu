@@ -638,18 +638,19 @@ moe_status moe_router_backward(const void* logits, moe_dtype dtype, int64_t T, i
   return ok();
 }
 
-moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv, const void* weights,
-                                moe_dtype weights_dtype, const void* grad_out, int64_t T, int32_t top_k, int64_t H,
-                                void* dexpert, float* dweights, void* stream) {
+moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
+                                const uint32_t* row_src, const void* weights, moe_dtype weights_dtype,
+                                const void* grad_out, int64_t T, int32_t top_k, int64_t H, void* dexpert,
+                                float* dweights, void* stream) {
   if (!dtype_valid(dtype) || !dtype_valid(weights_dtype)) return fail(MOE_ERR_DTYPE, "unknown dtype");
   if (top_k < 1) return fail(MOE_ERR_TOP_K, "top_k must be >= 1");
   if (H < 1 || T < 0 || !slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "need H >= 1, T >= 0, T*top_k < 2^32-1");
-  if (T > 0 && (y_dispatched == nullptr || inv == nullptr || weights == nullptr || grad_out == nullptr ||
-                dexpert == nullptr || dweights == nullptr))
+  if (T > 0 && (y_dispatched == nullptr || inv == nullptr || row_src == nullptr || weights == nullptr ||
+                grad_out == nullptr || dexpert == nullptr || dweights == nullptr))
     return fail(MOE_ERR_NULL, "every buffer must be non-NULL");
   if (T == 0) return ok();
-  cudaError_t err = moe::launch_combine_backward(y_dispatched, dtype, inv, weights, weights_dtype, grad_out, T, top_k,
-                                                 H, dexpert, dweights, static_cast<cudaStream_t>(stream));
+  cudaError_t err = moe::launch_combine_backward(y_dispatched, dtype, inv, row_src, weights, weights_dtype, grad_out,
+                                                 T, top_k, H, dexpert, dweights, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "moe_combine_backward launch");
   return ok();
 }

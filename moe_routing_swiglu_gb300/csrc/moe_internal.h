@@ -128,8 +128,9 @@ cudaError_t launch_router_backward(const void* logits, moe_dtype dtype, int64_t 
                                    int index_type, int top_k, const RouterParams& p, const float* grad_weights,
                                    void* dlogits, cudaStream_t stream);
 cudaError_t launch_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
-                                    const void* weights, moe_dtype weights_dtype, const void* grad_out, int64_t T,
-                                    int top_k, int64_t H, void* dexpert, float* dweights, cudaStream_t stream);
+                                    const uint32_t* row_src, const void* weights, moe_dtype weights_dtype,
+                                    const void* grad_out, int64_t T, int top_k, int64_t H, void* dexpert,
+                                    float* dweights, cudaStream_t stream);
 cudaError_t launch_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* inv, int64_t T,
                                      int top_k, int64_t H, void* dx, cudaStream_t stream);
 struct TrainBuffers {

@@ -23,16 +23,17 @@ namespace moe {
 namespace {
 
 constexpr int TB_M = 64, TB_N = 64, TB_K = 16, TB_THREADS = 256;
-constexpr int CB_MAX_K = 1024;
 
 // ------------------------------------------------------------------ combine backward
-// One warp per token: dexpert[inv[t,j]] = w[t,j] * dout[t] and
-// dweights[t,j] = <dout[t], y[inv[t,j]]> (FP32: each lane's columns in order,
-// then a butterfly over the warp). A slot whose inv entry is out of range
-// gets a NaN dweight and no dexpert row. Lane l owns the NV-element vectors
-// at columns (l + 32 i) * NV (16-byte vectors when the rows are 16-byte
-// multiples); slots are taken in groups of 8. No shared memory and no block
-// barrier: the warps of a block stream their tokens independently.
+// dexpert[r] = w[s] * dout[s / k] and dweights[s] = <dout[s / k], y[r]> (FP32:
+// each lane's columns in order, then a butterfly over the warp) for every
+// dispatched row r, s = row_src[r]. One warp per row, so y is read and
+// dexpert written as sequential row streams (in slot order both would be
+// scattered 4 KB rows: measured 1.4x slower). A row is real when
+// inv[row_src[r]] == r (row_src past the dispatched rows is not consulted
+// otherwise); warp r also gives slot r a NaN dweight when inv[r] is out of
+// range (such a slot has no row). Lane l owns the NV-element vectors at
+// columns (l + 32 i) * NV (16-byte vectors when rows are 16-byte multiples).
 template <typename T, int NV>
 struct VecIO {
   static __device__ __forceinline__ void load(const T* p, float (&v)[NV]) {
@@ -61,61 +62,35 @@ struct VecIO {
 };
 
 template <typename T, typename TW, int NV>
-__global__ void __launch_bounds__(128) combine_backward_kernel(
-    const T* __restrict__ y, const uint32_t* __restrict__ inv, const TW* __restrict__ w,
-    const T* __restrict__ dout, int64_t T_tokens, int k, int64_t H, uint32_t rows, T* __restrict__ dexpert,
-    float* __restrict__ dweights) {
+__global__ void __launch_bounds__(256) combine_backward_kernel(
+    const T* __restrict__ y, const uint32_t* __restrict__ inv, const uint32_t* __restrict__ row_src,
+    const TW* __restrict__ w, const T* __restrict__ dout, int k, int64_t H, uint32_t nslots,
+    T* __restrict__ dexpert, float* __restrict__ dweights) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const float qnan = __int_as_float(0x7FC00000);
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T_tokens;
-       t += warps) {
-    for (int j0 = 0; j0 < k; j0 += 8) {
-      const int nj = k - j0 < 8 ? k - j0 : 8;
-      uint32_t r[8];
-      float wq[8], part[8];
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nslots;
+       r += warps) {
+    if (lane == 0 && inv[r] >= nslots) dweights[r] = qnan;  // slot r has no row
+    const uint32_t s = row_src[r];
+    if (s >= nslots || inv[s] != static_cast<uint32_t>(r)) continue;
+    const int64_t t = s / static_cast<uint32_t>(k);
+    const float wq = to_f32(w[s]);
+    float part = 0.0f;
+    for (int64_t c = static_cast<int64_t>(lane) * NV; c < H; c += 32 * NV) {
+      float go[NV], yv[NV], dv[NV];
+      VecIO<T, NV>::load(dout + t * H + c, go);
+      VecIO<T, NV>::load(y + r * H + c, yv);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        r[q] = q < nj ? inv[t * k + j0 + q] : 0xFFFFFFFFu;
-        wq[q] = q < nj ? to_f32(w[t * k + j0 + q]) : 0.0f;
-        part[q] = 0.0f;
+      for (int i = 0; i < NV; ++i) {
+        part = fmaf(go[i], yv[i], part);
+        dv[i] = wq * go[i];
       }
-#pragma unroll 1
-      for (int64_t c = static_cast<int64_t>(lane) * NV; c < H; c += 32 * NV) {
-        float go[NV];
-        VecIO<T, NV>::load(dout + t * H + c, go);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (r[q] < rows) {
-            float yv[NV], dv[NV];
-            VecIO<T, NV>::load(y + static_cast<int64_t>(r[q]) * H + c, yv);
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-              part[q] = fmaf(go[i], yv[i], part[q]);
-              dv[i] = wq[q] * go[i];
-            }
-            VecIO<T, NV>::store(dexpert + static_cast<int64_t>(r[q]) * H + c, dv);
-          }
-        }
-      }
-      // Butterfly over the warp: every lane ends with all eight sums.
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part[q] += __shfl_xor_sync(FULL_MASK, part[q], off);
-      }
-      if (lane < nj) {
-        float sum = 0.0f;
-        uint32_t row = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q == lane) {
-            sum = part[q];
-            row = r[q];
-          }
-        dweights[t * k + j0 + lane] = row < rows ? sum : qnan;
-      }
+      VecIO<T, NV>::store(dexpert + r * H + c, dv);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
+    if (lane == 0) dweights[s] = part;
   }
 }
 
@@ -317,9 +292,11 @@ cudaError_t backward_t(const TrainBuffers& b, const uint32_t* offsets, int E, in
 }
 
 template <typename T, typename TW>
-cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const void* w, const void* dout, int64_t T_tokens,
-                               int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s) {
-  const int64_t want = (T_tokens + 3) / 4;  // four tokens (warps) per block
+cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const uint32_t* row_src, const void* w,
+                               const void* dout, int64_t T_tokens, int k, int64_t H, void* dexpert, float* dweights,
+                               cudaStream_t s) {
+  const uint32_t nslots = static_cast<uint32_t>(T_tokens * k);
+  const int64_t want = (static_cast<int64_t>(nslots) + 7) / 8;  // eight rows (warps) per block
   const int blocks = static_cast<int>(want < 65536 ? want : 65536);
   constexpr int NV = 16 / static_cast<int>(sizeof(T));
   const bool vec = (H * static_cast<int64_t>(sizeof(T))) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
@@ -328,42 +305,44 @@ cudaError_t combine_backward_t(const void* y, const uint32_t* inv, const void* w
   const auto* wp = static_cast<const TW*>(w);
   const auto* dp = static_cast<const T*>(dout);
   auto* ep = static_cast<T*>(dexpert);
-  const uint32_t rows = static_cast<uint32_t>(T_tokens * k);
   if (vec)
-    combine_backward_kernel<T, TW, NV><<<blocks, 128, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
+    combine_backward_kernel<T, TW, NV><<<blocks, 256, 0, s>>>(yp, inv, row_src, wp, dp, k, H, nslots, ep, dweights);
   else
-    combine_backward_kernel<T, TW, 1><<<blocks, 128, 0, s>>>(yp, inv, wp, dp, T_tokens, k, H, rows, ep, dweights);
+    combine_backward_kernel<T, TW, 1><<<blocks, 256, 0, s>>>(yp, inv, row_src, wp, dp, k, H, nslots, ep, dweights);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t combine_backward_w(const void* y, const uint32_t* inv, const void* w, moe_dtype wdt, const void* dout,
-                               int64_t T_tokens, int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s) {
+cudaError_t combine_backward_w(const void* y, const uint32_t* inv, const uint32_t* row_src, const void* w,
+                               moe_dtype wdt, const void* dout, int64_t T_tokens, int k, int64_t H, void* dexpert,
+                               float* dweights, cudaStream_t s) {
   switch (wdt) {
-    case MOE_F32: return combine_backward_t<T, float>(y, inv, w, dout, T_tokens, k, H, dexpert, dweights, s);
-    case MOE_F16: return combine_backward_t<T, __half>(y, inv, w, dout, T_tokens, k, H, dexpert, dweights, s);
-    default: return combine_backward_t<T, __nv_bfloat16>(y, inv, w, dout, T_tokens, k, H, dexpert, dweights, s);
+    case MOE_F32:
+      return combine_backward_t<T, float>(y, inv, row_src, w, dout, T_tokens, k, H, dexpert, dweights, s);
+    case MOE_F16:
+      return combine_backward_t<T, __half>(y, inv, row_src, w, dout, T_tokens, k, H, dexpert, dweights, s);
+    default:
+      return combine_backward_t<T, __nv_bfloat16>(y, inv, row_src, w, dout, T_tokens, k, H, dexpert, dweights, s);
   }
 }
 
 }  // namespace
 
-static_assert(CB_MAX_K >= 1, "combine backward handles any top_k in groups of 8");
-
 cudaError_t launch_combine_backward(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
-                                    const void* weights, moe_dtype weights_dtype, const void* grad_out, int64_t T,
-                                    int top_k, int64_t H, void* dexpert, float* dweights, cudaStream_t stream) {
+                                    const uint32_t* row_src, const void* weights, moe_dtype weights_dtype,
+                                    const void* grad_out, int64_t T, int top_k, int64_t H, void* dexpert,
+                                    float* dweights, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   switch (dtype) {
     case MOE_F32:
-      return combine_backward_w<float>(y_dispatched, inv, weights, weights_dtype, grad_out, T, top_k, H, dexpert,
-                                       dweights, stream);
+      return combine_backward_w<float>(y_dispatched, inv, row_src, weights, weights_dtype, grad_out, T, top_k, H,
+                                       dexpert, dweights, stream);
     case MOE_F16:
-      return combine_backward_w<__half>(y_dispatched, inv, weights, weights_dtype, grad_out, T, top_k, H, dexpert,
-                                        dweights, stream);
+      return combine_backward_w<__half>(y_dispatched, inv, row_src, weights, weights_dtype, grad_out, T, top_k, H,
+                                        dexpert, dweights, stream);
     default:
-      return combine_backward_w<__nv_bfloat16>(y_dispatched, inv, weights, weights_dtype, grad_out, T, top_k, H,
-                                               dexpert, dweights, stream);
+      return combine_backward_w<__nv_bfloat16>(y_dispatched, inv, row_src, weights, weights_dtype, grad_out, T,
+                                               top_k, H, dexpert, dweights, stream);
   }
 }
 

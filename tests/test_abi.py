@@ -203,9 +203,10 @@ def test_training_entry_points_reject_null_buffers(lib):
     o = moe.RouterWeightOptions("sigmoid", False, 1.0)
     assert lib.moe_router_backward(FAKE, 2, 4, 8, FAKE, 1, 2, ctypes.byref(o), None, FAKE, None) == 1
     assert lib.moe_router_backward(FAKE, 2, 0, 8, None, 1, 2, ctypes.byref(o), None, None, None) == 0
-    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, 2, None, 4, 2, 64, FAKE, FAKE, None) == 1
-    assert lib.moe_combine_backward(FAKE, 9, FAKE, FAKE, 2, FAKE, 4, 2, 64, FAKE, FAKE, None) == 3
-    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, 2, FAKE, 4, 0, 64, FAKE, FAKE, None) == 4
+    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, FAKE, 2, None, 4, 2, 64, FAKE, FAKE, None) == 1
+    assert lib.moe_combine_backward(FAKE, 2, FAKE, None, FAKE, 2, FAKE, 4, 2, 64, FAKE, FAKE, None) == 1
+    assert lib.moe_combine_backward(FAKE, 9, FAKE, FAKE, FAKE, 2, FAKE, 4, 2, 64, FAKE, FAKE, None) == 3
+    assert lib.moe_combine_backward(FAKE, 2, FAKE, FAKE, FAKE, 2, FAKE, 4, 0, 64, FAKE, FAKE, None) == 4
     assert lib.moe_dispatch_backward(None, 2, FAKE, 4, 2, 64, FAKE, None) == 1
     assert lib.moe_dispatch_backward(FAKE, 2, FAKE, 4, 2, 0, FAKE, None) == 2
     assert lib.moe_experts_forward_training(None, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 10, None) == 1

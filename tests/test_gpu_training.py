@@ -143,7 +143,12 @@ def test_combine_and_dispatch_backward_parity(cuda_lib, name):
     go = torch.randn(cfg.T, cfg.H, generator=g).to(cfg.torch_dtype)
     w = torch.from_numpy(rt.weights).to(cfg.torch_dtype)
     inv = torch.from_numpy(dp.inv.astype(np.int64)).to(torch.int32)
-    dexp, dw = moe.moe_combine_backward(y.to(DEV), inv.to(DEV), w.to(DEV), go.to(DEV))
+    # row -> slot for the dispatched rows; the entries past them hold an
+    # invalid slot (the kernel only trusts rows with inv[row_src[r]] == r)
+    rs = np.full(n, 0xFFFFFFFF, dtype=np.uint32)
+    rs[:dp.row_src.size] = dp.row_src
+    row_src = torch.from_numpy(rs.view(np.int32).copy())
+    dexp, dw = moe.moe_combine_backward(y.to(DEV), inv.to(DEV), row_src.to(DEV), w.to(DEV), go.to(DEV))
     torch.cuda.synchronize()
     ref_dexp, ref_dw = oracle.combine_backward(y, dp.inv, f64(w), go, cfg.T, cfg.top_k)
     used = int(dp.offsets[-1])
@@ -195,7 +200,7 @@ def test_whole_training_step_matches_oracle(cuda_lib):
     y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
     g = torch.Generator().manual_seed(23)
     go = (torch.randn(cfg.T, cfg.H, generator=g)).to(cfg.torch_dtype)
-    dexp, dw = moe.moe_combine_backward(y, disp.inv, w, go.to(DEV))
+    dexp, dw = moe.moe_combine_backward(y, disp.inv, disp.row_src, w, go.to(DEV))
     gr = moe.moe_experts_backward(ex, cache, dexp)
     dx = moe.moe_dispatch_backward(gr.dx_dispatched, disp.inv, cfg.T, cfg.top_k)
     o = Opt("softmax", True, 1.0)
@@ -258,3 +263,26 @@ def test_experts_backward_full_size_sampled_experts(cuda_lib):
         _grad_close(f64(gr.dup[e:e + 1]), ref.dup, ref.dup_abs, cfg.torch_dtype, f"dup (expert {e})")
         _grad_close(f64(gr.ddown[e:e + 1]), ref.ddown, ref.ddown_abs, cfg.torch_dtype, f"ddown (expert {e})")
     assert moe.moe_device_status() == 0
+
+
+def test_combine_backward_ignores_row_src_past_the_dispatched_rows(cuda_lib):
+    """row_src entries past the dispatched rows (here: a token with an invalid
+    index, so one row fewer than slots) may hold anything, even a valid slot:
+    the results equal those with a clean row_src."""
+    moe = cuda_lib
+    idx = torch.tensor([[0, 1], [1, 9], [2, 0]], dtype=torch.int32)   # slot 3 is invalid: 5 rows for 6 slots
+    d = moe.moe_dispatch(idx.to(DEV), 3)
+    g = torch.Generator().manual_seed(3)
+    y = torch.randn(6, 64, generator=g).to(torch.bfloat16).to(DEV)
+    go = torch.randn(3, 64, generator=g).to(torch.bfloat16).to(DEV)
+    w = torch.rand(3, 2, generator=g).to(torch.bfloat16).to(DEV)
+    clean = d.row_src.clone()
+    clean[5] = -1
+    dirty = d.row_src.clone()
+    dirty[5] = 0                                                      # a valid slot, not this row's
+    e1, w1 = moe.moe_combine_backward(y, d.inv, clean, w, go)
+    e2, w2 = moe.moe_combine_backward(y, d.inv, dirty, w, go)
+    torch.cuda.synchronize()
+    assert torch.equal(e1[:5].view(torch.uint8), e2[:5].view(torch.uint8))
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
+    assert torch.isnan(w1[1, 1]) and torch.isfinite(w1[0]).all()

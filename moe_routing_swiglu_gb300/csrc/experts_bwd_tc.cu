@@ -53,7 +53,13 @@ constexpr int DH_PITCH = 36;                  // DGRAD_H: FP32 [16 tokens][36] s
 constexpr int STAGE_SMEM = 192 * 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 constexpr uint32_t TILE_END = 0xFFFFFFFFu;
-constexpr int TBM = 256;                      // DGRAD token block (N of the MMAs)
+// DGRAD token block (N of the MMAs). dh: 128, so that its two accumulators
+// (2 x 128 channels x 128 tokens) fit TMEM twice and the heavy SiLU-backward
+// epilogue of one tile overlaps the MMAs of the next (193 -> 146 us at the
+// prefill workload); dx: 256 (its light epilogue gains nothing from the
+// overlap and 128-token tiles re-stream its weights: 193 -> 215 us).
+template <int MODE>
+constexpr int dgrad_tbm() { return MODE == DGRAD_H ? 128 : 256; }
 // WGRAD output columns per tile (N). 128 for dgate/dup would let their two
 // accumulators fit TMEM twice (epilogue overlapping the next tile's MMAs),
 // but twice the tiles means twice the TMA operations per output byte on a
@@ -72,6 +78,7 @@ template <int MODE>
 struct BwdCfg {
   static constexpr bool DGRAD = MODE == DGRAD_H || MODE == DGRAD_X;
   static constexpr int N_A = (MODE == WGRAD_D) ? 1 : 2;                // MMAs per k-step
+  static constexpr int TBM = dgrad_tbm<MODE>();
   static constexpr int B_BYTES = DGRAD ? TBM * 128 : (WN / 64) * BOX;  // B operand per stage
   static constexpr int STAGE_BYTES = N_A * A_BYTES + B_BYTES;
   // WGRAD keeps 32 KB for its FP32 output transposes.
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_b1);
   }
   __syncwarp();
-  if (DGRAD && warp == 0) build_tile_prefix(args.offsets, args.E, TBM, args.n_wblocks, tile_start);
+  if (DGRAD && warp == 0) build_tile_prefix(args.offsets, args.E, C::TBM, args.n_wblocks, tile_start);
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto decode = [&](uint32_t tile) {
     Work w;
     if (DGRAD) {
-      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TBM, args.n_wblocks);
+      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, C::TBM, args.n_wblocks);
       w.e = tc.e;
       w.mb = tc.m;
       w.nb = tc.n;
@@ -677,7 +684,7 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
     *why = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return cudaErrorInvalidValue;
   };
-  const int64_t tok_blocks = rows / TBM + (rows < E ? rows : E);
+  auto tok_blocks = [&](int tbm) { return rows / tbm + (rows < E ? rows : E); };
   const uint32_t srows = static_cast<uint32_t>(rows);
   // dh = dy W_down: A = W_down [E][H][I] (K = H, M = I), B = dy [rows][H];
   // the epilogue turns dh into dg and du with the cached g and u.
@@ -692,7 +699,8 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
     maps[6] = maps[7] = maps[0];
     const int nw = static_cast<int>((I + 2 * BM - 1) / (2 * BM));
     BwdArgs a{offsets, b.dg, b.du, sched, E, nw, 0, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
-              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, b.g, b.u, merged ? 1 : 0, 0};
+              0, srows, static_cast<uint32_t>(tok_blocks(dgrad_tbm<DGRAD_H>()) * nw), status, b.g, b.u,
+              merged ? 1 : 0, 0};
     err = launch_mode<T, DGRAD_H>(maps, a, num_sms, s);
     if (err != cudaSuccess) return err;
   }
@@ -707,7 +715,8 @@ cudaError_t backward_tc_t(moe_dtype dt, const TrainBuffers& b, const uint32_t* o
     maps[6] = maps[7] = maps[0];
     const int nw = static_cast<int>((H + 2 * BM - 1) / (2 * BM));
     BwdArgs a{offsets, b.dx, nullptr, sched, E, nw, 0, static_cast<int>((I + BK - 1) / BK), static_cast<int>(H),
-              0, srows, static_cast<uint32_t>(tok_blocks * nw), status, nullptr, nullptr, merged ? 1 : 0, 0};
+              0, srows, static_cast<uint32_t>(tok_blocks(dgrad_tbm<DGRAD_X>()) * nw), status, nullptr, nullptr,
+              merged ? 1 : 0, 0};
     err = launch_mode<T, DGRAD_X>(maps, a, num_sms, s);
     if (err != cudaSuccess) return err;
   }

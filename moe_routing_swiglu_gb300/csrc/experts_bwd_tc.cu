@@ -62,8 +62,8 @@ template <int MODE>
 constexpr int dgrad_tbm() { return MODE == DGRAD_H ? 128 : 256; }
 // WGRAD output columns per tile (N). 128 for dgate/dup would let their two
 // accumulators fit TMEM twice (epilogue overlapping the next tile's MMAs),
-// but twice the tiles means twice the TMA operations per output byte on a
-// TMA unit the output stores also use: measured slower (536 vs 443 us).
+// but the tiles double and each re-loads its dg/du operand: measured slower
+// at the prefill workload (463 vs 444 us).
 constexpr int WN = 256;
 
 constexpr uint32_t ST_PRODUCER_EMPTY = 0x21;

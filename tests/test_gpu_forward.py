@@ -192,3 +192,44 @@ def test_forward_host_two_streams_pipelined(cuda_lib):
         torch.cuda.synchronize()
         assert torch.equal(outs[b].view(torch.uint8), ref.cpu().view(torch.uint8)), f"batch {b}"
     assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("T", [0, 1, 3])
+def test_forward_host_tiny_token_counts(cuda_lib, T):
+    """moe_forward_host on 0, 1 and 3 tokens equals moe_forward (T = 0: an
+    empty output, no copies)."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_fine"].scaled("tiny", T=max(T, 1), seed=99)
+    inp = workloads.generate(cfg)
+    hx, hl = inp["x"][:T].contiguous().pin_memory(), inp["logits"][:T].contiguous().pin_memory()
+    d = _device_inputs(inp)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    out = moe.moe_forward_host(ex, hx, hl, cfg.top_k, cfg.renormalize)
+    torch.cuda.synchronize()
+    assert out.shape == (T, cfg.H) and not out.is_cuda
+    if T:
+        ref = moe.moe_forward(ex, hx.to(DEV), hl.to(DEV), cfg.top_k, cfg.renormalize)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.uint8), ref.cpu().view(torch.uint8))
+
+
+def test_forward_host_rejects_bad_arguments(cuda_lib):
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_ragged"]
+    inp = workloads.generate(cfg)
+    d = _device_inputs(inp)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    hx, hl = inp["x"].contiguous().pin_memory(), inp["logits"].contiguous().pin_memory()
+    lib = moe.load_library()
+    need = lib.moe_forward_host_workspace_size(ex.handle, cfg.T, cfg.top_k, moe._dt(hl))
+    assert need >= lib.moe_forward_workspace_size(ex.handle, cfg.T, cfg.top_k)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_forward_host(ex, hx, hl, cfg.top_k, True, workspace=ws)
+    assert err.value.status == 6
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_forward_host(ex, hx, hl, cfg.E + 1, True)
+    assert err.value.status == 4
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward_host(ex, d["x"], hl, cfg.top_k, True)      # a device tensor where host memory belongs
+    assert lib.moe_forward_host_workspace_size(ex.handle, cfg.T, cfg.top_k, 7) == 0

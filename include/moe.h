@@ -465,7 +465,9 @@ moe_status moe_combine_backward(const void* y_dispatched, moe_dtype dtype, const
  *   dh = W_down^T dy; dg = dh * u * SiLU'(g); du = dh * SiLU(g);
  *   dx = W_gate^T dg + W_up^T du; ddown = dy h^T; dgate = dg x^T; dup = du x^T.
  *   workspace  moe_experts_backward_workspace_size(experts, rows) bytes,
- *              256-byte aligned (dh in FP32, dg and du in the dtype).
+ *              256-byte aligned (dg and du in the dtype; F32 experts also
+ *              keep dh there in FP32, F16/BF16 experts turn dh into dg and du
+ *              inside the dgrad GEMM).
  */
 size_t moe_experts_backward_workspace_size(const moe_experts* experts, int64_t rows);
 moe_status moe_experts_backward(const moe_experts* experts, const void* x_dispatched, const uint32_t* offsets,

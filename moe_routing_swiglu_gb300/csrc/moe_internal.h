@@ -153,9 +153,6 @@ struct TrainBuffers {
 // CUDA-core backward (every dtype; the F32 path).
 cudaError_t launch_experts_backward(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,
                                     int64_t rows, int64_t H, int64_t I, cudaStream_t stream);
-// dg = dh * u * SiLU'(g), du = dh * SiLU(g) over n elements, rounded to the dtype.
-cudaError_t launch_silu_backward(moe_dtype dtype, const float* dh, const void* g, const void* u, int64_t n,
-                                 void* dg, void* du, cudaStream_t stream);
 // Tensor-core backward (F16/BF16): dgrad and wgrad grouped GEMMs on tcgen05
 // (experts_bwd_tc.cu); sched is one uint32 of device memory.
 cudaError_t launch_experts_backward_tc(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,

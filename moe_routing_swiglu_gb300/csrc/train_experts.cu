@@ -13,9 +13,9 @@
 // SiLU'(g) = s (1 + g (1 - s)) with s the logistic function of g.
 // Here the GEMMs accumulate in FP32 on CUDA cores (64 x 64 output tiles, 4 x 4
 // per thread): the F32 experts' path (no TF32, as in the forward); F16/BF16
-// run them on the tensor cores (experts_bwd_tc.cu) and share the SiLU
-// backward below. dh stays FP32, dg and du are rounded to the dtype like the
-// forward's activations, the weight gradients are FP32.
+// run them on the tensor cores (experts_bwd_tc.cu, with the SiLU backward in
+// the dgrad epilogue). dh stays FP32, dg and du are rounded to the dtype like
+// the forward's activations, the weight gradients are FP32.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -346,28 +346,6 @@ cudaError_t launch_combine_backward(const void* y_dispatched, moe_dtype dtype, c
   }
 }
 
-cudaError_t launch_silu_backward(moe_dtype dtype, const float* dh, const void* g, const void* u, int64_t n,
-                                 void* dg, void* du, cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  const int blocks = static_cast<int>(n / 256 + 1 < 152 * 16 ? n / 256 + 1 : 152 * 16);
-  switch (dtype) {
-    case MOE_F32:
-      silu_backward_kernel<float><<<blocks, 256, 0, stream>>>(dh, static_cast<const float*>(g),
-                                                              static_cast<const float*>(u), n,
-                                                              static_cast<float*>(dg), static_cast<float*>(du));
-      break;
-    case MOE_F16:
-      silu_backward_kernel<__half><<<blocks, 256, 0, stream>>>(dh, static_cast<const __half*>(g),
-                                                               static_cast<const __half*>(u), n,
-                                                               static_cast<__half*>(dg), static_cast<__half*>(du));
-      break;
-    default:
-      silu_backward_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-          dh, static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(u), n,
-          static_cast<__nv_bfloat16*>(dg), static_cast<__nv_bfloat16*>(du));
-  }
-  return cudaGetLastError();
-}
 
 cudaError_t launch_experts_backward(moe_dtype dtype, const TrainBuffers& b, const uint32_t* offsets, int E,
                                     int64_t rows, int64_t H, int64_t I, cudaStream_t stream) {

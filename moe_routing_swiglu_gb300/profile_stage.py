@@ -8,8 +8,9 @@ dispatch run once to set up the stage's inputs, then the chosen stage runs
 Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
 row_src), down, combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
-variant in ``workloads.GROUPED``), and backward (the experts' backward of
-first-order training on a random output gradient).
+variant in ``workloads.GROUPED``), backward (the experts' backward of
+first-order training on a random output gradient) and combine_backward (the
+combine's backward on a random output gradient).
 """
 from __future__ import annotations
 
@@ -35,7 +36,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="cfg2", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
                     choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "combine", "forward",
-                             "route_grouped", "backward"])
+                             "route_grouped", "backward", "combine_backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     cfg = names[args.workload]
@@ -61,6 +62,9 @@ def main(argv=None):
         _, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
         g = torch.Generator().manual_seed(7)
         dy = torch.randn(cfg.T * cfg.top_k, cfg.H, generator=g).to(cfg.torch_dtype).to(dev)
+    if args.stage == "combine_backward":
+        g = torch.Generator().manual_seed(7)
+        grad_out = torch.randn(cfg.T, cfg.H, generator=g).to(cfg.torch_dtype).to(dev)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         if args.stage == "route":
@@ -79,6 +83,8 @@ def main(argv=None):
             moe.moe_experts_backward(ex, cache, dy)
         elif args.stage == "combine":
             moe.moe_combine(y, disp.inv, w)
+        elif args.stage == "combine_backward":
+            moe.moe_combine_backward(y, disp.inv, disp.row_src, w, grad_out)
         else:
             moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, cfg.renormalize)
     torch.cuda.synchronize()

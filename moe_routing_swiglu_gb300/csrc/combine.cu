@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
   __shared__ float s_w[COMBINE_MAX_K];
   __shared__ int s_bad;
   grid_dependency_wait();
+  launch_dependents();
   const float qnan = __int_as_float(0x7FC00000);
   for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
     __syncthreads();

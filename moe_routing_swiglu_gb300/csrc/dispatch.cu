@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const uint32_t* __r
                                                              uint32_t* __restrict__ hist) {
   __shared__ uint32_t h[ROUTE_MAX_E];
   grid_dependency_wait();
+  launch_dependents();
   constexpr int PER = DISPATCH_CHUNK / 256;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK;
   uint32_t e_reg[PER];
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
   __shared__ uint32_t warp_sums[SCATTER_WARPS];
   constexpr int STEPS = SLOTS_PER_WARP / 32;
   grid_dependency_wait();
+  launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK +
                      static_cast<int64_t>(warp) * SLOTS_PER_WARP;
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
 // With no slots at all the scatter kernel has no blocks: write zero counts/offsets.
 __global__ void dispatch_empty_kernel(int E, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets) {
   grid_dependency_wait();
+  launch_dependents();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     if (e < E) counts[e] = 0;
     offsets[e] = 0;
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const VecT* __rest
                                                               int E, int k, int64_t vec_per_row,
                                                               VecT* __restrict__ xd) {
   grid_dependency_wait();
+  launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t rows = offsets[E];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(SB_THREADS) experts_simt_kernel(
   __shared__ float B0s[SB_K][SB_N + 4];
   __shared__ float B1s[GATE_UP ? SB_K : 1][SB_N + 4];
   grid_dependency_wait();
+  launch_dependents();
   const int n_tiles = static_cast<int>((N + SB_N - 1) / SB_N);
   if (threadIdx.x < 32) build_tile_prefix(offsets, E, SB_M, n_tiles, tile_start);
   __syncthreads();

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         if (lane == 0) {
           ring[slot] = TILE_END;
           mbar_arrive(&tile_full[slot]);
+          launch_dependents();  // this CTA claims no more tiles
         }
         break;
       }
@@ -371,7 +372,10 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         const uint32_t tile = claimed < total ? claimed : TILE_END;
         ring[slot] = tile;
         mbar_arrive(&tile_full[slot]);  // release: the ring entry is visible to the waiters
-        if (tile == TILE_END) break;
+        if (tile == TILE_END) {
+          launch_dependents();  // this CTA claims no more tiles
+          break;
+        }
         const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
         const int n_tok = (tc.rows + 15) & ~15;        // N of this tile
         const int n128 = n_tok >> 7;                   // 128-row boxes

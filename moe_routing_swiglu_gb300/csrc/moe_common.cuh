@@ -81,6 +81,14 @@ __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code) {
 // wrote or writing anything it reads. Returns at once otherwise.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Let the kernel launched after this one as a programmatic dependent start
+// once every block of this grid has reached this point (or exited): its blocks
+// then run their prologue while this grid finishes, and they still wait in
+// grid_dependency_wait for this grid's completion before touching its data.
+// Every block of this grid has started by then, so the dependent's blocks can
+// never hold resources that one of this grid's blocks still needs.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- grouped-GEMM tile plan
 
 // Tiles of a grouped GEMM: expert e owns ceil(count_e / bm) row tiles times

@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(const TL* __res
                                                                  float* __restrict__ weights32) {
   __shared__ __align__(16) float e_sm[ROUTE_WARPS][32 * V];
   grid_dependency_wait();
+  launch_dependents();
   const int lane = threadIdx.x & 31;
   float* my_e = e_sm[threadIdx.x >> 5];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

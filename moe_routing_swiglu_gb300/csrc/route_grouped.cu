@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(GR_WARPS * 32)
   __shared__ uint8_t grp_sm[ROUTE_MAX_E];
   __shared__ __align__(16) float c_sm[GR_WARPS][32 * V];
   grid_dependency_wait();
+  launch_dependents();
   const int lane = threadIdx.x & 31;
   float* my_c = c_sm[threadIdx.x >> 5];
 

@@ -352,20 +352,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         uint8_t* st = smem + C::SMEM_STAGES + stage * STAGE_BYTES;
+        // MMAs (16 K-rows each) of this stage: all 4, except in WGRAD's last
+        // k-block, where those wholly past the expert's end are skipped.
+        int n_sub = BK / UMMA_K;
         if (!DGRAD) {
-          // Rows of this k-block past the expert's end belong to the next
-          // expert: zero them in every box before the MMAs read the stage.
+          // Rows past the expert's end belong to the next expert (or are the
+          // tensor's zero fill). Inside the last MMA that runs they are zeroed
+          // in every box before the MMAs read the stage: at most 15 rows, each
+          // a 128-byte line of its box, four rows per warp store.
           const int valid = w.rows - kb * BK;
           if (valid < BK) {
-            constexpr int boxes = C::N_A * 2 + WN / 64;
-            const int bad_rows = BK - valid;
-            for (int i = lane; i < boxes * bad_rows * 8; i += 32) {
-              const int bx = i / (bad_rows * 8);
-              const int rr = valid + (i / 8) % bad_rows;
-              const int ch = i % 8;
-              *reinterpret_cast<uint4*>(st + bx * BOX + rr * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+            n_sub = (valid + UMMA_K - 1) / UMMA_K;
+            const int end = n_sub * UMMA_K;
+            if (valid < end) {
+              constexpr int boxes = C::N_A * 2 + WN / 64;
+              const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+              for (int bx = 0; bx < boxes; ++bx)
+                for (int rr = valid + (lane >> 3); rr < end; rr += 4)
+                  *reinterpret_cast<uint4*>(st + bx * BOX + rr * 128 + (lane & 7) * 16) = z;
+              fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             __syncwarp();
           }
         }
@@ -376,6 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b = a0 + C::N_A * A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
+            if (k >= n_sub) break;
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
             // A: MN-major, 16 K-rows per MMA = 2 atoms of 8 rows (2 KB).
             const uint64_t ad0 = sdesc_mnmajor_sw128(a0 + k * 2048, BOX, 1024);

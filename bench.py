@@ -56,7 +56,7 @@ METRIC = "MoE fwd tokens/s + grouped-GEMM TFLOP/s vs bf16 peak; decode HBM GB/s"
 PREFILL = workloads.CONFIGS[2]
 DECODE = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 7  # route, dispatch count + scatter + gather, gate/up GEMM, down GEMM, combine
+KERNELS_PER_STEP = 6  # route, dispatch count + scatter + gather, gate/up + down GEMMs (one launch), combine
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -118,7 +118,9 @@ ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
   L.row_src = take(n * 4);
   L.inv = take(n * 4);
   L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
-  L.sched = take(moe::TC_SCHED_BYTES);
+  // Tile counters, then (from word 64) one ready counter per expert for the
+  // chained gate/up + down kernel.
+  L.sched = take(moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4);
   L.xd = take(moe::forward_gathers_rows(static_cast<int64_t>(n), ex->E) ? 0 : n * static_cast<size_t>(ex->H) * es);
   L.h = take(n * static_cast<size_t>(ex->I) * es);
   L.yd = take(n * static_cast<size_t>(ex->H) * es);
@@ -212,19 +214,32 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   // GEMM streams with 128-row TMA boxes (a row gather costs about as much
   // TMA time as a whole box, so gathering every weight tile's 256 rows is
   // slower there than the extra copy).
-  // The dispatch's scatter kernel zeroes the two GEMMs' tile counters, so
-  // the chain is kernels only (each launched as a dependent of the previous).
+  // The dispatch's scatter kernel zeroes the GEMMs' tile counter and the
+  // per-expert ready counters, so the chain is kernels only (each launched
+  // as a dependent of the previous). F16/BF16: gate/up and down run as one
+  // launch whose down tiles start on each expert as soon as its h rows are
+  // stored; F32: two launches.
   uint32_t* sched = reinterpret_cast<uint32_t*>(ws + L.sched);
+  uint32_t* ready = sched + moe::TC_SCHED_BYTES / 4;
   cudaError_t err = route(indices, weights, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
   err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
-                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched);
+                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched,
+                             static_cast<int>(moe::TC_SCHED_BYTES / 4 + ex->E));
   if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
   const moe::TcGather gather{x, row_src, top_k, T};
-  st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, sched, s, nullptr, true);
-  if (st != MOE_OK) return st;
-  st = run_stage(ex, false, h, nullptr, offsets, rows, yd, sched + 1, s, nullptr, true);
-  if (st != MOE_OK) return st;
+  if (ex->dtype == MOE_F32) {
+    st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, sched, s, nullptr, true);
+    if (st != MOE_OK) return st;
+    st = run_stage(ex, false, h, nullptr, offsets, rows, yd, sched + 1, s, nullptr, true);
+    if (st != MOE_OK) return st;
+  } else {
+    const char* why = nullptr;
+    err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, xd, gather_rows ? &gather : nullptr, offsets,
+                                       static_cast<int>(ex->E), rows, ex->H, ex->I, h, yd, sched, ready, ex->num_sms,
+                                       s, &why);
+    if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
+  }
   err = moe::launch_combine(yd, ex->dtype, inv, weights, logits_dtype, T, top_k, ex->H, out, s);
   if (err != cudaSuccess) return cuda_fail(err, "forward combine launch");
   return ok();

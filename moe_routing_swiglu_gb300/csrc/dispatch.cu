@@ -56,7 +56,7 @@ template <bool SINGLE>
 __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     const uint32_t* __restrict__ indices, int64_t n, int E, int nchunks,
     const uint32_t* __restrict__ hist, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets,
-    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv, uint32_t* __restrict__ zero_words) {
+    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv, uint32_t* __restrict__ zero_words, int n_zero) {
   __shared__ uint32_t wh[SCATTER_WARPS][ROUTE_MAX_E];
   __shared__ uint32_t first[ROUTE_MAX_E];   // first row of this chunk per expert
   __shared__ uint32_t tot[ROUTE_MAX_E];
@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
   constexpr int STEPS = SLOTS_PER_WARP / 32;
   grid_dependency_wait();
   launch_dependents();
+  // The counters of the expert GEMMs that follow in moe_forward (tile
+  // counter and per-expert ready counters).
+  if (blockIdx.x == 0 && zero_words != nullptr)
+    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK +
                      static_cast<int64_t>(warp) * SLOTS_PER_WARP;
@@ -146,8 +150,6 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
       uint32_t all = 0;
       for (int w = 0; w < SCATTER_WARPS; ++w) all += warp_sums[w];
       offsets[E] = all;
-      // The tile counters of the expert GEMMs that follow in moe_forward.
-      if (zero_words != nullptr) zero_words[0] = zero_words[1] = 0u;
     }
   }
   if (!SINGLE && blockIdx.x == 0) {
@@ -249,19 +251,19 @@ size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                            cudaStream_t stream, uint32_t* zero_words) {
+                            cudaStream_t stream, uint32_t* zero_words, int n_zero) {
   const int64_t n = T * top_k;
   const int nchunks = static_cast<int>((n + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
   uint32_t* hist = static_cast<uint32_t*>(scratch);
   cudaError_t err = cudaSuccess;
   if (nchunks == 1) {
     err = launch_dependent(dispatch_scatter_kernel<true>, dim3(1), dim3(SCATTER_WARPS * 32), 0, stream, indices, n, E,
-                           1, hist, counts, offsets, row_src, inv, zero_words);
+                           1, hist, counts, offsets, row_src, inv, zero_words, n_zero);
   } else if (nchunks > 1) {
     err = launch_dependent(dispatch_count_kernel, dim3(nchunks), dim3(256), 0, stream, indices, n, E, hist);
     if (err == cudaSuccess)
       err = launch_dependent(dispatch_scatter_kernel<false>, dim3(nchunks), dim3(SCATTER_WARPS * 32), 0, stream,
-                             indices, n, E, nchunks, hist, counts, offsets, row_src, inv, zero_words);
+                             indices, n, E, nchunks, hist, counts, offsets, row_src, inv, zero_words, n_zero);
   } else {
     dispatch_empty_kernel<<<1, 256, 0, stream>>>(E, counts, offsets);
   }

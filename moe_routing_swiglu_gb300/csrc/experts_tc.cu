@@ -114,9 +114,13 @@ struct TcCfg {
   static constexpr int SMEM_BAD = SMEM_MISC + 16;                  // [RING][BAD_WORDS]
   static constexpr int SMEM_TILES = SMEM_BAD + 4 * RING * BAD_WORDS;
   static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
+  // The chained gate/up + down kernel keeps a second tile prefix (the down
+  // tiles') after the first.
+  static constexpr int SMEM_TILES2 = SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
+  static constexpr int SMEM_BYTES_CHAIN = SMEM_BYTES + 4 * (ROUTE_MAX_E + 1);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(STAGES >= 3, "pipeline depth");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM_BYTES_CHAIN <= 227 * 1024, "shared memory budget");
   static_assert(TBM % 32 == 0 && TBM <= 256, "token block");
   static_assert(2 * TBM <= static_cast<int>(ACC_COLS), "D0 and D1 fit one accumulator buffer");
 };
@@ -130,6 +134,7 @@ constexpr uint32_t ST_MMA_DRAIN = 0x15;
 constexpr uint32_t ST_PRODUCER_DRAIN = 0x16;
 constexpr uint32_t ST_TILE_RING = 0x17;
 constexpr uint32_t ST_LOADER_EMPTY = 0x18;
+constexpr uint32_t ST_CHAIN_READY = 0x19;
 constexpr uint32_t ST_SELFTEST = 0x100;
 
 struct TcArgs {
@@ -152,6 +157,15 @@ struct TcArgs {
   // Training mode (K3 only): the pre-activations g and u, [rows, I] each.
   void* out_g;
   void* out_u;
+  // Chained mode (K3 then K4 in one launch): the down tiles' output y
+  // [rows, n_out2], their weight blocks per expert and k-blocks, and one
+  // counter per expert (zero at launch) that each gate/up epilogue warp
+  // raises once its h rows are stored.
+  void* out2;
+  int n_wblocks2;
+  int k_blocks2;
+  int n_out2;
+  uint32_t* ready;
 };
 
 // SiLU(g) = g * sigmoid(g), sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
@@ -165,12 +179,25 @@ __device__ __forceinline__ float silu_f32(float g) {
 // Tensor maps: a0/a1 weight tiles (128-row boxes: K3 gate/up, K4 down rows
 // n0 and n0+128), b128/b16 token rows in 128-row and 16-row boxes
 // (TOK_GATHER4: b128 is x with a one-row box).
-template <typename T, bool GATE_UP, int TBM, int LOAD>
+// CHAIN: one launch runs K3's tiles and then K4's from one tile counter
+// (GATE_UP is then ignored): tiles [0, n_gu) are gate/up tiles over a0/a1
+// (gate, up) and b128/b16 (x rows), the rest down tiles over a2 (down) and
+// c128/c16 (h rows, written by this launch's gate/up tiles). A down tile of
+// expert e waits until every gate/up tile of e has stored its h rows (a
+// per-expert counter, bounded wait): CTAs that run out of gate/up tiles
+// start the down GEMM of the experts already done instead of idling until
+// the last gate/up tile ends. Every gate/up tile is claimed before any down
+// tile, by a running CTA, so every wait ends.
+template <typename T, bool GATE_UP, int TBM, int LOAD, bool CHAIN = false>
 __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
                       const __grid_constant__ CUtensorMap tm_b128,
-                      const __grid_constant__ CUtensorMap tm_b16, const TcArgs args) {
+                      const __grid_constant__ CUtensorMap tm_b16,
+                      const __grid_constant__ CUtensorMap tm_a2,
+                      const __grid_constant__ CUtensorMap tm_c128,
+                      const __grid_constant__ CUtensorMap tm_c16, const TcArgs args) {
+  static_assert(!CHAIN || LOAD != TOK_CPASYNC, "the chained kernel streams dense or row-gathered tokens");
   using C = TcCfg<TBM>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
@@ -190,6 +217,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC + 4);
   volatile uint32_t* tile_bad = reinterpret_cast<volatile uint32_t*>(smem + C::SMEM_BAD);
   uint32_t* tile_start = reinterpret_cast<uint32_t*>(smem + C::SMEM_TILES);
+  uint32_t* tile_start2 = reinterpret_cast<uint32_t*>(smem + C::SMEM_TILES2);  // CHAIN: down tiles
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,6 +245,11 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     tma_prefetch_desc(&tm_a1);
     tma_prefetch_desc(&tm_b128);
     tma_prefetch_desc(&tm_b16);
+    if (CHAIN) {
+      tma_prefetch_desc(&tm_a2);
+      tma_prefetch_desc(&tm_c128);
+      tma_prefetch_desc(&tm_c16);
+    }
   }
   __syncwarp();
   if (warp == 1) {
@@ -227,12 +260,23 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
   // here on the kernel reads what earlier kernels wrote (offsets, rows).
   grid_dependency_wait();
   if (warp == 0) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks, tile_start);
+  if (CHAIN && warp == 2) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks2, tile_start2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // The cap keeps a corrupt offsets array from producing an endless tile loop.
-  const uint32_t total = min(tile_start[args.E], args.tile_cap);
+  const uint32_t n_gu = CHAIN ? tile_start[args.E] : 0u;
+  const uint32_t total = min(CHAIN ? n_gu + tile_start2[args.E] : tile_start[args.E], args.tile_cap);
+  // Tile -> coordinates, and whether it is a gate/up tile.
+  auto tile_coord = [&](uint32_t tile, bool& gu) -> TileCoord {
+    if (!CHAIN || tile < n_gu) {
+      gu = CHAIN ? true : GATE_UP;
+      return decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+    }
+    gu = false;
+    return decode_tile(tile - n_gu, tile_start2, args.E, args.offsets, TB, args.n_wblocks2);
+  };
 
   if (warp == 0 && LOAD == TOK_GATHER4) {
     // ------------------------------------------------------------ scheduler + TMA producer, row gathers
@@ -265,12 +309,13 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         }
         break;
       }
-      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+      bool gu;
+      const TileCoord tc = tile_coord(tile, gu);
       const int n_tok = (tc.rows + 15) & ~15;
       // Rows past the tile's rows (up to its 16-row N) read x row 0: their
       // outputs are never written. A row whose token is out of range reads
       // row 0 too and is flagged, and the epilogue writes zeros for it (the
-      // outputs of a zero x row).
+      // outputs of a zero x row). Down tiles (CHAIN) read h densely: no flags.
       int tok[G4][4];
       uint32_t nib[G4];
 #pragma unroll
@@ -280,7 +325,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * (lane + 32 * g) + i;
           uint32_t t = 0;
-          if (r < tc.rows && tc.row0 + static_cast<uint32_t>(r) < args.rows_total) {
+          if (gu && r < tc.rows && tc.row0 + static_cast<uint32_t>(r) < args.rows_total) {
             t = args.row_src[tc.row0 + r] / static_cast<uint32_t>(args.top_k);
             if (t >= args.x_rows) {
               nib[g] |= 1u << i;
@@ -308,33 +353,55 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         ring[slot] = tile;
         mbar_arrive(&tile_full[slot]);  // release: the ring entry and flags are visible to the waiters
       }
+      if (CHAIN && !gu) {
+        // The expert's h rows: every gate/up tile of it has stored them.
+        bool ready = true;
+        if (lane == 0) {
+          const uint32_t need = static_cast<uint32_t>(NUM_EPI_WARPS) * (tile_start[tc.e + 1] - tile_start[tc.e]);
+          ready = counter_wait_bounded(args.ready + tc.e, need, abort_flag, args.status, ST_CHAIN_READY,
+                                       WAIT_LIMIT_NS);
+        }
+        if (__shfl_sync(FULL_MASK, ready ? 1 : 0, 0) == 0) {
+          ok = false;
+          break;
+        }
+      }
       const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + n_tok * ROW_BYTES);
       const int n_gather = n_tok >> 2;
-      const int wrow = tc.n * BM;
-      for (int kb = 0; kb < args.k_blocks; ++kb) {
+      const int wrow0 = gu ? tc.n * BM : tc.n * (2 * BM);
+      const int wrow1 = gu ? tc.n * BM : tc.n * (2 * BM) + BM;
+      const int k_blocks = CHAIN && !gu ? args.k_blocks2 : args.k_blocks;
+      for (int kb = 0; kb < k_blocks; ++kb) {
         uint8_t* st = smem + C::SMEM_STAGES + stage * STAGE_BYTES;
         const int k0 = kb * BK;
+        uint8_t* b_dst = st + 2 * A_BYTES;
         bool got = true;
         if (lane == 0) {
           got = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status, ST_PRODUCER_EMPTY,
                                   WAIT_LIMIT_NS);
           if (got) {
             mbar_arrive_expect_tx(&full[stage], tx);
-            tma_load_3d(st, &tm_a0, &full[stage], k0, wrow, tc.e);
-            tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], k0, wrow, tc.e);
+            tma_load_3d(st, CHAIN && !gu ? &tm_a2 : &tm_a0, &full[stage], k0, wrow0, tc.e);
+            tma_load_3d(st + A_BYTES, CHAIN && !gu ? &tm_a2 : &tm_a1, &full[stage], k0, wrow1, tc.e);
+            if (CHAIN && !gu) {
+              // h rows in 16-row boxes (a decode tile has at most TBM = 32).
+              for (int r = 0; r < n_tok; r += 16)
+                tma_load_2d(b_dst + r * ROW_BYTES, &tm_c16, &full[stage], k0, static_cast<int>(tc.row0) + r);
+            }
           }
         }
         if (__shfl_sync(FULL_MASK, got ? 1 : 0, 0) == 0) {
           ok = false;
           break;
         }
-        uint8_t* b_dst = st + 2 * A_BYTES;
+        if (gu) {
 #pragma unroll
-        for (int g = 0; g < G4; ++g) {
-          const int gi = lane + 32 * g;
-          if (gi < n_gather)
-            tma_gather4(b_dst + gi * 4 * ROW_BYTES, &tm_b128, &full[stage], k0, tok[g][0], tok[g][1], tok[g][2],
-                        tok[g][3]);
+          for (int g = 0; g < G4; ++g) {
+            const int gi = lane + 32 * g;
+            if (gi < n_gather)
+              tma_gather4(b_dst + gi * 4 * ROW_BYTES, &tm_b128, &full[stage], k0, tok[g][0], tok[g][1], tok[g][2],
+                          tok[g][3]);
+          }
         }
         ++issued;
         if (++stage == STAGES) {
@@ -376,14 +443,29 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
           launch_dependents();  // this CTA claims no more tiles
           break;
         }
-        const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+        bool gu;
+        const TileCoord tc = tile_coord(tile, gu);
         const int n_tok = (tc.rows + 15) & ~15;        // N of this tile
         const int n128 = n_tok >> 7;                   // 128-row boxes
         const int n16 = (n_tok & 127) >> 4;            // then 16-row boxes
         const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + (GATHER ? 0 : n_tok * ROW_BYTES));
-        const int wrow0 = GATE_UP ? tc.n * BM : tc.n * (2 * BM);
-        const int wrow1 = GATE_UP ? tc.n * BM : tc.n * (2 * BM) + BM;
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        const int wrow0 = gu ? tc.n * BM : tc.n * (2 * BM);
+        const int wrow1 = gu ? tc.n * BM : tc.n * (2 * BM) + BM;
+        const int k_blocks = CHAIN && !gu ? args.k_blocks2 : args.k_blocks;
+        // Down tile (CHAIN): the expert's h rows, once every gate/up tile of
+        // it has stored them.
+        if (CHAIN && !gu &&
+            !counter_wait_bounded(args.ready + tc.e,
+                                  static_cast<uint32_t>(NUM_EPI_WARPS) * (tile_start[tc.e + 1] - tile_start[tc.e]),
+                                  abort_flag, args.status, ST_CHAIN_READY, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const CUtensorMap* ma0 = CHAIN && !gu ? &tm_a2 : &tm_a0;
+        const CUtensorMap* ma1 = CHAIN && !gu ? &tm_a2 : &tm_a1;
+        const CUtensorMap* mb128 = CHAIN && !gu ? &tm_c128 : &tm_b128;
+        const CUtensorMap* mb16 = CHAIN && !gu ? &tm_c16 : &tm_b16;
+        for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  ST_PRODUCER_EMPTY, WAIT_LIMIT_NS)) {
             ok = false;
@@ -392,15 +474,15 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
           uint8_t* st = smem + C::SMEM_STAGES + stage * STAGE_BYTES;
           const int k0 = kb * BK;
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_3d(st, &tm_a0, &full[stage], k0, wrow0, tc.e);
-          tma_load_3d(st + A_BYTES, &tm_a1, &full[stage], k0, wrow1, tc.e);
+          tma_load_3d(st, ma0, &full[stage], k0, wrow0, tc.e);
+          tma_load_3d(st + A_BYTES, ma1, &full[stage], k0, wrow1, tc.e);
           if (!GATHER) {
             uint8_t* b_dst = st + 2 * A_BYTES;
             int r = 0;
             for (int b = 0; b < n128; ++b, r += 128)
-              tma_load_2d(b_dst + r * ROW_BYTES, &tm_b128, &full[stage], k0, static_cast<int>(tc.row0) + r);
+              tma_load_2d(b_dst + r * ROW_BYTES, mb128, &full[stage], k0, static_cast<int>(tc.row0) + r);
             for (int b = 0; b < n16; ++b, r += 16)
-              tma_load_2d(b_dst + r * ROW_BYTES, &tm_b16, &full[stage], k0, static_cast<int>(tc.row0) + r);
+              tma_load_2d(b_dst + r * ROW_BYTES, mb16, &full[stage], k0, static_cast<int>(tc.row0) + r);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -437,8 +519,10 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         }
         const uint32_t tile = ring[slot];
         if (tile == TILE_END) break;
-        const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+        bool gu;
+        const TileCoord tc = tile_coord(tile, gu);
         const int n_tok = (tc.rows + 15) & ~15;
+        const int k_blocks = CHAIN && !gu ? args.k_blocks2 : args.k_blocks;
         const uint32_t idesc = idesc_f16(kBF16, BM, n_tok);
         const uint32_t acc = it % C::ACC;             // accumulator buffer of this tile
         const uint32_t acc_use = it / C::ACC;         // earlier tiles on this buffer
@@ -449,7 +533,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status, ST_MMA_FULL,
                                  WAIT_LIMIT_NS)) {
             ok = false;
@@ -498,7 +582,8 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
                                   ST_TILE_RING, WAIT_LIMIT_NS);
       const uint32_t tile = ok ? static_cast<uint32_t>(ring[slot]) : static_cast<uint32_t>(TILE_END);
       if (!__all_sync(FULL_MASK, ok) || tile == TILE_END) break;
-      const TileCoord tc = decode_tile(tile, tile_start, args.E, args.offsets, TB, args.n_wblocks);
+      bool gu;
+      const TileCoord tc = tile_coord(tile, gu);
       const uint32_t acc = it % C::ACC;
       ok = mbar_wait_bounded(&tfull[acc], (it / C::ACC) & 1u, abort_flag, args.status, ST_EPI_TMEM_FULL,
                              WAIT_LIMIT_NS);
@@ -508,9 +593,14 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
       const int n_tok = (tc.rows + 15) & ~15;
       const uint32_t t_lane = tmem_base + acc * C::ACC_COLS + (static_cast<uint32_t>(quad * 32) << 16);
       const volatile uint32_t* bad = tile_bad + slot * BAD_WORDS;  // TOK_GATHER4: rows to write as zeros
+      // The tile's outputs, compiled once per tile kind (G: gate/up).
+      auto drain = [&](auto g_tag) {
+      constexpr bool G = decltype(g_tag)::value;
       // Output columns of this warp's 32 lanes (two blocks for K4).
-      const int64_t colA = GATE_UP ? static_cast<int64_t>(tc.n) * BM + quad * 32
-                                   : static_cast<int64_t>(tc.n) * (2 * BM) + quad * 32;
+      const int64_t colA = G ? static_cast<int64_t>(tc.n) * BM + quad * 32
+                              : static_cast<int64_t>(tc.n) * (2 * BM) + quad * 32;
+      void* const out_main = CHAIN && !G ? args.out2 : args.out;
+      const int n_out = CHAIN && !G ? args.n_out2 : args.n_out;
       for (int c0 = 32 * half; c0 < n_tok; c0 += 64) {
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0), v0);
@@ -518,13 +608,13 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         tmem_ld_wait();
         // K3 writes h, and in training mode also the pre-activations g and u
         // (the forward cache); K4 writes its two 128-column blocks.
-        const int n_blk = GATE_UP ? (args.out_g != nullptr ? 3 : 1) : 2;
+        const int n_blk = G ? (args.out_g != nullptr ? 3 : 1) : 2;
         for (int blk = 0; blk < n_blk; ++blk) {
           // Lane = output column, j = token: write column-major, read token rows.
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             float val;
-            if (GATE_UP) {
+            if (G) {
               const float gv = __uint_as_float(v0[j]), uv = __uint_as_float(v1[j]);
               val = blk == 0 ? silu_f32(gv) * uv : (blk == 1 ? gv : uv);
             } else {
@@ -534,28 +624,41 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
             xp[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
           }
           __syncwarp();
-          const int64_t col = colA + ((GATE_UP || blk == 0) ? 0 : BM) + rd_part * 8;
-          void* out_base = !GATE_UP || blk == 0 ? args.out : (blk == 1 ? args.out_g : args.out_u);
+          const int64_t col = colA + ((G || blk == 0) ? 0 : BM) + rd_part * 8;
+          void* out_base = !G || blk == 0 ? out_main : (blk == 1 ? args.out_g : args.out_u);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int j = p * 8 + rd_tok;
             const uint4 row = *reinterpret_cast<const uint4*>(xp + j * 32 + rd_part * 8);
             const int t_in = c0 + j;
             if (t_in < tc.rows && tc.row0 + static_cast<uint32_t>(t_in) < args.rows_total &&
-                col + 8 <= args.n_out) {
-              T* dst = static_cast<T*>(out_base) + (static_cast<int64_t>(tc.row0) + t_in) * args.n_out + col;
-              const bool zero = LOAD == TOK_GATHER4 && ((bad[t_in >> 5] >> (t_in & 31)) & 1u) != 0;
+                col + 8 <= n_out) {
+              T* dst = static_cast<T*>(out_base) + (static_cast<int64_t>(tc.row0) + t_in) * n_out + col;
+              const bool zero = LOAD == TOK_GATHER4 && G && ((bad[t_in >> 5] >> (t_in & 31)) & 1u) != 0;
               *reinterpret_cast<uint4*>(dst) = zero ? make_uint4(0u, 0u, 0u, 0u) : row;
             }
           }
           __syncwarp();
         }
       }
+      };
+      if (!CHAIN) drain(std::integral_constant<bool, GATE_UP>{});
+      else if (gu) drain(std::true_type{});
+      else drain(std::false_type{});
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&tempty[acc]);
         mbar_arrive(&tile_empty[slot]);
+      }
+      if (CHAIN && gu) {
+        // Publish this warp's h rows of the tile to the down tiles (other
+        // CTAs' TMA reads): each lane's stores, then one release per warp.
+        // After the accumulator is released, so that waiting for the stores
+        // to drain overlaps the next tile's MMAs.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) counter_release_add(args.ready + tc.e);
       }
     }
   } else if (GATHER) {
@@ -708,7 +811,25 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
     err = cudaMemsetAsync(args.sched, 0, sizeof(uint32_t), stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_dependent(kern, dim3(grid), dim3(num_threads<LOAD>()), SMEM_BYTES, stream, a0, a1, b128, b16, args);
+  return launch_dependent(kern, dim3(grid), dim3(num_threads<LOAD>()), SMEM_BYTES, stream, a0, a1, b128, b16, a0,
+                          b128, b16, args);
+}
+
+// K3 and K4 in one launch (CHAIN): gate/up tiles, then down tiles that wait
+// for their expert's h rows. args carries both stages' sizes, y in out2 and
+// the per-expert ready counters (zero at launch, like the tile counter).
+template <typename T, int TBM, int LOAD>
+cudaError_t launch_chain(const TcWeights& w, const CUtensorMap& x128, const CUtensorMap& x16,
+                         const CUtensorMap& h128, const CUtensorMap& h16, const TcArgs& args, int num_sms,
+                         cudaStream_t stream) {
+  auto kern = experts_tc_kernel<T, true, TBM, LOAD, true>;
+  constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES_CHAIN;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  const int grid = static_cast<int>(args.tile_cap < static_cast<uint32_t>(num_sms) ? args.tile_cap : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  return launch_dependent(kern, dim3(grid), dim3(num_threads<LOAD>()), SMEM_BYTES, stream, w.gate, w.up, x128, x16,
+                          w.down, h128, h16, args);
 }
 
 template <typename T>
@@ -776,7 +897,62 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   return launch_one<T, false, 256>(w.down, w.down, t128, t16, args, num_sms, stream, sz);
 }
 
+template <typename T>
+cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
+                        const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h, void* y,
+                        uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream, const char** why) {
+  uint32_t* status = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
+  if (err != cudaSuccess) return err;
+  const bool small = rows <= 8 * static_cast<int64_t>(E);
+  if (gather != nullptr && !small) {
+    *why = "the chained experts gather x rows only for decode-sized batches";
+    return cudaErrorInvalidValue;
+  }
+  CUtensorMap x128 = w.gate, x16 = w.gate, h128 = w.gate, h16 = w.gate;
+  const bool maps_ok =
+      (gather == nullptr
+           ? encode_2d(&x128, dtype, xd, static_cast<uint64_t>(H), static_cast<uint64_t>(rows), 128) &&
+                 encode_2d(&x16, dtype, xd, static_cast<uint64_t>(H), static_cast<uint64_t>(rows), 16)
+           : encode_2d(&x128, dtype, gather->x, static_cast<uint64_t>(H), static_cast<uint64_t>(gather->x_rows), 1)) &&
+      encode_2d(&h128, dtype, h, static_cast<uint64_t>(I), static_cast<uint64_t>(rows), 128) &&
+      encode_2d(&h16, dtype, h, static_cast<uint64_t>(I), static_cast<uint64_t>(rows), 16);
+  if (!maps_ok) {
+    *why = "cuTensorMapEncodeTiled rejected a token tensor map";
+    return cudaErrorInvalidValue;
+  }
+  const int nw3 = static_cast<int>((I + BM - 1) / BM);
+  const int nw4 = static_cast<int>((H + 2 * BM - 1) / (2 * BM));
+  const int tbm = small ? 32 : 256;
+  const int64_t cap = tile_bound(rows, E, nw3, tbm) + tile_bound(rows, E, nw4, tbm);
+  TcArgs args{offsets, h, sched, E, nw3, static_cast<int>((H + BK - 1) / BK), static_cast<int>(I),
+              static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status,
+              nullptr, nullptr, 1, 0, static_cast<int>(H * 2), nullptr, nullptr,
+              y, nw4, static_cast<int>((I + BK - 1) / BK), static_cast<int>(H), ready};
+  if (gather != nullptr) {
+    args.gx = static_cast<const uint8_t*>(gather->x);
+    args.row_src = gather->row_src;
+    args.top_k = gather->top_k;
+    args.x_rows = static_cast<uint32_t>(gather->x_rows);
+    return launch_chain<T, 32, TOK_GATHER4>(w, x128, x16, h128, h16, args, num_sms, stream);
+  }
+  if (small) return launch_chain<T, 32, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream);
+  return launch_chain<T, 256, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream);
+}
+
 }  // namespace
+
+cudaError_t launch_experts_tc_chain(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
+                                    const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h,
+                                    void* y, uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream,
+                                    const char** why) {
+  if (rows == 0) return cudaSuccess;
+  if (dtype == MOE_BF16)
+    return chain_stage<__nv_bfloat16>(w, dtype, xd, gather, offsets, E, rows, H, I, h, y, sched, ready, num_sms,
+                                      stream, why);
+  return chain_stage<__half>(w, dtype, xd, gather, offsets, E, rows, H, I, h, y, sched, ready, num_sms, stream,
+                             why);
+}
 
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,
                        int64_t E, int64_t H, int64_t I, TcWeights* out, const char** why) {

@@ -223,6 +223,44 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits (bounded, like mbar_wait_bounded) until the device counter *ctr,
+// read with acquire semantics at GPU scope, reaches `need`; then orders the
+// data that the counter's writers stored (generic proxy) before this
+// thread's later TMA reads of it (async proxy).
+__device__ __forceinline__ bool counter_wait_bounded(const uint32_t* ctr, uint32_t need, volatile int* abort_flag,
+                                                     uint32_t* status, uint32_t code, uint64_t limit_ns) {
+  auto ready = [&]() {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v >= need;
+  };
+  bool ok = ready();
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; !ok; ++it) {
+      __nanosleep(64);
+      ok = ready();
+      if (!ok && (it & 15u) == 0) {
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+          if (abort_flag != nullptr) *abort_flag = 1;
+          record_status(status, code);
+          return false;
+        }
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// Raises the device counter *ctr by one with release semantics at GPU scope
+// (the calling thread's earlier stores, and those it observed, become
+// visible to an acquiring reader first).
+__device__ __forceinline__ void counter_release_add(uint32_t* ctr) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA (bulk tensor copies)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {

@@ -265,6 +265,39 @@ def test_experts_backward_full_size_sampled_experts(cuda_lib):
     assert moe.moe_device_status() == 0
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_experts_backward_expert_row_counts_around_the_k_steps(cuda_lib, dtype):
+    """The weight-gradient GEMMs take K over an expert's rows in blocks of 64,
+    16 rows per MMA: counts on both sides of 16 and 64 (and 0, 1, 130) check
+    that the MMAs past an expert's end are skipped and the rows of the next
+    expert inside the last one are zeroed (each expert's rows here are the
+    next expert's garbage). Ragged H and I clip the tiles too."""
+    moe = cuda_lib
+    counts = [0, 1, 15, 16, 17, 63, 64, 65, 127, 130, 3]
+    E, H, I = len(counts), 136, 200
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(41)
+    gate = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dtype)
+    up = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dtype)
+    down = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(dtype)
+    xd = torch.randn(rows, H, generator=g).to(dtype)
+    dy = (torch.randn(rows, H, generator=g) * 0.5).to(dtype)
+    ex = moe.Experts(gate.to(DEV), up.to(DEV), down.to(DEV))
+    offs = torch.from_numpy(offsets).to(torch.int32).to(DEV)
+    y, cache = moe.moe_experts_forward_training(ex, xd.to(DEV), offs)
+    gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.experts_backward(xd, gate, up, down, offsets, dy,
+                                  cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
+    _grad_close(f64(gr.dx_dispatched), ref.dx_dispatched, ref.dx_abs, dtype, "dx_dispatched")
+    _grad_close(f64(gr.dgate), ref.dgate, ref.dgate_abs, dtype, "dgate")
+    _grad_close(f64(gr.dup), ref.dup, ref.dup_abs, dtype, "dup")
+    _grad_close(f64(gr.ddown), ref.ddown, ref.ddown_abs, dtype, "ddown")
+    assert (gr.dgate[0] == 0).all() and (gr.ddown[0] == 0).all()  # the expert without rows
+    assert moe.moe_device_status() == 0
+
+
 def test_combine_backward_ignores_row_src_past_the_dispatched_rows(cuda_lib):
     """row_src entries past the dispatched rows (here: a token with an invalid
     index, so one row fewer than slots) may hold anything, even a valid slot:

@@ -391,9 +391,10 @@ def traffic_record(kernel_source: Path):
 
 
 def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
-    """Mean seconds of the gate/up and down GEMM stages on one workload
-    (routing and dispatch done once beforehand; L2 flushed before each
-    timed stage)."""
+    """Mean seconds of the gate/up and down GEMM stages on one workload, each
+    launched on its own, and of the chained launch of both (the one
+    moe_forward runs; moe_experts_forward_dispatched). Routing and dispatch
+    done once beforehand; L2 flushed before each timed call."""
     inp = workloads.generate(cfg)
     d = {k: v.to(dev) for k, v in inp.items()}
     del inp
@@ -403,24 +404,31 @@ def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
     h = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
     y = moe.moe_experts_down(ex, h, disp.offsets)
     ws = torch.empty(moe.STAGE_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
-    times = {"gate_up": [], "down": []}
+    rows = disp.x_dispatched.shape[0]
+    cws = torch.empty(moe.load_library().moe_experts_forward_dispatched_workspace_size(ex.handle, rows),
+                      dtype=torch.uint8, device=dev)
+    y2 = torch.empty_like(y)
+    times = {"gate_up": [], "down": [], "chain": []}
     for i in range(steps + 2):
-        for name in ("gate_up", "down"):
+        for name in ("gate_up", "down", "chain"):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             if name == "gate_up":
                 moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h, workspace=ws)
-            else:
+            elif name == "down":
                 moe.moe_experts_down(ex, h, disp.offsets, out=y, workspace=ws)
+            else:
+                moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets, out=y2, workspace=cws)
             b.record(stream)
             b.synchronize()
             if i >= 2:
                 times[name].append(a.elapsed_time(b) / 1e3)
     assert moe.moe_device_status() == 0
-    del ex, d, h, y, disp
+    assert torch.equal(y.view(torch.uint8), y2.view(torch.uint8)), "chained and split expert GEMMs differ"
+    del ex, d, h, y, y2, disp, cws
     torch.cuda.empty_cache()
-    return float(np.mean(times["gate_up"])), float(np.mean(times["down"]))
+    return float(np.mean(times["gate_up"])), float(np.mean(times["down"])), float(np.mean(times["chain"]))
 
 
 def training_step_times(moe, cfg, dev, stream, flush, steps):
@@ -557,15 +565,17 @@ def run_ours(args, rank, world, local_rank):
                 "router_backward_us": round(tr[4] * 1e6, 1),
                 "experts_backward_tflops": round(bwd_flops / tr[2] / 1e12, 1),
                 "experts_backward_frac_bf16_peak": round(bwd_flops / tr[2] / 1e12 / peaks["bf16_tflops"], 4)}
+    # The chained gate/up + down launch on the prefill workload, on its own.
+    _, _, t_chain = gemm_stage_times(moe, PREFILL, dev, stream, flush, 20)
     other_gemms = {}
     for cid in (3, 5):
         oc = workloads.CONFIGS[cid]
-        t_g, t_d = gemm_stage_times(moe, oc, dev, stream, flush, 5)
-        tf = oc.expert_flops / (t_g + t_d) / 1e12
+        t_g, t_d, t_c = gemm_stage_times(moe, oc, dev, stream, flush, 5)
+        tf = oc.expert_flops / t_c / 1e12
         peak = peaks["bf16_tflops"]  # F16 and BF16 share the dense tensor rate
         other_gemms[oc.name] = {"tflops": round(tf, 1), "frac_peak": round(tf / peak, 4),
-                                "gate_up_us": round(t_g * 1e6, 1), "down_us": round(t_d * 1e6, 1),
-                                "flops": oc.expert_flops}
+                                "chained_us": round(t_c * 1e6, 1), "gate_up_us": round(t_g * 1e6, 1),
+                                "down_us": round(t_d * 1e6, 1), "flops": oc.expert_flops}
     clk = clocks.stop()
     assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
 
@@ -575,26 +585,32 @@ def run_ours(args, rank, world, local_rank):
     t_route, t_disp, t_gu, t_down, t_comb = [float(x) for x in stages]
     es = 2
     gemm_flops = c.expert_flops
-    gemm_tflops = gemm_flops / (t_gu + t_down) / 1e12
+    gemm_tflops = gemm_flops / t_chain / 1e12
     touched = chain.touched_experts()
-    # K3 (gate/up GEMM): algorithmic work per launch
-    k3_flops = 4 * c.T * c.top_k * c.H * c.I
+    # Dominant kernel: the chained gate/up + down launch (K3 + K4). Its
+    # algorithmic work per launch: the touched gate, up and down weights, x
+    # rows read through x_dispatched, h written and read back, y written.
+    k_flops = gemm_flops
     k3_bytes = touched * 2 * c.I * c.H * es + c.T * c.H * es + c.T * c.top_k * c.I * es
-    k3_tflops = k3_flops / t_gu / 1e12
-    k3_gbs = k3_bytes / t_gu / 1e9
-    t_floor_tensor = k3_flops / (peaks["bf16_tflops"] * 1e12)
-    t_floor_hbm = k3_bytes / (peaks["hbm_gbs"] * 1e9)
+    k4_bytes = touched * c.H * c.I * es + c.T * c.top_k * c.I * es + c.T * c.top_k * c.H * es
+    k_bytes = k3_bytes + k4_bytes
+    k_tflops = k_flops / t_chain / 1e12
+    k_gbs = k_bytes / t_chain / 1e9
+    t_floor_tensor = k_flops / (peaks["bf16_tflops"] * 1e12)
+    t_floor_hbm = k_bytes / (peaks["hbm_gbs"] * 1e9)
     bound = "hbm" if t_floor_hbm >= t_floor_tensor else "tensor"
     traffic = traffic_record(ROOT / "moe_routing_swiglu_gb300" / "csrc" / "experts_tc.cu")
-    roof = {"kernel": "experts_tc_kernel<bf16, gate/up + SwiGLU> (K3)", "bound": bound,
-            "achieved": round(k3_gbs if bound == "hbm" else k3_tflops, 2),
+    roof = {"kernel": "experts_tc_kernel<bf16, chained gate/up + SwiGLU and down> (K3 + K4)", "bound": bound,
+            "achieved": round(k_gbs if bound == "hbm" else k_tflops, 2),
             "peak": peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"],
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-            "frac": round((k3_gbs / peaks["hbm_gbs"]) if bound == "hbm" else (k3_tflops / peaks["bf16_tflops"]), 4),
+            "frac": round((k_gbs / peaks["hbm_gbs"]) if bound == "hbm" else (k_tflops / peaks["bf16_tflops"]), 4),
             "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-            "algorithmic_bytes": k3_bytes, "algorithmic_flops": k3_flops, "us": round(t_gu * 1e6, 2),
-            "tensor_frac": round(k3_tflops / peaks["bf16_tflops"], 4),
-            "hbm_frac": round(k3_gbs / peaks["hbm_gbs"], 4), "peak_source": peaks_src}
+            "algorithmic_bytes": k_bytes, "algorithmic_flops": k_flops, "us": round(t_chain * 1e6, 2),
+            "tensor_frac": round(k_tflops / peaks["bf16_tflops"], 4),
+            "hbm_frac": round(k_gbs / peaks["hbm_gbs"], 4), "peak_source": peaks_src,
+            "timing": "mean of 20 launches of moe_experts_forward_dispatched (the chained kernel alone), "
+                      "CUDA events, L2 flushed before each"}
 
     d = DECODE
     dec_touched = decode.touched_experts()
@@ -609,8 +625,8 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(c, world),
         "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
                          "frac_bf16_sustained": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
-                         "flops_per_step": gemm_flops, "gate_up_us": round(t_gu * 1e6, 2),
-                         "down_us": round(t_down * 1e6, 2)},
+                         "flops_per_step": gemm_flops, "chained_us": round(t_chain * 1e6, 2),
+                         "split_gate_up_us": round(t_gu * 1e6, 2), "split_down_us": round(t_down * 1e6, 2)},
         "route_dispatch_us": {"route": round(t_route * 1e6, 2), "dispatch": round(t_disp * 1e6, 2),
                               "total": round((t_route + t_disp) * 1e6, 2)},
         "combine_us": round(t_comb * 1e6, 2),
@@ -619,7 +635,8 @@ def run_ours(args, rank, world, local_rank):
                    "stages": f"{stage_steps} steps launched directly with events between the stages "
                              f"({stage_total / stage_steps * 1e6:.1f} us per step including the events)"},
         "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
-                   "timing": "CUDA-graph replays of the decode step (forward); experts_us from the staged run",
+                   "timing": "CUDA-graph replays of the decode step (forward, gate/up and down chained in one "
+                             "launch); experts_us from the staged run (the two GEMMs launched apart)",
                    "frac_hbm_forward": round(dec_bytes / dec_fwd / 1e9 / peaks["hbm_gbs"], 4),
                    "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dec_touched,
                    "touched_weight_bytes": dec_bytes,

@@ -185,8 +185,15 @@ void moe_experts_destroy(moe_experts* experts);
  *                 projection.
  *   workspace     device scratch of
  *                 moe_experts_forward_dispatched_workspace_size(experts, rows)
- *                 bytes (holds h and the GEMMs' tile counter), 256-byte
- *                 aligned.
+ *                 bytes (holds h, the GEMMs' tile counter and one counter per
+ *                 expert), 256-byte aligned.
+ *
+ * F16/BF16 run both GEMMs as one launch (after a reset of the counters):
+ * tiles of the gate/up GEMM first, then tiles of the down GEMM, each of
+ * which waits (bounded, about a second; on timeout the device status word
+ * records 0x19) until every gate/up tile of its expert has stored its h
+ * rows. The results are bit-identical to moe_experts_gate_up followed by
+ * moe_experts_down.
  */
 size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* experts, int64_t rows);
 moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void* x_dispatched,
@@ -493,7 +500,9 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
  * wins): 0x11 producer waiting for a free stage, 0x12 MMA waiting for a
  * loaded stage, 0x13 MMA waiting for a drained accumulator, 0x14 epilogue
  * waiting for a finished accumulator, 0x15 / 0x16 teardown drains, 0x17 a
- * wait on the shared-memory tile ring of the tile scheduler, 0x100
+ * wait on the shared-memory tile ring of the tile scheduler, 0x18 a gather
+ * loader waiting for a free stage, 0x19 a down tile of the chained gate/up +
+ * down launch waiting for its expert's h rows, 0x100
  * moe_selftest_bounded_wait. Synchronises the current device; *code = 0 when
  * no wait has timed out.
  */

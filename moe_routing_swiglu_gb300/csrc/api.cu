@@ -415,10 +415,12 @@ moe_status moe_experts_create(const void* gate, const void* up, const void* down
 
 void moe_experts_destroy(moe_experts* experts) { delete experts; }
 
+// h, then the tile counter (and, from word 64, one ready counter per expert
+// for the chained gate/up + down launch).
 size_t moe_experts_forward_dispatched_workspace_size(const moe_experts* ex, int64_t rows) {
   if (ex == nullptr || rows < 0) return 0;
   return align_up(static_cast<size_t>(rows) * static_cast<size_t>(ex->I) * dtype_size(ex->dtype) + 1, 256) +
-         moe::TC_SCHED_BYTES;
+         moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4;
 }
 
 moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_dispatched,
@@ -438,10 +440,23 @@ moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_d
   moe_status st = check_current_device(ex);
   if (st != MOE_OK) return st;
   if (rows == 0) return ok();
-  const size_t h_bytes = need - moe::TC_SCHED_BYTES;
-  st = run_experts(ex, x_dispatched, offsets, rows, workspace, y_dispatched,
-                   static_cast<uint8_t*>(workspace) + h_bytes, static_cast<cudaStream_t>(stream));
-  if (st != MOE_OK) return st;
+  const size_t cnt_bytes = moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4;
+  uint8_t* counters = static_cast<uint8_t*>(workspace) + (need - cnt_bytes);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ex->dtype == MOE_F32) {
+    st = run_experts(ex, x_dispatched, offsets, rows, workspace, y_dispatched, counters, s);
+    if (st != MOE_OK) return st;
+    return ok();
+  }
+  // F16/BF16: one chained launch (as in moe_forward); its counters start at 0.
+  cudaError_t err = cudaMemsetAsync(counters, 0, cnt_bytes, s);
+  if (err != cudaSuccess) return cuda_fail(err, "counter reset");
+  const char* why = nullptr;
+  uint32_t* sched = reinterpret_cast<uint32_t*>(counters);
+  err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, x_dispatched, nullptr, offsets, static_cast<int>(ex->E), rows,
+                                     ex->H, ex->I, workspace, y_dispatched, sched, sched + moe::TC_SCHED_BYTES / 4,
+                                     ex->num_sms, s, &why);
+  if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
   return ok();
 }
 

@@ -6,7 +6,8 @@ The inputs are the seeded synthetic workloads of ``workloads.py``; routing and
 dispatch run once to set up the stage's inputs, then the chosen stage runs
 ``--reps`` times back to back (stream-ordered) and the device is synchronised.
 Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
-row_src), down, combine, forward (moe_forward), and
+row_src), down, experts (gate/up and down chained in one launch, as
+moe_forward runs them), combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
 variant in ``workloads.GROUPED``), backward (the experts' backward of
 first-order training on a random output gradient) and combine_backward (the
@@ -35,7 +36,7 @@ def main(argv=None):
     names.update(workloads.SMALL_CONFIGS)
     ap.add_argument("--workload", default="cfg2", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "combine", "forward",
+                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "experts", "combine", "forward",
                              "route_grouped", "backward", "combine_backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
@@ -77,6 +78,8 @@ def main(argv=None):
             moe.moe_experts_gate_up_gather(ex, d["x"], disp.row_src, cfg.top_k, disp.offsets, out=h)
         elif args.stage == "down":
             moe.moe_experts_down(ex, h, disp.offsets, out=y)
+        elif args.stage == "experts":  # gate/up and down chained in one launch
+            moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets, out=y)
         elif args.stage == "route_grouped":
             moe.moe_route_sigmoid_grouped(d["logits"], bias, opts, indices=idx, weights=w)
         elif args.stage == "backward":

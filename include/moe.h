@@ -433,9 +433,13 @@ moe_status moe_router_backward(const void* logits, moe_dtype dtype, int64_t T, i
  *   y_dispatched  device [rows, H] out.
  *   cache_g, cache_u  device [rows, I] out: the pre-activations g = W_gate x
  *                 and u = W_up x, rounded to the dtype.
- *   workspace     at least 256 bytes, 256-byte aligned.
- * y_dispatched and h are bit-identical to moe_experts_forward_dispatched's.
+ *   workspace     device scratch of
+ *                 moe_experts_forward_training_workspace_size(experts) bytes
+ *                 (the GEMMs' counters), 256-byte aligned.
+ * y_dispatched and h are bit-identical to moe_experts_forward_dispatched's
+ * (F16/BF16: the same chained launch, whose gate/up tiles also store g, u).
  */
+size_t moe_experts_forward_training_workspace_size(const moe_experts* experts);
 moe_status moe_experts_forward_training(const moe_experts* experts, const void* x_dispatched,
                                         const uint32_t* offsets, int64_t rows, void* h, void* y_dispatched,
                                         void* cache_g, void* cache_u, void* workspace, size_t workspace_bytes,

@@ -87,6 +87,7 @@ SIGNATURES = {
     "moe_router_weights": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P]),
     "moe_router_backward": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P,
                                            _P]),
+    "moe_experts_forward_training_workspace_size": (_SZ, [_P]),
     "moe_experts_forward_training": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P, _I64, _I32, _I64, _P,
                                             _P, _P]),
@@ -488,7 +489,7 @@ def moe_experts_forward_training(experts: Experts, x_dispatched: torch.Tensor, o
     dev = x_dispatched.device
     y = torch.empty(rows, experts.H, dtype=experts.dtype, device=dev)
     h, g, u = (torch.empty(rows, experts.I, dtype=experts.dtype, device=dev) for _ in range(3))
-    ws = _workspace(STAGE_WORKSPACE_BYTES, dev, workspace)
+    ws = _workspace(lib.moe_experts_forward_training_workspace_size(experts.handle), dev, workspace)
     _check(lib.moe_experts_forward_training(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows, _ptr(h),
                                             _ptr(y), _ptr(g), _ptr(u), _ptr(ws), ws.numel(), _stream(stream)))
     return y, TrainingCache(x_dispatched, offsets, h, g, u)

@@ -235,7 +235,7 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
     if (st != MOE_OK) return st;
   } else {
     const char* why = nullptr;
-    err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, xd, gather_rows ? &gather : nullptr, offsets,
+    err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, xd, gather_rows ? &gather : nullptr, nullptr, offsets,
                                        static_cast<int>(ex->E), rows, ex->H, ex->I, h, yd, sched, ready, ex->num_sms,
                                        s, &why);
     if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
@@ -453,7 +453,7 @@ moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_d
   if (err != cudaSuccess) return cuda_fail(err, "counter reset");
   const char* why = nullptr;
   uint32_t* sched = reinterpret_cast<uint32_t*>(counters);
-  err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, x_dispatched, nullptr, offsets, static_cast<int>(ex->E), rows,
+  err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, x_dispatched, nullptr, nullptr, offsets, static_cast<int>(ex->E), rows,
                                      ex->H, ex->I, workspace, y_dispatched, sched, sched + moe::TC_SCHED_BYTES / 4,
                                      ex->num_sms, s, &why);
   if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
@@ -698,11 +698,18 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
   return ok();
 }
 
+size_t moe_experts_forward_training_workspace_size(const moe_experts* ex) {
+  if (ex == nullptr) return 0;
+  return moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4;
+}
+
 moe_status moe_experts_forward_training(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets,
                                         int64_t rows, void* h, void* y_dispatched, void* cache_g, void* cache_u,
                                         void* workspace, size_t workspace_bytes, void* stream) {
   moe_status st = check_stage_args(ex, x_dispatched, offsets, rows, y_dispatched, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
+  if (workspace_bytes < moe_experts_forward_training_workspace_size(ex))
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_experts_forward_training_workspace_size()");
   if (rows > 0 && (h == nullptr || cache_g == nullptr || cache_u == nullptr))
     return fail(MOE_ERR_NULL, "h, cache_g and cache_u must be non-NULL");
   if (ex->dtype != MOE_F32 && (!aligned16(h) || !aligned16(cache_g) || !aligned16(cache_u)))
@@ -710,10 +717,23 @@ moe_status moe_experts_forward_training(const moe_experts* ex, const void* x_dis
   if (rows == 0) return ok();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const moe::TcCache cache{cache_g, cache_u};
-  st = run_stage(ex, true, x_dispatched, nullptr, offsets, rows, h, workspace, s, &cache);
-  if (st != MOE_OK) return st;
-  st = run_stage(ex, false, h, nullptr, offsets, rows, y_dispatched, workspace, s);
-  return st != MOE_OK ? st : ok();
+  if (ex->dtype == MOE_F32) {
+    st = run_stage(ex, true, x_dispatched, nullptr, offsets, rows, h, workspace, s, &cache);
+    if (st != MOE_OK) return st;
+    st = run_stage(ex, false, h, nullptr, offsets, rows, y_dispatched, workspace, s);
+    return st != MOE_OK ? st : ok();
+  }
+  // F16/BF16: the chained launch, its counters reset first.
+  const size_t cnt_bytes = moe_experts_forward_training_workspace_size(ex);
+  cudaError_t err = cudaMemsetAsync(workspace, 0, cnt_bytes, s);
+  if (err != cudaSuccess) return cuda_fail(err, "counter reset");
+  const char* why = nullptr;
+  uint32_t* sched = static_cast<uint32_t*>(workspace);
+  err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, x_dispatched, nullptr, &cache, offsets, static_cast<int>(ex->E),
+                                     rows, ex->H, ex->I, h, y_dispatched, sched, sched + moe::TC_SCHED_BYTES / 4,
+                                     ex->num_sms, s, &why);
+  if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
+  return ok();
 }
 
 size_t moe_experts_backward_workspace_size(const moe_experts* ex, int64_t rows) {

@@ -899,7 +899,7 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
 
 template <typename T>
 cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
-                        const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h, void* y,
+                        const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h, void* y,
                         uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream, const char** why) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
@@ -929,6 +929,10 @@ cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, con
               static_cast<uint32_t>(rows), static_cast<uint32_t>(cap), status,
               nullptr, nullptr, 1, 0, static_cast<int>(H * 2), nullptr, nullptr,
               y, nw4, static_cast<int>((I + BK - 1) / BK), static_cast<int>(H), ready};
+  if (cache != nullptr) {
+    args.out_g = cache->g;
+    args.out_u = cache->u;
+  }
   if (gather != nullptr) {
     args.gx = static_cast<const uint8_t*>(gather->x);
     args.row_src = gather->row_src;
@@ -943,15 +947,15 @@ cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, con
 }  // namespace
 
 cudaError_t launch_experts_tc_chain(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
-                                    const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h,
-                                    void* y, uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream,
-                                    const char** why) {
+                                    const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H,
+                                    int64_t I, void* h, void* y, uint32_t* sched, uint32_t* ready, int num_sms,
+                                    cudaStream_t stream, const char** why) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
-    return chain_stage<__nv_bfloat16>(w, dtype, xd, gather, offsets, E, rows, H, I, h, y, sched, ready, num_sms,
-                                      stream, why);
-  return chain_stage<__half>(w, dtype, xd, gather, offsets, E, rows, H, I, h, y, sched, ready, num_sms, stream,
-                             why);
+    return chain_stage<__nv_bfloat16>(w, dtype, xd, gather, cache, offsets, E, rows, H, I, h, y, sched, ready,
+                                      num_sms, stream, why);
+  return chain_stage<__half>(w, dtype, xd, gather, cache, offsets, E, rows, H, I, h, y, sched, ready, num_sms,
+                             stream, why);
 }
 
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,

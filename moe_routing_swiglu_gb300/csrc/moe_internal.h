@@ -114,10 +114,11 @@ cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up,
 // gathered through row_src for decode-sized batches -> h), then down tiles
 // (h -> y), each waiting for its expert's h rows. sched[0] and ready[0..E)
 // must be zero on the stream before the launch (the dispatch zeroes them).
+// cache (optional): the gate/up tiles also store the pre-activations g, u.
 cudaError_t launch_experts_tc_chain(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
-                                    const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h,
-                                    void* y, uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream,
-                                    const char** why);
+                                    const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H,
+                                    int64_t I, void* h, void* y, uint32_t* sched, uint32_t* ready, int num_sms,
+                                    cudaStream_t stream, const char** why);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 // Device address of the status word the bounded waits report into.
 cudaError_t device_status_ptr(uint32_t** p);

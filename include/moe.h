@@ -274,9 +274,11 @@ moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t
  *
  * Same numerics as calling moe_route, moe_dispatch,
  * moe_experts_forward_dispatched and moe_combine in turn: the outputs are
- * bit-identical to that sequence. For decode-sized batches (T * top_k <=
- * 8 * E) it dispatches the maps only and runs the gate/up stage as
- * moe_experts_gate_up_gather, so x_dispatched is never written.
+ * bit-identical to that sequence. F16/BF16 run the two expert GEMMs as one
+ * launch (as moe_experts_forward_dispatched does; the dispatch zeroes its
+ * counters). For decode-sized batches (T * top_k <= 8 * E) it dispatches
+ * the maps only and the gate/up tiles gather x rows through row_src (as
+ * moe_experts_gate_up_gather), so x_dispatched is never written.
  */
 size_t moe_forward_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k);
 moe_status moe_forward(const moe_experts* experts, const void* x, const void* logits,

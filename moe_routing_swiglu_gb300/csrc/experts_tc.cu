@@ -52,6 +52,12 @@
 // CTAs that share a weight tile run together and read it from L2. The plan
 // comes from the device offsets (the host never learns per-expert counts).
 //
+// Chained mode (what moe_forward runs for F16/BF16): one launch takes K3's
+// tiles and then K4's from one counter; a K4 tile waits for its expert's h
+// rows through a per-expert counter that K3's epilogue warps raise (see the
+// kernel's comment). CTAs that run out of K3 tiles start K4 tiles instead of
+// idling through K3's last wave.
+//
 // Every mbarrier wait is bounded (about a second). A wait that runs out
 // records a code in the device status word, raises the CTA's abort flag so
 // the other roles stop, drains the copies and MMAs already issued, frees

@@ -319,3 +319,29 @@ def test_combine_backward_ignores_row_src_past_the_dispatched_rows(cuda_lib):
     assert torch.equal(e1[:5].view(torch.uint8), e2[:5].view(torch.uint8))
     assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
     assert torch.isnan(w1[1, 1]) and torch.isfinite(w1[0]).all()
+
+
+def test_training_forward_workspace_holds_the_counters(cuda_lib):
+    """The chained training forward keeps a tile counter and one ready counter
+    per expert in its workspace: the documented size is 256 + 4 E bytes, and
+    anything smaller is rejected before any launch."""
+    moe = cuda_lib
+    cfg = workloads.SMALL_CONFIGS["bf16_ragged"]
+    inp = workloads.generate(cfg)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    lib = moe.load_library()
+    need = lib.moe_experts_forward_training_workspace_size(ex.handle)
+    assert need == 256 + 4 * cfg.E
+    idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets,
+                                         workspace=torch.empty(need - 4, dtype=torch.uint8, device=DEV))
+    assert err.value.status == 6
+    y, _ = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets,
+                                            workspace=torch.empty(need, dtype=torch.uint8, device=DEV))
+    y_ref = moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.uint8), y_ref.view(torch.uint8))
+    assert moe.moe_device_status() == 0

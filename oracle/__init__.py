@@ -32,4 +32,5 @@ from .training import (  # noqa: F401
     router_jacobian,
     selected_router_backward,
     selected_router_weights,
+    training_forward_cache,
 )

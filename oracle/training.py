@@ -197,6 +197,28 @@ class ExpertGrads:
     ddown_abs: np.ndarray | None = None
 
 
+def training_forward_cache(x_dispatched, gate, up, offsets):
+    """The forward cache of the training forward (ruDNN user guide, section
+    12, forward_dispatched_training): per dispatched row r of expert e, the
+    pre-activations g = W_gate[e] x_r and u = W_up[e] x_r and the SwiGLU
+    output h = SiLU(g) * u, in f64 from the dtype-rounded inputs with no
+    intermediate rounding. Returns (g, u, h), each [rows, I]."""
+    x, Wg, Wu = widen(x_dispatched), widen(gate), widen(up)
+    E, I, _ = Wg.shape
+    off = np.asarray(offsets, dtype=np.int64)
+    g = np.zeros((x.shape[0], I))
+    u = np.zeros((x.shape[0], I))
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi <= lo:
+            continue
+        g[lo:hi] = x[lo:hi] @ Wg[e].T
+        u[lo:hi] = x[lo:hi] @ Wu[e].T
+    with np.errstate(over="ignore"):
+        h = _silu(g) * u
+    return g, u, h
+
+
 def experts_backward(x_dispatched, gate, up, down, offsets, dexpert, cache=None) -> ExpertGrads:
     """Backward of y_r = W_down[e] (SiLU(W_gate[e] x_r) * (W_up[e] x_r)) over the
     dispatched rows of each expert (f64 from the dtype-rounded inputs):
@@ -204,12 +226,12 @@ def experts_backward(x_dispatched, gate, up, down, offsets, dexpert, cache=None)
     dx = dg W_gate + du W_up, dW_gate = dg^T x, dW_up = du^T x.
 
     ``cache`` = (g, u, h) [rows, I] each: the forward cache the backward
-    consumes (cache.backward of the pages); without it g, u and h are
-    recomputed from x in f64."""
+    consumes (cache.backward of the pages); without it g, u and h come from
+    training_forward_cache, in f64 from x."""
     x = widen(x_dispatched)
-    cg = cu = ch = None
-    if cache is not None:
-        cg, cu, ch = (widen(c) if isinstance(c, torch.Tensor) else np.asarray(c, dtype=np.float64) for c in cache)
+    if cache is None:
+        cache = training_forward_cache(x, gate, up, offsets)
+    cg, cu, ch = (widen(c) if isinstance(c, torch.Tensor) else np.asarray(c, dtype=np.float64) for c in cache)
     dy = widen(dexpert) if isinstance(dexpert, torch.Tensor) else np.asarray(dexpert, dtype=np.float64)
     Wg, Wu, Wd = widen(gate), widen(up), widen(down)
     E, I, H = Wg.shape
@@ -224,12 +246,7 @@ def experts_backward(x_dispatched, gate, up, down, offsets, dexpert, cache=None)
         if hi <= lo:
             continue
         X, dY = x[lo:hi], dy[lo:hi]
-        if cache is None:
-            G = X @ Wg[e].T
-            U = X @ Wu[e].T
-            Hh = _silu(G) * U
-        else:
-            G, U, Hh = cg[lo:hi], cu[lo:hi], ch[lo:hi]
+        G, U, Hh = cg[lo:hi], cu[lo:hi], ch[lo:hi]
         dH = dY @ Wd[e]
         dWd[e] = dY.T @ Hh
         dG = dH * U * _silu_grad(G)

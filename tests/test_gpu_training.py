@@ -9,6 +9,7 @@ import torch
 import oracle
 import workloads
 from oracle import moe_oracle
+from tests.grad_bounds import ACC, UNIT, assert_within_bound, expert_error_bounds
 from tests.parity import assert_nan_positions_equal, f64, u32
 
 pytestmark = pytest.mark.gpu
@@ -78,22 +79,20 @@ def _small_training_case(name, seed=5):
     return cfg, inp, rt, dp, xd, dy
 
 
-# Gradient tolerance: each gradient entry is a sum, and its rounding error is
-# measured against the sum of |terms| (the oracle returns it): the F32 path
-# computes every step in FP32 (2e-5 covers FP32 sums of up to a few thousand
-# terms); the 16-bit paths round g, u, h, dg and du to the dtype once each on
-# the way, a few 2^-9 relative, so 2e-2 as in the forward outputs' bar.
-GRAD_TOL = {torch.float32: 2e-5, torch.float16: 2e-2, torch.bfloat16: 2e-2}
-
-
-def _grad_close(got, ref, abs_terms, dtype, what):
-    assert_nan_positions_equal(got, ref, what)
-    fin = np.isfinite(ref)
-    err = np.abs(got[fin] - ref[fin])
-    bound = GRAD_TOL[dtype] * abs_terms[fin] + 1e-30
-    worst = np.argmax(err / bound) if err.size else 0
-    assert (err <= bound).all(), (f"{what}: error {err.flat[worst]:.3e} against sum |terms| "
-                                  f"{abs_terms[fin].flat[worst]:.3e}")
+def check_experts_training(cache, gr, xd, gate, up, down, offsets, dy, dtype, what=""):
+    """The training forward's cache (g, u, h) and the experts' backward
+    against the oracle, which recomputes the cache itself in f64 from x (it
+    never sees the GPU's cache), each entry within its rounding bound
+    (tests/grad_bounds.py). Only the dispatched rows [0, offsets[E]) count."""
+    n = int(offsets[-1])
+    bounds = expert_error_bounds(xd, gate, up, down, offsets, dy, dtype)
+    g_ref, u_ref, h_ref = oracle.training_forward_cache(xd, gate, up, offsets)
+    for name, got, ref in (("g", cache.g, g_ref), ("u", cache.u, u_ref), ("h", cache.h, h_ref)):
+        assert_within_bound(f64(got)[:n], ref[:n], bounds[name][:n], f"{what}cache {name}")
+    ref = oracle.experts_backward(xd, gate, up, down, offsets, dy)
+    assert_within_bound(f64(gr.dx_dispatched)[:n], ref.dx_dispatched[:n], bounds["dx"][:n], f"{what}dx_dispatched")
+    for name in ("dgate", "dup", "ddown"):
+        assert_within_bound(f64(getattr(gr, name)), getattr(ref, name), bounds[name], f"{what}{name}")
 
 
 @pytest.mark.parametrize("name", ["f32_ragged", "bf16_ragged", "bf16_fine", "f16_zipf", "bf16_decode"])
@@ -108,25 +107,38 @@ def test_experts_training_forward_and_backward_parity(cuda_lib, name):
     y_ref = moe.moe_experts_forward_dispatched(ex, xdd, offs)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.uint8), y_ref.view(torch.uint8))
-    # The cached pre-activation g is the oracle's W_gate x (one rounding).
-    gref = np.zeros((xd.shape[0], cfg.I))
-    gabs = np.zeros((xd.shape[0], cfg.I))
-    for e in range(cfg.E):
-        lo, hi = int(dp.offsets[e]), int(dp.offsets[e + 1])
-        gref[lo:hi] = f64(xd[lo:hi]) @ f64(inp["gate"][e]).T
-        gabs[lo:hi] = np.abs(f64(xd[lo:hi])) @ np.abs(f64(inp["gate"][e])).T
-    _grad_close(f64(cache.g), gref, gabs, cfg.torch_dtype, "cache g")
-
     gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
     torch.cuda.synchronize()
-    # cache.backward consumes the cache the forward produced (checked above).
-    ref = oracle.experts_backward(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy,
-                                  cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
-    n = int(dp.offsets[-1])
-    _grad_close(f64(gr.dx_dispatched)[:n], ref.dx_dispatched[:n], ref.dx_abs[:n], cfg.torch_dtype, "dx_dispatched")
-    _grad_close(f64(gr.dgate), ref.dgate, ref.dgate_abs, cfg.torch_dtype, "dgate")
-    _grad_close(f64(gr.dup), ref.dup, ref.dup_abs, cfg.torch_dtype, "dup")
-    _grad_close(f64(gr.ddown), ref.ddown, ref.ddown_abs, cfg.torch_dtype, "ddown")
+    check_experts_training(cache, gr, xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy, cfg.torch_dtype)
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("which", ["u_is_g", "h_is_u"])
+def test_planted_wrong_cache_entry_is_caught(cuda_lib, which):
+    """A cache whose u holds the gate pre-activation (or whose h holds u),
+    planted by overwriting the cached tensor from the host before the
+    backward, fails the parity check of the cache and of the gradients the
+    backward computes from it: the oracle recomputes g, u and h from x."""
+    moe = cuda_lib
+    cfg, inp, rt, dp, xd, dy = _small_training_case("bf16_fine")
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    offs = torch.from_numpy(dp.offsets.astype(np.int64)).to(torch.int32).to(DEV)
+    _, cache = moe.moe_experts_forward_training(ex, xd.to(DEV).contiguous(), offs)
+    if which == "u_is_g":
+        cache.u.copy_(cache.g)
+    else:
+        cache.h.copy_(cache.u)
+    gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
+    torch.cuda.synchronize()
+    with pytest.raises(AssertionError, match="cache u" if which == "u_is_g" else "cache h"):
+        check_experts_training(cache, gr, xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy, cfg.torch_dtype)
+    # The gradients alone catch it too (the cache check is not what fails them).
+    ref = oracle.experts_backward(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy)
+    bounds = expert_error_bounds(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy, cfg.torch_dtype)
+    with pytest.raises(AssertionError):
+        for name in ("dgate", "dup", "ddown"):
+            assert_within_bound(f64(getattr(gr, name)), getattr(ref, name), bounds[name], name)
     assert moe.moe_device_status() == 0
 
 
@@ -189,7 +201,9 @@ def test_whole_training_step_matches_oracle(cuda_lib):
     route -> dispatch -> training forward; then combine backward -> experts
     backward -> dispatch backward, and the router gradient of the FP32
     dweights (softmax, renormalize); every stage checked against the oracle
-    on the inputs that stage received on the GPU."""
+    on the inputs that stage received on the GPU (the experts' cache
+    excepted: the oracle recomputes it from x), within rounding bounds
+    derived from the documented roundings."""
     moe = cuda_lib
     cfg = workloads.SMALL_CONFIGS["bf16_fine"]
     inp = workloads.generate(cfg)
@@ -211,25 +225,24 @@ def test_whole_training_step_matches_oracle(cuda_lib):
     dp = moe_oracle.dispatch(rt.indices, cfg.E)
     assert np.array_equal(u32(idx), rt.indices)
     assert np.array_equal(u32(disp.inv), dp.inv)
-    # Each stage against the oracle on the GPU's inputs to that stage.
     xd = inp["x"][torch.from_numpy(dp.row_src.astype(np.int64) // cfg.top_k)]
-    ref_dexp, ref_dw = oracle.combine_backward(y.cpu(), dp.inv, rt.weights, go, cfg.T, cfg.top_k)
-    ref_gr = oracle.experts_backward(xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dexp.cpu(),
-                                     cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
-    ref_dx = oracle.dispatch_backward(gr.dx_dispatched.cpu(), dp.inv, cfg.T, cfg.top_k)
+    assert torch.equal(disp.x_dispatched.cpu().view(torch.int16), xd.view(torch.int16))
+    T, k, H = cfg.T, cfg.top_k, cfg.H
+    # Combine backward on the forward's y; dweights is an FP32 dot over H.
+    ref_dexp, ref_dw = oracle.combine_backward(y.cpu(), dp.inv, rt.weights, go, T, k)
+    dw_abs = (np.abs(f64(go))[:, None, :] * np.abs(f64(y))[dp.inv.astype(np.int64).reshape(T, k)]).sum(-1)
+    assert_within_bound(dw, ref_dw, H * ACC * dw_abs + 2.0 ** -24 * np.abs(ref_dw), "dweights")
+    # The experts' cache and backward: the oracle recomputes g, u and h from x.
+    check_experts_training(cache, gr, xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dexp.cpu(),
+                           cfg.torch_dtype)
+    # Dispatch backward: k rows added in FP32, rounded once to the dtype.
+    ref_dx = oracle.dispatch_backward(gr.dx_dispatched.cpu(), dp.inv, T, k)
+    dx_abs = oracle.dispatch_backward(np.abs(f64(gr.dx_dispatched)), dp.inv, T, k)
+    assert_within_bound(dx, ref_dx, UNIT[cfg.torch_dtype] * np.abs(ref_dx) + k * ACC * dx_abs, "dx")
+    # Router gradient: FP32 evaluation (the router test's bound), rounded to the logits dtype.
     ref_dl, _ = oracle.selected_router_backward(inp["logits"], rt.indices, dw.cpu(), o)
-    dw_abs = (np.abs(f64(go))[:, None, :] * np.abs(f64(y))[dp.inv.astype(np.int64).reshape(cfg.T, cfg.top_k)]).sum(-1)
-    _grad_close(f64(dw), ref_dw, dw_abs, torch.float32, "dweights")
-    n = cfg.T * cfg.top_k
-    _grad_close(f64(gr.dx_dispatched)[:n], ref_gr.dx_dispatched[:n], ref_gr.dx_abs[:n], cfg.torch_dtype,
-                "dx_dispatched")
-    for name in ("dgate", "dup", "ddown"):
-        _grad_close(f64(getattr(gr, name)), getattr(ref_gr, name), getattr(ref_gr, name + "_abs"), cfg.torch_dtype,
-                    name)
-    dx_abs = oracle.dispatch_backward(np.abs(f64(gr.dx_dispatched)), dp.inv, cfg.T, cfg.top_k)
-    _grad_close(f64(dx), ref_dx, dx_abs, cfg.torch_dtype, "dx")
-    dl_abs = o.scale * np.abs(f64(dw)).sum(axis=1, keepdims=True) * np.ones((1, cfg.E))
-    _grad_close(f64(dl), ref_dl, dl_abs, cfg.torch_dtype, "dlogits")
+    dl_bound = UNIT[cfg.torch_dtype] * np.abs(ref_dl) + 4e-6 * o.scale * np.abs(f64(dw)).sum(axis=1, keepdims=True)
+    assert_within_bound(dl, ref_dl, dl_bound, "dlogits")
     assert moe.moe_device_status() == 0
 
 
@@ -252,17 +265,28 @@ def test_experts_backward_full_size_sampled_experts(cuda_lib):
     torch.cuda.synchronize()
     offs = u32(disp.offsets).astype(np.int64)
     counts = np.diff(offs)
+    xd_all = disp.x_dispatched.cpu()
     for e in sorted({0, 77, int(np.argmax(counts))}):
         lo, hi = int(offs[e]), int(offs[e + 1])
-        sub_off = np.array([0, hi - lo])
-        ref = oracle.experts_backward(cache.x_dispatched[lo:hi].cpu(), inp["gate"][e:e + 1], inp["up"][e:e + 1],
-                                      inp["down"][e:e + 1], sub_off, dy[lo:hi],
-                                      cache=(cache.g[lo:hi].cpu(), cache.u[lo:hi].cpu(), cache.h[lo:hi].cpu()))
-        _grad_close(f64(gr.dx_dispatched[lo:hi]), ref.dx_dispatched, ref.dx_abs, cfg.torch_dtype, f"dx (expert {e})")
-        _grad_close(f64(gr.dgate[e:e + 1]), ref.dgate, ref.dgate_abs, cfg.torch_dtype, f"dgate (expert {e})")
-        _grad_close(f64(gr.dup[e:e + 1]), ref.dup, ref.dup_abs, cfg.torch_dtype, f"dup (expert {e})")
-        _grad_close(f64(gr.ddown[e:e + 1]), ref.ddown, ref.ddown_abs, cfg.torch_dtype, f"ddown (expert {e})")
+        sub = _Sub(cache, lo, hi)
+        sub_gr = _Sub(gr, lo, hi, e)
+        check_experts_training(sub, sub_gr, xd_all[lo:hi], inp["gate"][e:e + 1], inp["up"][e:e + 1],
+                               inp["down"][e:e + 1], np.array([0, hi - lo]), dy[lo:hi], cfg.torch_dtype,
+                               what=f"expert {e}: ")
     assert moe.moe_device_status() == 0
+
+
+class _Sub:
+    """The rows [lo, hi) of a cache or of the row gradients, and expert e's
+    weight gradients (one expert cut out of the full problem)."""
+
+    def __init__(self, src, lo, hi, e=None):
+        for name in ("g", "u", "h", "dx_dispatched"):
+            if hasattr(src, name):
+                setattr(self, name, getattr(src, name)[lo:hi])
+        if e is not None:
+            for name in ("dgate", "dup", "ddown"):
+                setattr(self, name, getattr(src, name)[e:e + 1])
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
@@ -288,12 +312,7 @@ def test_experts_backward_expert_row_counts_around_the_k_steps(cuda_lib, dtype):
     y, cache = moe.moe_experts_forward_training(ex, xd.to(DEV), offs)
     gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
     torch.cuda.synchronize()
-    ref = oracle.experts_backward(xd, gate, up, down, offsets, dy,
-                                  cache=(cache.g.cpu(), cache.u.cpu(), cache.h.cpu()))
-    _grad_close(f64(gr.dx_dispatched), ref.dx_dispatched, ref.dx_abs, dtype, "dx_dispatched")
-    _grad_close(f64(gr.dgate), ref.dgate, ref.dgate_abs, dtype, "dgate")
-    _grad_close(f64(gr.dup), ref.dup, ref.dup_abs, dtype, "dup")
-    _grad_close(f64(gr.ddown), ref.ddown, ref.ddown_abs, dtype, "ddown")
+    check_experts_training(cache, gr, xd, gate, up, down, offsets, dy, dtype)
     assert (gr.dgate[0] == 0).all() and (gr.ddown[0] == 0).all()  # the expert without rows
     assert moe.moe_device_status() == 0
 

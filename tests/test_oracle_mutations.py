@@ -225,6 +225,18 @@ def _experts_backward_swapped_gate_up(x, gate, up, down, offsets, dexpert):
     return _training.ExpertGrads(g.dx_dispatched, g.dup, g.dgate, g.ddown)
 
 
+_tfc = _training.training_forward_cache
+
+
+def _training_cache_gate_up_swapped(x, gate, up, offsets):
+    return _tfc(x, up, gate, offsets)
+
+
+def _training_cache_h_from_up(x, gate, up, offsets):
+    g, u, _ = _tfc(x, gate, up, offsets)
+    return g, u, _training._silu(u) * g
+
+
 def _dispatch_backward_mean(dinput, inv, T, top_k):
     return _db(dinput, inv, T, top_k) / top_k
 
@@ -237,6 +249,8 @@ TRAINING_MUTATIONS = {
     "silu_used_for_its_derivative": ("experts_backward", _experts_backward_silu_for_derivative),
     "gate_and_up_gradients_swapped": ("experts_backward", _experts_backward_swapped_gate_up),
     "dispatch_backward_averages_slots": ("dispatch_backward", _dispatch_backward_mean),
+    "training_cache_gate_up_swapped": ("training_forward_cache", _training_cache_gate_up_swapped),
+    "training_cache_silu_of_up": ("training_forward_cache", _training_cache_h_from_up),
 }
 
 

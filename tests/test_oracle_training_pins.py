@@ -201,6 +201,25 @@ def pin_experts_backward_finite_differences(m):
         assert abs(fd - dx_tok[pos]) < 1e-6 * max(1.0, abs(fd))
 
 
+def pin_training_forward_cache_hand_worked(m):
+    """A hand-worked cache, H = 2, I = 3, two experts (the second with gate
+    and up exchanged, an empty expert between them): x = (1, 2) gives
+    g = (1, 2, 3), u = (2, 1, 0) on expert 0, so h = (2 SiLU(1), SiLU(2), 0)
+    with SiLU(a) = a / (1 + e^-a); expert 2 sees the same x with the roles
+    swapped: g = (2, 1, 0), u = (1, 2, 3), h = (SiLU(2), 2 SiLU(1), 0)."""
+    A = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    B = np.array([[0.0, 1.0], [1.0, 0.0], [2.0, -1.0]])
+    gate = np.stack([A, np.zeros((3, 2)), B])
+    up = np.stack([B, np.zeros((3, 2)), A])
+    x = np.array([[1.0, 2.0], [1.0, 2.0]])
+    g, u, h = m.training_forward_cache(torch.from_numpy(x), torch.from_numpy(gate), torch.from_numpy(up),
+                                       np.array([0, 1, 1, 2]))
+    s1, s2 = 1.0 / (1.0 + np.exp(-1.0)), 2.0 / (1.0 + np.exp(-2.0))
+    np.testing.assert_array_equal(g, [[1, 2, 3], [2, 1, 0]])
+    np.testing.assert_array_equal(u, [[2, 1, 0], [1, 2, 3]])
+    np.testing.assert_allclose(h, [[2 * s1, s2, 0.0], [s2, 2 * s1, 0.0]], rtol=1e-15, atol=0)
+
+
 def pin_dispatch_backward_brute_force(m):
     rng = np.random.default_rng(17)
     idx = np.array([[0, 2], [1, 0], [2, 2], [5, 1]])   # token 3 holds an invalid index
@@ -283,6 +302,7 @@ TRAINING_PINS = [
     pin_router_backward_invariants,
     pin_combine_backward_finite_differences,
     pin_experts_backward_finite_differences,
+    pin_training_forward_cache_hand_worked,
     pin_dispatch_backward_brute_force,
     pin_whole_backward_against_autograd,
     pin_router_option_ranges,

@@ -135,9 +135,11 @@ moe_status moe_dispatch(const uint32_t* indices, int64_t T, int64_t E, int32_t t
  * library's device image; every GPU that loads the library holds it until the
  * process exits. Requests whose scratch, ceil(T*top_k/2048)*E*4 bytes, exceeds
  * it are rejected with MOE_ERR_SHAPE before anything is launched. No call
- * allocates or frees device memory. The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. All calls on a device share
+ * allocates or frees device memory. Every call looks up the array's device
+ * address (cudaGetSymbolAddress) with the calling device current, so the
+ * address stays right after a cudaDeviceReset; the first call on a device
+ * also loads the library's device code there, so make it before any stream
+ * capture. All calls on a device share
  * the array and it keeps the last call's contents (each call writes every
  * entry it reads, so nothing needs clearing): calls that may overlap on the
  * GPU, such as calls on different streams without ordering between them, race

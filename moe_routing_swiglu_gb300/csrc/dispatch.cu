@@ -16,8 +16,6 @@
 //               per expert, and __match_any_sync ranks equal experts inside
 //               each 32-slot step. Indices are loaded once into registers.
 // An index >= E is never dispatched; its inv entry is INVALID_ROW.
-#include <mutex>
-
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -222,24 +220,12 @@ static __device__ __align__(256) uint32_t g_noalloc_dispatch_scratch[NOALLOC_DIS
 
 cudaError_t noalloc_dispatch_scratch(void** ptr) {
   // In host code the array's name is only a stand-in for the device symbol;
-  // the device address comes from cudaGetSymbolAddress, looked up once per
-  // device with that device current and cached.
-  constexpr int kMaxDevices = 256;
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_dispatch_scratch);
-    if (err != cudaSuccess) return err;
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
-  return cudaSuccess;
+  // its device address comes from cudaGetSymbolAddress with the device
+  // current. It is looked up again on every call (a host-side table lookup
+  // once the module is loaded): an address kept from an earlier call would be
+  // stale after cudaDeviceReset, which unloads the module and drops the array.
+  *ptr = nullptr;
+  return cudaGetSymbolAddress(ptr, g_noalloc_dispatch_scratch);
 }
 
 size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {

@@ -103,7 +103,7 @@ def test_gate_up_gather_full_size(cuda_lib):
     """The fine-grained prefill workload at full size (the benchmark's launch
     configuration): gathered and dense gate/up stages agree bit for bit."""
     moe = cuda_lib
-    cfg = workloads.CONFIGS[2]
+    cfg = workloads.CONFIGS[1]
     d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
     ex = moe.Experts(d["gate"], d["up"], d["down"])
     idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
@@ -142,7 +142,7 @@ def test_gate_up_gather_bad_rows_across_a_full_tile(cuda_lib):
     boundary) each give a zero row; every other row matches the dense stage
     bit for bit (prefill workload, full size)."""
     moe = cuda_lib
-    cfg = workloads.CONFIGS[2]
+    cfg = workloads.CONFIGS[1]
     d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
     ex = moe.Experts(d["gate"], d["up"], d["down"])
     idx, _ = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)

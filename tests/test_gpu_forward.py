@@ -40,7 +40,7 @@ def test_forward_full_oracle(cuda_lib, name):
     assert moe.moe_device_status() == 0
 
 
-@pytest.mark.parametrize("cfg_id,n_sample", [(2, 192), (3, 48), (4, 16), (5, 192)])
+@pytest.mark.parametrize("cfg_id,n_sample", [(1, 192), (2, 48), (3, 16), (4, 192)])
 def test_forward_full_size_sampled(cuda_lib, cfg_id, n_sample):
     """Full-size workloads in the benchmark's launch configuration: routing
     and dispatch compared in full, outputs on sampled tokens (first, last and
@@ -80,7 +80,7 @@ def test_forward_equals_split_api(cuda_lib, name):
     assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8))
 
 
-@pytest.mark.parametrize("cfg_id", [2, 5])
+@pytest.mark.parametrize("cfg_id", [1, 4])
 def test_forward_equals_split_api_full_size(cuda_lib, cfg_id):
     """At full size (thousands of tiles): moe_forward is bit-identical, three
     times in a row, to the split route -> dispatch -> experts -> combine path."""
@@ -169,7 +169,7 @@ def test_forward_host_two_streams_pipelined(cuda_lib):
     (one batch's copies overlapping the other's kernels), the prefill
     workload at full size: every batch's host output equals moe_forward's."""
     moe = cuda_lib
-    cfg = workloads.CONFIGS[2]
+    cfg = workloads.CONFIGS[1]
     base = workloads.generate(cfg)
     d = _device_inputs(base)
     ex = moe.Experts(d["gate"], d["up"], d["down"])

@@ -252,7 +252,7 @@ def test_experts_backward_full_size_sampled_experts(cuda_lib):
     sampled experts (their rows, weights and gradients cut out of the full
     problem), including the expert with the most rows."""
     moe = cuda_lib
-    cfg = workloads.CONFIGS[2]
+    cfg = workloads.CONFIGS[1]
     inp = workloads.generate(cfg)
     d = {k: v.to(DEV) for k, v in inp.items()}
     ex = moe.Experts(d["gate"], d["up"], d["down"])

@@ -58,7 +58,7 @@ def pin_exact_tie_lower_id(m):
         assert rt.indices[0].tolist() == [a, b]
         assert rt.weights32[0].tolist() == [0.5, 0.5]
     # the contract row of the F32 workload
-    inp = workloads.generate(workloads.CONFIGS[1], weights=False)
+    inp = workloads.generate(workloads.CONFIGS[0], weights=False)
     rt = m.route(inp["logits"], 2, True)
     assert rt.indices[0].tolist() == [1, 6]
     assert rt.weights32[0].tolist() == [0.5, 0.5]
@@ -168,7 +168,7 @@ def pin_fp32_within_rounding_bound(m):
 
 def pin_contract_rows_of_f32_workload(m):
     """The four special rows of the F32 routing-contract workload."""
-    inp = workloads.generate(workloads.CONFIGS[1], weights=False)
+    inp = workloads.generate(workloads.CONFIGS[0], weights=False)
     rt = m.route(inp["logits"], 2, True)
     assert rt.indices[0].tolist() == [1, 6]
     for r in (1, 2, 3):
@@ -300,7 +300,7 @@ def pin_einsum_cross_statement(m):
 def pin_forward_tokens_consistent(m):
     """Sampled-token evaluation equals the full forward on those tokens
     (including the NaN rows of the contract workload)."""
-    cfg = workloads.CONFIGS[1]
+    cfg = workloads.CONFIGS[0]
     inp = workloads.generate(cfg)
     full = m.forward(inp["x"], inp["logits"], inp["gate"], inp["up"], inp["down"], cfg.top_k, True)
     toks = np.array([0, 1, 2, 3, 17, 63])

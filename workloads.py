@@ -6,8 +6,9 @@ holds none of the routing, dispatch, expert or combine arithmetic, so neither
 the CUDA path nor the CPU oracle depends on the other through it.
 
 Recipe (identical bytes for both sides):
-  * one torch CPU ``Generator`` per configuration (seed ``1000 + cfg``) draws
-    the logits and x, in that order;
+  * one torch CPU ``Generator`` per configuration (seed ``1001 + i`` for
+    configuration i, numbered from 0) draws the logits and x, in that order
+    (token shard r > 0 of a data-parallel run: seed ``1001 + i + 7919 r``);
   * gate, up and down are drawn in fixed chunks of ``_CHUNK`` elements, each
     from its own generator seeded from (config seed, tensor id, chunk index),
     so the bytes do not depend on how many threads draw them;
@@ -64,34 +65,37 @@ class MoeConfig:
         return replace(self, name=name, **kw)
 
 
-# The five workloads of the local MoE forward chain.
+# The five workloads of the local MoE forward chain, numbered from 0 in the
+# order they are listed: 0 the F32 routing-contract case, 1 the fine-grained
+# BF16 prefill, 2 the coarse BF16 prefill (the GEMM-bound case), 3 the BF16
+# decode, 4 the Zipf-skewed F16 prefill.
 CONFIGS = {
-    1: MoeConfig("f32_routing_contract_T64_H128_I256_E8_k2", "f32", 64, 128, 256, 8, 2, True,
+    0: MoeConfig("f32_routing_contract_T64_H128_I256_E8_k2", "f32", 64, 128, 256, 8, 2, True,
                  "contract_rows", 1001),
-    2: MoeConfig("bf16_prefill_T4096_H2048_I768_E128_k8", "bf16", 4096, 2048, 768, 128, 8, True,
+    1: MoeConfig("bf16_prefill_T4096_H2048_I768_E128_k8", "bf16", 4096, 2048, 768, 128, 8, True,
                  "normal", 1002),
-    3: MoeConfig("bf16_prefill_T8192_H4096_I14336_E8_k2", "bf16", 8192, 4096, 14336, 8, 2, True,
+    2: MoeConfig("bf16_prefill_T8192_H4096_I14336_E8_k2", "bf16", 8192, 4096, 14336, 8, 2, True,
                  "normal", 1003),
-    4: MoeConfig("bf16_decode_T16_H2048_I768_E128_k8", "bf16", 16, 2048, 768, 128, 8, True,
+    3: MoeConfig("bf16_decode_T16_H2048_I768_E128_k8", "bf16", 16, 2048, 768, 128, 8, True,
                  "normal", 1004),
-    5: MoeConfig("f16_zipf_T16384_H2048_I1408_E64_k6", "f16", 16384, 2048, 1408, 64, 6, False,
+    4: MoeConfig("f16_zipf_T16384_H2048_I1408_E64_k6", "f16", 16384, 2048, 1408, 64, 6, False,
                  "zipf", 1005),
 }
 
 # Reduced sizes of the same workloads: small enough for the full oracle in a few
 # seconds, still several tiles in every dimension and ragged per-expert tails.
 SMALL_CONFIGS = {
-    "f32_contract": CONFIGS[1],
-    "bf16_fine": CONFIGS[2].scaled("bf16_fine_small_T600_H512_I384_E24_k5", T=600, H=512, I=384,
+    "f32_contract": CONFIGS[0],
+    "bf16_fine": CONFIGS[1].scaled("bf16_fine_small_T600_H512_I384_E24_k5", T=600, H=512, I=384,
                                    E=24, top_k=5, seed=2002),
-    "bf16_coarse": CONFIGS[3].scaled("bf16_coarse_small_T520_H1024_I1280_E4_k2", T=520, H=1024,
+    "bf16_coarse": CONFIGS[2].scaled("bf16_coarse_small_T520_H1024_I1280_E4_k2", T=520, H=1024,
                                      I=1280, E=4, top_k=2, seed=2003),
-    "bf16_decode": CONFIGS[4],
-    "f16_zipf": CONFIGS[5].scaled("f16_zipf_small_T1200_H512_I640_E16_k3", T=1200, H=512, I=640,
+    "bf16_decode": CONFIGS[3],
+    "f16_zipf": CONFIGS[4].scaled("f16_zipf_small_T1200_H512_I640_E16_k3", T=1200, H=512, I=640,
                                   E=16, top_k=3, seed=2005),
-    "f32_ragged": CONFIGS[1].scaled("f32_ragged_T333_H200_I136_E7_k3", T=333, H=200, I=136, E=7,
+    "f32_ragged": CONFIGS[0].scaled("f32_ragged_T333_H200_I136_E7_k3", T=333, H=200, I=136, E=7,
                                     top_k=3, logits_kind="normal", seed=2006),
-    "bf16_ragged": CONFIGS[2].scaled("bf16_ragged_T77_H136_I200_E5_k2", T=77, H=136, I=200, E=5,
+    "bf16_ragged": CONFIGS[1].scaled("bf16_ragged_T77_H136_I200_E5_k2", T=77, H=136, I=200, E=5,
                                      top_k=2, seed=2007),
 }
 
@@ -118,8 +122,8 @@ class GroupedRouting:
 # smaller group layouts on the reduced workloads (one expert per group,
 # one group of all experts, groups of 6 and of 4).
 GROUPED = {
-    "bf16_prefill_grouped": (CONFIGS[2], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3002)),
-    "bf16_decode_grouped": (CONFIGS[4], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3004)),
+    "bf16_prefill_grouped": (CONFIGS[1], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3002)),
+    "bf16_decode_grouped": (CONFIGS[3], GroupedRouting(8, 4, 8, True, True, 2.5, 0.02, 3004)),
     "bf16_fine_grouped": (SMALL_CONFIGS["bf16_fine"], GroupedRouting(4, 2, 5, True, True, 1.0, 0.05, 3012)),
     "f16_zipf_grouped": (SMALL_CONFIGS["f16_zipf"], GroupedRouting(4, 2, 3, False, False, 1.5, 0.1, 3015)),
     "f32_ragged_grouped": (SMALL_CONFIGS["f32_ragged"], GroupedRouting(7, 3, 3, False, True, 1.0, 0.1, 3016)),
@@ -198,15 +202,26 @@ def _zipf_logits(logits: torch.Tensor, g: torch.Generator) -> torch.Tensor:
     return l.to(torch.float32)
 
 
+def token_seed(cfg: MoeConfig, shard: int = 0) -> int:
+    """Seed of the logits and x of token shard ``shard`` (0: the workload's own
+    batch). Shards of a data-parallel run draw distinct tokens; the expert
+    weights are always drawn from the workload's seed (replicated experts)."""
+    return cfg.seed + 7919 * shard
+
+
 def generate(cfg: MoeConfig, device: str | torch.device = "cpu", weights: bool = True,
-             pin: bool = False) -> dict:
+             pin: bool = False, shard: int = 0) -> dict:
     """Draw logits [T,E], x [T,H], gate/up [E,I,H] and down [E,H,I] in cfg.dtype.
 
     The tensors are created on the CPU and then moved to ``device``; ``pin``
     places the CPU copies of x and logits in pinned memory (for timed
-    host-to-device copies)."""
+    host-to-device copies). ``shard`` > 0 draws another batch of T tokens
+    (logits and x) with the same expert weights; only plain N(0,1) logits
+    have shards."""
     dt = cfg.torch_dtype
-    g = torch.Generator().manual_seed(cfg.seed)
+    if shard and cfg.logits_kind != "normal":
+        raise ValueError("token shards are defined for N(0,1) logits only")
+    g = torch.Generator().manual_seed(token_seed(cfg, shard))
     logits = torch.randn(cfg.T, cfg.E, generator=g)
     x = torch.randn(cfg.T, cfg.H, generator=g)
     if cfg.logits_kind == "contract_rows":

@@ -204,6 +204,48 @@ moe_status moe_experts_forward_dispatched(const moe_experts* experts, const void
                                           size_t workspace_bytes, void* stream);
 
 /*
+ * moe_experts_forward_combine - the experts and the weighted combine in one
+ * launch: SwiGluExperts::forward_dispatched followed by
+ * DispatchedTokens::combine (ruDNN user guide section 6), the combine run by
+ * the down GEMM's epilogue warps ("PyTorch general ops", section "two ways
+ * to write a contraction": the routing-weighted sum over a token's top_k
+ * expert outputs is part of the expert contraction).
+ *
+ *   x_dispatched, offsets   as in moe_experts_forward_dispatched.
+ *   inv           device, [T * top_k] uint32 (from moe_dispatch).
+ *   weights       device, [T, top_k] in `weights_dtype` (from moe_route),
+ *                 aligned to its element size.
+ *   T, top_k      1 <= top_k <= min(E, 64); rows = T * top_k.
+ *   out           device, [T, H] out in the experts' dtype, 16-byte aligned:
+ *                 out[t] = sum over j = 0..top_k-1, in that order, of
+ *                 w[t, j] * y[inv[t * top_k + j]], FP32 accumulation, then
+ *                 rounded to the dtype, y being the expert outputs rounded to
+ *                 the dtype. The bits equal moe_experts_forward_dispatched
+ *                 followed by moe_combine.
+ *   workspace     device scratch of
+ *                 moe_experts_forward_combine_workspace_size(experts, T,
+ *                 top_k) bytes (h, y_dispatched, the tile counter, one
+ *                 counter per expert and the combine's counter), 256-byte
+ *                 aligned.
+ *
+ * How: every epilogue warp of every down tile raises one done counter once
+ * its y rows are stored; a CTA that has run out of tiles waits (bounded,
+ * about a second: on timeout the device status word records 0x1A) until the
+ * counter shows every down tile done, then its epilogue warps combine a
+ * fixed stripe of the tokens, four tokens' slot rows in one stream of loads
+ * per warp. It waits only on tiles already claimed by running CTAs, so it
+ * cannot deadlock. The counters are reset on the stream first. F16/BF16
+ * experts and top_k <= 64 only (else MOE_ERR_UNSUPPORTED; use
+ * moe_experts_forward_dispatched and moe_combine). An inv entry >= rows
+ * makes its token's row NaN, as in moe_combine.
+ */
+size_t moe_experts_forward_combine_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k);
+moe_status moe_experts_forward_combine(const moe_experts* experts, const void* x_dispatched,
+                                       const uint32_t* offsets, const uint32_t* inv, const void* weights,
+                                       moe_dtype weights_dtype, int64_t T, int32_t top_k, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * moe_experts_gate_up / moe_experts_down - the two grouped-GEMM stages of
  * moe_experts_forward_dispatched, for callers that want h or want to time or
  * schedule the stages apart. Same arguments and checks as above.
@@ -278,8 +320,10 @@ moe_status moe_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t
  * moe_experts_forward_dispatched and moe_combine in turn: the outputs are
  * bit-identical to that sequence. F16/BF16 run the two expert GEMMs as one
  * launch (as moe_experts_forward_dispatched does; the dispatch zeroes its
- * counters). For decode-sized batches (T * top_k <= 8 * E) it dispatches
- * the maps only and the gate/up tiles gather x rows through row_src (as
+ * counters), then the combine as its own launch (measured faster than the
+ * combine inside the experts' launch, moe_experts_forward_combine). For
+ * decode-sized batches (T * top_k <= 8 * E) it dispatches the maps only and
+ * the gate/up tiles gather x rows through row_src (as
  * moe_experts_gate_up_gather), so x_dispatched is never written.
  */
 size_t moe_forward_workspace_size(const moe_experts* experts, int64_t T, int32_t top_k);

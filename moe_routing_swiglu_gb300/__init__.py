@@ -73,6 +73,9 @@ SIGNATURES = {
     "moe_experts_destroy": (None, [_P]),
     "moe_experts_forward_dispatched_workspace_size": (_SZ, [_P, _I64]),
     "moe_experts_forward_dispatched": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
+    "moe_experts_forward_combine_workspace_size": (_SZ, [_P, _I64, _I32]),
+    "moe_experts_forward_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int, _I64, _I32, _P, _P, _SZ,
+                                                   _P]),
     "moe_experts_gate_up": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
     "moe_experts_down": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _SZ, _P]),
     "moe_experts_gate_up_gather": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _P, _I64, _P, _P, _SZ, _P]),
@@ -274,6 +277,23 @@ def moe_experts_forward_dispatched(experts: Experts, x_dispatched: torch.Tensor,
     ws = _workspace(need, x_dispatched.device, workspace)
     _check(lib.moe_experts_forward_dispatched(experts.handle, _ptr(x_dispatched), _ptr(offsets), rows,
                                               _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def moe_experts_forward_combine(experts: Experts, x_dispatched: torch.Tensor, offsets: torch.Tensor,
+                                inv: torch.Tensor, weights: torch.Tensor, out=None, workspace=None, stream=None):
+    """forward_dispatched and combine in one launch: out [T, H] = sum over
+    slots j (in order) of w[t, j] * y[inv[t * top_k + j]] (inv from
+    moe_dispatch, weights [T, top_k] from moe_route)."""
+    lib = load_library()
+    _dev_tensor(x_dispatched, "x_dispatched")
+    T, top_k = weights.shape
+    y = out if out is not None else torch.empty(T, experts.H, dtype=experts.dtype, device=x_dispatched.device)
+    need = lib.moe_experts_forward_combine_workspace_size(experts.handle, T, top_k)
+    ws = _workspace(need, x_dispatched.device, workspace)
+    _check(lib.moe_experts_forward_combine(experts.handle, _ptr(x_dispatched), _ptr(offsets), _ptr(inv),
+                                           _ptr(weights), _dt(weights), T, top_k, _ptr(y), _ptr(ws), ws.numel(),
+                                           _stream(stream)))
     return y
 
 

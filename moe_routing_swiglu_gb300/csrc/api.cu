@@ -97,6 +97,13 @@ moe_status check_bias(const float* bias) {
   return MOE_OK;
 }
 
+// The fused combine (moe_experts_forward_combine) runs for F16/BF16 and
+// top_k <= 64 (a warp stages the (row, weight) pairs of four tokens in a
+// 2 KB buffer).
+bool combine_can_fuse(const moe_experts* ex, int64_t top_k) {
+  return ex->dtype != MOE_F32 && top_k <= moe::COMB_MAX_TOP_K;
+}
+
 struct ForwardLayout {
   size_t indices, weights, counts, offsets, row_src, inv, scratch, sched, xd, h, yd, total;
 };
@@ -119,7 +126,7 @@ ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
   L.inv = take(n * 4);
   L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
   // Tile counters, then (from word 64) one ready counter per expert for the
-  // chained gate/up + down kernel.
+  // chained gate/up + down kernel; the dispatch zeroes them.
   L.sched = take(moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4);
   L.xd = take(moe::forward_gathers_rows(static_cast<int64_t>(n), ex->E) ? 0 : n * static_cast<size_t>(ex->H) * es);
   L.h = take(n * static_cast<size_t>(ex->I) * es);
@@ -225,7 +232,7 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
   err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
                              ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched,
-                             static_cast<int>(moe::TC_SCHED_BYTES / 4 + ex->E));
+                             static_cast<int64_t>(moe::TC_SCHED_BYTES / 4 + ex->E));
   if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
   const moe::TcGather gather{x, row_src, top_k, T};
   if (ex->dtype == MOE_F32) {
@@ -234,6 +241,9 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
     st = run_stage(ex, false, h, nullptr, offsets, rows, yd, sched + 1, s, nullptr, true);
     if (st != MOE_OK) return st;
   } else {
+    // F16/BF16: gate/up and down in one launch. The combine stays a launch
+    // of its own: with the combine inside the experts' launch
+    // (moe_experts_forward_combine) every measured workload ran slower.
     const char* why = nullptr;
     err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, xd, gather_rows ? &gather : nullptr, nullptr, offsets,
                                        static_cast<int>(ex->E), rows, ex->H, ex->I, h, yd, sched, ready, ex->num_sms,
@@ -457,6 +467,63 @@ moe_status moe_experts_forward_dispatched(const moe_experts* ex, const void* x_d
                                      ex->H, ex->I, workspace, y_dispatched, sched, sched + moe::TC_SCHED_BYTES / 4,
                                      ex->num_sms, s, &why);
   if (err != cudaSuccess) return cuda_fail(err, "gate/up + down GEMM launch", why);
+  return ok();
+}
+
+// h, then y_dispatched, then the tile counter, the per-expert ready counters
+// and the combine's done counter.
+size_t moe_experts_forward_combine_workspace_size(const moe_experts* ex, int64_t T, int32_t top_k) {
+  if (ex == nullptr || T < 0 || top_k < 1 || !slots_fit(T, top_k)) return 0;
+  const size_t n = static_cast<size_t>(T) * static_cast<size_t>(top_k);
+  const size_t es = dtype_size(ex->dtype);
+  return align_up(n * static_cast<size_t>(ex->I) * es + 1, 256) + align_up(n * static_cast<size_t>(ex->H) * es + 1, 256) +
+         moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4 + 16;
+}
+
+moe_status moe_experts_forward_combine(const moe_experts* ex, const void* x_dispatched, const uint32_t* offsets,
+                                       const uint32_t* inv, const void* weights, moe_dtype weights_dtype, int64_t T,
+                                       int32_t top_k, void* out, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (ex == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "experts and offsets must be non-NULL");
+  if (!dtype_valid(weights_dtype)) return fail(MOE_ERR_DTYPE, "weights dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (T < 0 || top_k < 1 || top_k > ex->E) return fail(MOE_ERR_TOP_K, "top_k must satisfy 1 <= top_k <= E");
+  if (!slots_fit(T, top_k)) return fail(MOE_ERR_SHAPE, "T * top_k must be below 2^32 - 1");
+  if (!combine_can_fuse(ex, top_k))
+    return fail(MOE_ERR_UNSUPPORTED, "the fused combine runs on the F16/BF16 tensor-core path with top_k <= 64; "
+                                     "otherwise use moe_experts_forward_dispatched and moe_combine");
+  if (T > 0 && (x_dispatched == nullptr || inv == nullptr || weights == nullptr || out == nullptr))
+    return fail(MOE_ERR_NULL, "x_dispatched, inv, weights and out must be non-NULL");
+  if (T > 0 && (!aligned16(x_dispatched) || !aligned16(out)))
+    return fail(MOE_ERR_ALIGNMENT, "x_dispatched and out must be 16-byte aligned");
+  if (T > 0 && reinterpret_cast<uintptr_t>(weights) % dtype_size(weights_dtype) != 0)
+    return fail(MOE_ERR_ALIGNMENT, "weights must be aligned to their element size");
+  const size_t need = moe_experts_forward_combine_workspace_size(ex, T, top_k);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_experts_forward_combine_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  moe_status st = check_current_device(ex);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  const int64_t rows = T * top_k;
+  const size_t n = static_cast<size_t>(rows);
+  const size_t es = dtype_size(ex->dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* h = ws;
+  const size_t h_bytes = align_up(n * static_cast<size_t>(ex->I) * es + 1, 256);
+  void* yd = ws + h_bytes;
+  uint8_t* counters = ws + h_bytes + align_up(n * static_cast<size_t>(ex->H) * es + 1, 256);
+  const size_t cnt_bytes = moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4 + 16;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemsetAsync(counters, 0, cnt_bytes, s);
+  if (err != cudaSuccess) return cuda_fail(err, "counter reset");
+  uint32_t* sched = reinterpret_cast<uint32_t*>(counters);
+  uint32_t* ready = sched + moe::TC_SCHED_BYTES / 4;
+  const moe::TcCombine comb{inv, weights, weights_dtype, top_k, T, ready + ex->E, out};
+  const char* why = nullptr;
+  err = moe::launch_experts_tc_chain(ex->tc, ex->dtype, x_dispatched, nullptr, nullptr, offsets,
+                                     static_cast<int>(ex->E), rows, ex->H, ex->I, h, yd, sched, ready, ex->num_sms, s,
+                                     &why, &comb);
+  if (err != cudaSuccess) return cuda_fail(err, "gate/up + down + combine GEMM launch", why);
   return ok();
 }
 

@@ -54,7 +54,7 @@ template <bool SINGLE>
 __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
     const uint32_t* __restrict__ indices, int64_t n, int E, int nchunks,
     const uint32_t* __restrict__ hist, uint32_t* __restrict__ counts, uint32_t* __restrict__ offsets,
-    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv, uint32_t* __restrict__ zero_words, int n_zero) {
+    uint32_t* __restrict__ row_src, uint32_t* __restrict__ inv, uint32_t* __restrict__ zero_words, int64_t n_zero) {
   __shared__ uint32_t wh[SCATTER_WARPS][ROUTE_MAX_E];
   __shared__ uint32_t first[ROUTE_MAX_E];   // first row of this chunk per expert
   __shared__ uint32_t tot[ROUTE_MAX_E];
@@ -63,9 +63,16 @@ __global__ void __launch_bounds__(SCATTER_WARPS * 32) dispatch_scatter_kernel(
   grid_dependency_wait();
   launch_dependents();
   // The counters of the expert GEMMs that follow in moe_forward (tile
-  // counter and per-expert ready counters).
-  if (blockIdx.x == 0 && zero_words != nullptr)
-    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
+  // counter and per-expert ready counters), 16 bytes per store, spread over
+  // the grid.
+  if (zero_words != nullptr) {
+    const int64_t n4 = n_zero >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint4* z4 = reinterpret_cast<uint4*>(zero_words);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+      z4[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (blockIdx.x == 0 && threadIdx.x < (n_zero & 3)) zero_words[(n4 << 2) + threadIdx.x] = 0u;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * DISPATCH_CHUNK +
                      static_cast<int64_t>(warp) * SLOTS_PER_WARP;
@@ -237,7 +244,7 @@ size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                            cudaStream_t stream, uint32_t* zero_words, int n_zero) {
+                            cudaStream_t stream, uint32_t* zero_words, int64_t n_zero) {
   const int64_t n = T * top_k;
   const int nchunks = static_cast<int>((n + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
   uint32_t* hist = static_cast<uint32_t*>(scratch);

@@ -116,7 +116,7 @@ struct TcCfg {
   // full[S], empty[S], tile_full[R], tile_empty[R], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 * RING + 5;
   static constexpr int SMEM_RING = SMEM_BAR + 8 * NUM_BARS;
-  static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;
+  static constexpr int SMEM_MISC = SMEM_RING + 4 * RING;          // TMEM address, abort flag, combine flag
   static constexpr int SMEM_BAD = SMEM_MISC + 16;                  // [RING][BAD_WORDS]
   static constexpr int SMEM_TILES = SMEM_BAD + 4 * RING * BAD_WORDS;
   static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + 4 * (ROUTE_MAX_E + 1);
@@ -172,7 +172,110 @@ struct TcArgs {
   int k_blocks2;
   int n_out2;
   uint32_t* ready;
+  // Fused combine (chained mode): every epilogue warp of every down tile
+  // raises one done counter once its y rows are stored. A CTA whose tiles
+  // are all done waits until the counter shows every down tile done, then
+  // its epilogue warps write out[t] = sum_{j=0..k-1} w[t, j] * y[inv[t*k + j]]
+  // (FP32, slot order) for a fixed stripe of the tokens.
+  const uint32_t* comb_inv;  // [T * top_k] flat slot -> dispatched row
+  const void* comb_w;        // [T, top_k] routing weights, dtype comb_wdt
+  int comb_wdt;              // moe_dtype of the weights
+  int comb_k;                // top_k, 1 .. COMB_MAX_K
+  uint32_t comb_T;           // tokens
+  uint32_t* comb_done;       // [1] down-tile epilogue arrivals, zero at launch
+  void* comb_out;            // [T, n_out2]
 };
+
+constexpr int COMB_TOKENS_PER_PASS = 4;  // tokens a warp combines in one stream of loads
+// A warp stages the (row, weight) pairs of COMB_TOKENS_PER_PASS tokens in
+// its 2 KB buffer: top_k is at most 2048 / (8 * COMB_TOKENS_PER_PASS).
+constexpr int COMB_PAIRS = XPOSE_BYTES / 8;
+constexpr int COMB_MAX_K = COMB_PAIRS / COMB_TOKENS_PER_PASS;
+static_assert(COMB_MAX_K == COMB_MAX_TOP_K, "the host's top_k bound matches the staging buffer");
+constexpr uint32_t ST_COMB_WAIT = 0x1A;
+
+__device__ __forceinline__ float comb_weight(const void* w, int wdt, int64_t i) {
+  if (wdt == MOE_F32) return static_cast<const float*>(w)[i];
+  if (wdt == MOE_F16) return __half2float(static_cast<const __half*>(w)[i]);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(w)[i]);
+}
+
+// The combine of n tokens (tok[0..n)) by one warp from their staged (row,
+// weight) pairs rows[i*k + j], wts[i*k + j] (bad[i]: a slot of token i is
+// undispatched, its row becomes NaN as in the separate combine): lane l takes
+// the 8-column chunks q = l, l + 32, ... and computes
+//   out[t, c] = sum_{j=0..k-1} w[t, j] * y[row_j, c]
+// with FP32 FMAs in slot order (the order and arithmetic of the separate
+// combine kernel, so the two give the same bits), then rounds to T. The
+// (token, chunk, slot) triples are visited in that order, G row loads in
+// flight per lane across tokens.
+template <typename T, int NMAX>
+__device__ __forceinline__ void comb_tokens(int n, const uint32_t (&tok)[NMAX], const bool (&bad)[NMAX],
+                                            const TcArgs& a, const uint32_t* rows, const float* wts, int lane) {
+  constexpr int G = 16;
+  const int k = a.comb_k;
+  const int64_t H = a.n_out2;
+  const int nq = static_cast<int>((H / 8 + 31) / 32);  // chunks per lane (H is a multiple of 8)
+  const T* y = static_cast<const T*>(a.out2);
+  const float qnan = __int_as_float(0x7FC00000);
+  int b = 0, i = 0, j = 0;  // token, chunk, slot of the next triple
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  while (b < n) {
+    uint4 v[G];
+    float wv[G];
+    int pb[G], pi[G], pj[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      pb[g] = b;
+      pi[g] = i;
+      pj[g] = j;
+      wv[g] = 0.0f;
+      v[g] = make_uint4(0u, 0u, 0u, 0u);
+      if (b < n) {
+        const int64_t col = static_cast<int64_t>(lane + 32 * i) * 8;
+        wv[g] = wts[b * k + j];
+        if (col < H) v[g] = __ldcg(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(rows[b * k + j]) * H + col));
+        if (++j == k) {
+          j = 0;
+          if (++i == nq) {
+            i = 0;
+            ++b;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (pb[g] < n) {
+        if (pj[g] == 0) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        }
+        const T* e8 = reinterpret_cast<const T*>(&v[g]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[g], to_f32(e8[e]), acc[e]);
+        const int64_t col = static_cast<int64_t>(lane + 32 * pi[g]) * 8;
+        if (pj[g] == k - 1 && col < H) {
+          bool badb = false;
+          uint32_t t = 0;
+#pragma unroll
+          for (int x = 0; x < NMAX; ++x)
+            if (x == pb[g]) {
+              badb = bad[x];
+              t = tok[x];
+            }
+          uint4 raw;
+          T* r = reinterpret_cast<T*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) r[e] = from_f32<T>(badb ? qnan : acc[e]);
+          *reinterpret_cast<uint4*>(static_cast<T*>(a.comb_out) + static_cast<int64_t>(t) * H + col) = raw;
+        }
+      }
+    }
+  }
+}
 
 // SiLU(g) = g * sigmoid(g), sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
 // tanh.approx (relative error about 2^-11, below the 16-bit output's rounding).
@@ -194,7 +297,8 @@ __device__ __forceinline__ float silu_f32(float g) {
 // start the down GEMM of the experts already done instead of idling until
 // the last gate/up tile ends. Every gate/up tile is claimed before any down
 // tile, by a running CTA, so every wait ends.
-template <typename T, bool GATE_UP, int TBM, int LOAD, bool CHAIN = false>
+// COMB (chained mode only): the down tiles combine into out (see TcArgs).
+template <typename T, bool GATE_UP, int TBM, int LOAD, bool CHAIN = false, bool COMB = false>
 __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     experts_tc_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
@@ -204,6 +308,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
                       const __grid_constant__ CUtensorMap tm_c128,
                       const __grid_constant__ CUtensorMap tm_c16, const TcArgs args) {
   static_assert(!CHAIN || LOAD != TOK_CPASYNC, "the chained kernel streams dense or row-gathered tokens");
+  static_assert(!COMB || CHAIN, "the fused combine belongs to the chained kernel");
   using C = TcCfg<TBM>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
@@ -245,6 +350,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    abort_flag[1] = 0;  // the fused combine's go flag
     fence_mbarrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&tm_a0);
@@ -267,6 +373,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
   grid_dependency_wait();
   if (warp == 0) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks, tile_start);
   if (CHAIN && warp == 2) build_tile_prefix(args.offsets, args.E, TB, args.n_wblocks2, tile_start2);
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -274,7 +381,7 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
   // The cap keeps a corrupt offsets array from producing an endless tile loop.
   const uint32_t n_gu = CHAIN ? tile_start[args.E] : 0u;
   const uint32_t total = min(CHAIN ? n_gu + tile_start2[args.E] : tile_start[args.E], args.tile_cap);
-  // Tile -> coordinates, and whether it is a gate/up tile.
+  // Tile -> coordinates, and whether it is a gate/up tile (GEMM tiles only).
   auto tile_coord = [&](uint32_t tile, bool& gu) -> TileCoord {
     if (!CHAIN || tile < n_gu) {
       gu = CHAIN ? true : GATE_UP;
@@ -355,12 +462,10 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
           if (lane == 0 && 4 * g + q < BAD_WORDS) tile_bad[slot * BAD_WORDS + 4 * g + q] = word;
         }
       }
-      if (lane == 0) {
-        ring[slot] = tile;
-        mbar_arrive(&tile_full[slot]);  // release: the ring entry and flags are visible to the waiters
-      }
       if (CHAIN && !gu) {
         // The expert's h rows: every gate/up tile of it has stored them.
+        // Waited for before the tile is published, so that the MMA and
+        // epilogue waits of a down tile start only once its inputs exist.
         bool ready = true;
         if (lane == 0) {
           const uint32_t need = static_cast<uint32_t>(NUM_EPI_WARPS) * (tile_start[tc.e + 1] - tile_start[tc.e]);
@@ -371,6 +476,10 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
           ok = false;
           break;
         }
+      }
+      if (lane == 0) {
+        ring[slot] = tile;
+        mbar_arrive(&tile_full[slot]);  // release: the ring entry and flags are visible to the waiters
       }
       const uint32_t tx = static_cast<uint32_t>(2 * A_BYTES + n_tok * ROW_BYTES);
       const int n_gather = n_tok >> 2;
@@ -443,9 +552,9 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         }
         const uint32_t claimed = atomicAdd(args.sched, 1u);
         const uint32_t tile = claimed < total ? claimed : TILE_END;
-        ring[slot] = tile;
-        mbar_arrive(&tile_full[slot]);  // release: the ring entry is visible to the waiters
         if (tile == TILE_END) {
+          ring[slot] = tile;
+          mbar_arrive(&tile_full[slot]);  // release: the ring entry is visible to the waiters
           launch_dependents();  // this CTA claims no more tiles
           break;
         }
@@ -459,7 +568,9 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         const int wrow1 = gu ? tc.n * BM : tc.n * (2 * BM) + BM;
         const int k_blocks = CHAIN && !gu ? args.k_blocks2 : args.k_blocks;
         // Down tile (CHAIN): the expert's h rows, once every gate/up tile of
-        // it has stored them.
+        // it has stored them; waited for before the tile is published, so
+        // that the MMA and epilogue waits of a down tile start only once its
+        // inputs exist.
         if (CHAIN && !gu &&
             !counter_wait_bounded(args.ready + tc.e,
                                   static_cast<uint32_t>(NUM_EPI_WARPS) * (tile_start[tc.e + 1] - tile_start[tc.e]),
@@ -467,6 +578,8 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
           ok = false;
           break;
         }
+        ring[slot] = tile;
+        mbar_arrive(&tile_full[slot]);  // release: the ring entry is visible to the waiters
         const CUtensorMap* ma0 = CHAIN && !gu ? &tm_a2 : &tm_a0;
         const CUtensorMap* ma1 = CHAIN && !gu ? &tm_a2 : &tm_a1;
         const CUtensorMap* mb128 = CHAIN && !gu ? &tm_c128 : &tm_b128;
@@ -581,13 +694,17 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
     uint16_t* xp = reinterpret_cast<uint16_t*>(smem + C::SMEM_XPOSE + ew * XPOSE_BYTES);
     const int rd_tok = lane >> 2;               // transpose read-back: token within 8
     const int rd_part = lane & 3;               // 16-byte run within the 64-byte row
-    bool live = true;
-    for (uint32_t it = 0; live; ++it) {
+    bool tiles_done = false;  // the tile loop ended at the scheduler's end mark, not on a failure
+    for (uint32_t it = 0;; ++it) {
       const uint32_t slot = it % RING;
       bool ok = mbar_wait_bounded(&tile_full[slot], (it / RING) & 1u, abort_flag, args.status,
                                   ST_TILE_RING, WAIT_LIMIT_NS);
       const uint32_t tile = ok ? static_cast<uint32_t>(ring[slot]) : static_cast<uint32_t>(TILE_END);
-      if (!__all_sync(FULL_MASK, ok) || tile == TILE_END) break;
+      const bool all_ok = __all_sync(FULL_MASK, ok);
+      if (!all_ok || tile == TILE_END) {
+        tiles_done = all_ok;
+        break;
+      }
       bool gu;
       const TileCoord tc = tile_coord(tile, gu);
       const uint32_t acc = it % C::ACC;
@@ -665,6 +782,93 @@ __global__ void __launch_bounds__(num_threads<LOAD>(), 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) counter_release_add(args.ready + tc.e);
+      }
+      if (COMB && !gu) {
+        // Publish this warp's y rows of the tile to the combine (other CTAs'
+        // reads): each lane's stores, then one release per warp on the done
+        // counter, after the accumulator is released.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) counter_release_add(args.comb_done);
+      }
+    }
+    if (COMB && tiles_done) {
+      // Every tile was claimed by a running CTA before this one saw the end
+      // mark, so the done counter reaches its total and the wait ends. One
+      // warp per CTA polls it (bounded) and raises a shared flag for the
+      // others (whose wait is bounded too).
+      volatile int* go = abort_flag + 1;
+      bool ok = true;
+      if (ew == 0) {
+        if (lane == 0)
+          ok = counter_wait_bounded(args.comb_done, static_cast<uint32_t>(NUM_EPI_WARPS) * tile_start2[args.E],
+                                    abort_flag, args.status, ST_COMB_WAIT, WAIT_LIMIT_NS);
+        ok = __shfl_sync(FULL_MASK, ok ? 1 : 0, 0) != 0;
+        if (ok && lane == 0) {
+          __threadfence_block();
+          *go = 1;
+        }
+      } else {
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t poll = 0; *go == 0; ++poll) {
+            __nanosleep(128);
+            if ((poll & 15u) == 15u && (*abort_flag != 0 || globaltimer_ns() - t0 > WAIT_LIMIT_NS)) {
+              if (*abort_flag == 0) {
+                *abort_flag = 1;
+                record_status(args.status, ST_COMB_WAIT);
+              }
+              ok = false;
+              break;
+            }
+          }
+          __threadfence();  // the flag's writer had acquired the counter at GPU scope
+        }
+        ok = __shfl_sync(FULL_MASK, ok ? 1 : 0, 0) != 0;
+      }
+      __syncwarp();
+      if (ok) {
+        // Tokens gw, gw + nw, gw + 2 nw, ... of the global warp gw, up to
+        // COMB_TOKENS_PER_PASS per pass: stage their (row, weight) pairs,
+        // then combine them in one stream of loads.
+        constexpr int P = COMB_TOKENS_PER_PASS;
+        uint32_t* rows = reinterpret_cast<uint32_t*>(xp);
+        float* wts = reinterpret_cast<float*>(xp) + COMB_PAIRS;
+        const int k = args.comb_k;
+        const uint32_t nw = gridDim.x * NUM_EPI_WARPS;
+        const uint32_t gw = blockIdx.x * NUM_EPI_WARPS + ew;
+        for (uint32_t t0 = gw; t0 < args.comb_T; t0 += P * nw) {
+          uint32_t tok[P];
+          bool bad[P];
+          int n = 0;
+#pragma unroll
+          for (int i = 0; i < P; ++i) {
+            tok[i] = t0 + static_cast<uint32_t>(i) * nw;
+            bad[i] = false;
+            if (tok[i] < args.comb_T) n = i + 1;
+          }
+          for (int p0 = 0; p0 < n * k; p0 += 32) {
+            const int p = p0 + lane;
+            const int pi = p / k, pj = p - pi * k;
+            bool inval = false;
+            if (p < n * k) {
+              uint32_t t = 0;
+#pragma unroll
+              for (int i = 0; i < P; ++i)
+                if (i == pi) t = tok[i];
+              const int64_t sidx = static_cast<int64_t>(t) * k + pj;
+              const uint32_t r = args.comb_inv[sidx];
+              inval = r >= args.rows_total;
+              rows[p] = inval ? 0u : r;
+              wts[p] = comb_weight(args.comb_w, args.comb_wdt, sidx);
+            }
+#pragma unroll
+            for (int i = 0; i < P; ++i) bad[i] |= __any_sync(FULL_MASK, inval && pi == i);
+          }
+          __syncwarp();
+          comb_tokens<T, P>(n, tok, bad, args, rows, wts, lane);
+          __syncwarp();  // the staged pairs are rewritten by the next pass
+        }
       }
     }
   } else if (GATHER) {
@@ -824,11 +1028,11 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
 // K3 and K4 in one launch (CHAIN): gate/up tiles, then down tiles that wait
 // for their expert's h rows. args carries both stages' sizes, y in out2 and
 // the per-expert ready counters (zero at launch, like the tile counter).
-template <typename T, int TBM, int LOAD>
+template <typename T, int TBM, int LOAD, bool COMB>
 cudaError_t launch_chain(const TcWeights& w, const CUtensorMap& x128, const CUtensorMap& x16,
                          const CUtensorMap& h128, const CUtensorMap& h16, const TcArgs& args, int num_sms,
                          cudaStream_t stream) {
-  auto kern = experts_tc_kernel<T, true, TBM, LOAD, true>;
+  auto kern = experts_tc_kernel<T, true, TBM, LOAD, true, COMB>;
   constexpr int SMEM_BYTES = TcCfg<TBM>::SMEM_BYTES_CHAIN;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -903,10 +1107,19 @@ cudaError_t launch_stage(const TcWeights& w, moe_dtype dtype, bool gate_up, cons
   return launch_one<T, false, 256>(w.down, w.down, t128, t16, args, num_sms, stream, sz);
 }
 
+template <typename T, int TBM, int LOAD>
+cudaError_t launch_chain_comb(const TcWeights& w, const CUtensorMap& x128, const CUtensorMap& x16,
+                              const CUtensorMap& h128, const CUtensorMap& h16, const TcArgs& args, int num_sms,
+                              cudaStream_t stream, bool comb) {
+  if (comb) return launch_chain<T, TBM, LOAD, true>(w, x128, x16, h128, h16, args, num_sms, stream);
+  return launch_chain<T, TBM, LOAD, false>(w, x128, x16, h128, h16, args, num_sms, stream);
+}
+
 template <typename T>
 cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
                         const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H, int64_t I, void* h, void* y,
-                        uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream, const char** why) {
+                        uint32_t* sched, uint32_t* ready, int num_sms, cudaStream_t stream, const char** why,
+                        const TcCombine* comb) {
   uint32_t* status = nullptr;
   cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_moe_device_status);
   if (err != cudaSuccess) return err;
@@ -939,15 +1152,30 @@ cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, con
     args.out_g = cache->g;
     args.out_u = cache->u;
   }
+  if (comb != nullptr) {
+    if (cache != nullptr || comb->T * static_cast<int64_t>(comb->top_k) != rows || comb->top_k < 1 ||
+        comb->top_k > COMB_MAX_K) {
+      *why = "the fused combine needs rows == T * top_k, top_k <= 256 and no training cache";
+      return cudaErrorInvalidValue;
+    }
+    args.comb_inv = comb->inv;
+    args.comb_w = comb->weights;
+    args.comb_wdt = static_cast<int>(comb->weights_dtype);
+    args.comb_k = comb->top_k;
+    args.comb_T = static_cast<uint32_t>(comb->T);
+    args.comb_done = comb->done;
+    args.comb_out = comb->out;
+  }
+  const bool cb = comb != nullptr;
   if (gather != nullptr) {
     args.gx = static_cast<const uint8_t*>(gather->x);
     args.row_src = gather->row_src;
     args.top_k = gather->top_k;
     args.x_rows = static_cast<uint32_t>(gather->x_rows);
-    return launch_chain<T, 32, TOK_GATHER4>(w, x128, x16, h128, h16, args, num_sms, stream);
+    return launch_chain_comb<T, 32, TOK_GATHER4>(w, x128, x16, h128, h16, args, num_sms, stream, cb);
   }
-  if (small) return launch_chain<T, 32, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream);
-  return launch_chain<T, 256, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream);
+  if (small) return launch_chain_comb<T, 32, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream, cb);
+  return launch_chain_comb<T, 256, TOK_DENSE>(w, x128, x16, h128, h16, args, num_sms, stream, cb);
 }
 
 }  // namespace
@@ -955,13 +1183,13 @@ cudaError_t chain_stage(const TcWeights& w, moe_dtype dtype, const void* xd, con
 cudaError_t launch_experts_tc_chain(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
                                     const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H,
                                     int64_t I, void* h, void* y, uint32_t* sched, uint32_t* ready, int num_sms,
-                                    cudaStream_t stream, const char** why) {
+                                    cudaStream_t stream, const char** why, const TcCombine* comb) {
   if (rows == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
     return chain_stage<__nv_bfloat16>(w, dtype, xd, gather, cache, offsets, E, rows, H, I, h, y, sched, ready,
-                                      num_sms, stream, why);
+                                      num_sms, stream, why, comb);
   return chain_stage<__half>(w, dtype, xd, gather, cache, offsets, E, rows, H, I, h, y, sched, ready, num_sms,
-                             stream, why);
+                             stream, why, comb);
 }
 
 bool tc_encode_weights(const void* gate, const void* up, const void* down, moe_dtype dtype,

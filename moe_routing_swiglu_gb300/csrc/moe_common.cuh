@@ -261,6 +261,16 @@ __device__ __forceinline__ void counter_release_add(uint32_t* ctr) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
+// Adds one to the device counter *ctr with acquire-release semantics at GPU
+// scope and returns the value it held: stores the caller made (or observed)
+// before the add are visible to whoever later reads the counter, and stores
+// that earlier adders released are visible to the caller after it.
+__device__ __forceinline__ uint32_t counter_acq_rel_add(uint32_t* ctr) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- TMA (bulk tensor copies)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {

@@ -61,12 +61,13 @@ size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k);
 // the current device (set up on first use per device).
 constexpr size_t NOALLOC_DISPATCH_SCRATCH_BYTES = size_t{1} << 20;
 cudaError_t noalloc_dispatch_scratch(void** ptr);
-// zero_words (optional): n_zero uint32 the scatter kernel sets to 0
-// (moe_forward's GEMM tile and ready counters, so the GEMMs need no memset).
+// zero_words (optional, 16-byte aligned): n_zero uint32 the scatter kernel
+// sets to 0 (moe_forward's GEMM tile and ready counters, so the GEMMs need
+// no memset).
 cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k, const void* x,
                             moe_dtype dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                            cudaStream_t stream, uint32_t* zero_words = nullptr, int n_zero = 0);
+                            cudaStream_t stream, uint32_t* zero_words = nullptr, int64_t n_zero = 0);
 
 // ---- K5 combine (combine.cu)
 cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
@@ -110,15 +111,33 @@ cudaError_t launch_experts_tc(const TcWeights& w, moe_dtype dtype, bool gate_up,
                               const TcGather* gather, const TcCache* cache, const uint32_t* offsets, int E,
                               int64_t rows, int64_t H, int64_t I, void* out, uint32_t* sched, int num_sms,
                               cudaStream_t stream, const char** why, bool sched_zeroed = false);
+// Fused combine of the chained launch: once every down tile has stored its
+// y rows (one done counter), the epilogue warps of all CTAs write
+// out[t] = sum_j w[t, j] * y[inv[t*top_k + j]] (FP32, slot order), each warp
+// a fixed stripe of the tokens.
+struct TcCombine {
+  const uint32_t* inv;      // [T * top_k] flat slot -> dispatched row (from the dispatch)
+  const void* weights;      // [T, top_k], weights_dtype
+  moe_dtype weights_dtype;
+  int top_k;                // 1 .. COMB_MAX_TOP_K
+  int64_t T;
+  uint32_t* done;           // [1] counter, zero on the stream before the launch
+  void* out;                // [T, H]
+};
+// Largest top_k of the fused combine (a warp stages the (row, weight) pairs
+// of four tokens in its 2 KB shared buffer); larger top_k combine in their
+// own launch.
+constexpr int COMB_MAX_TOP_K = 64;
 // K3 and K4 in one launch (moe_forward): gate/up tiles (x_dispatched, or x
 // gathered through row_src for decode-sized batches -> h), then down tiles
 // (h -> y), each waiting for its expert's h rows. sched[0] and ready[0..E)
 // must be zero on the stream before the launch (the dispatch zeroes them).
 // cache (optional): the gate/up tiles also store the pre-activations g, u.
+// comb (optional): the fused combine (y is still written, in dispatched order).
 cudaError_t launch_experts_tc_chain(const TcWeights& w, moe_dtype dtype, const void* xd, const TcGather* gather,
                                     const TcCache* cache, const uint32_t* offsets, int E, int64_t rows, int64_t H,
                                     int64_t I, void* h, void* y, uint32_t* sched, uint32_t* ready, int num_sms,
-                                    cudaStream_t stream, const char** why);
+                                    cudaStream_t stream, const char** why, const TcCombine* comb = nullptr);
 cudaError_t read_device_status(uint32_t* code, bool clear);
 // Device address of the status word the bounded waits report into.
 cudaError_t device_status_ptr(uint32_t** p);

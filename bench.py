@@ -4,32 +4,31 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step is one pass of the whole chain over one batch of the BF16
-fine-grained prefill workload (T=4096, H=2048, I=768, E=128, top_k=8,
-renormalize), inputs resident in HBM. One moe_forward call is captured once
-in a CUDA graph; each timed step is one replay bracketed by CUDA events on
-the launching stream, and L2 is flushed between steps outside the events
-(a 256 MiB write, then a 256 MiB read so the flush's dirty lines are written
-back before the step). The per-stage times come from a second run that
-launches the split C-ABI calls (route, dispatch, gate/up, down, combine)
-directly with events between the stages. Under torchrun each
-rank runs its own batch (weak scaling, replicated experts, no collective on
+One step is one pass of the whole chain over one batch of the coarse BF16
+prefill workload (T=8192, H=4096, I=14336, E=8, top_k=2, renormalize; the
+GEMM-bound case and the largest one that fits one GPU), inputs resident in
+HBM. One moe_forward call is captured once in a CUDA graph; each timed step is
+one replay bracketed by CUDA events on the launching stream, and L2 is
+flushed between steps outside the events (a 256 MiB write, then a 256 MiB
+read so the flush's dirty lines are written back before the step). The
+per-stage times come from a second run that launches the C-ABI stage calls
+(route, dispatch, the experts' GEMMs, combine) directly with events between
+the stages. Under torchrun each rank runs its own T-token shard of an
+N*T-token global batch (weak scaling, replicated experts, no collective on
 the data path); the time is the maximum over ranks.
 
 Printed (rank 0, one JSON line): tokens/s, grouped-GEMM TFLOP/s against the
-measured BF16 peak, route+dispatch microseconds, the decode workload's HBM
-GB/s over the touched expert weights, the roofline of the dominant kernel,
-the end-to-end number through moe_forward with host buffers, the CPU oracle
-baseline, kernel launches and the SM clocks seen during the run, and the
-grouped-GEMM TFLOP/s of the coarse BF16 and Zipf-skewed F16 prefill
-workloads (the two GEMM stages timed on their own), and one first-order
-training step (forward with the experts' cache, then combine, experts,
-dispatch and router backward) on the prefill workload. A second,
-shorter run of the same chain with the grouped sigmoid routing in place of
-the softmax routing reports its tokens/s and routing time.
+measured BF16 peak, route+dispatch microseconds, the roofline of the dominant
+kernel (the experts' GEMMs), the end-to-end number through moe_forward_host
+with host buffers (two streams pipelined, and one batch at a time), the CPU
+oracle baseline, kernel launches and the SM clocks seen during the run; then,
+as extra keys, the fine-grained BF16 prefill (T=4096, E=128, top_k=8) step
+with its GEMM roofline, the decode workload's HBM GB/s over the touched
+expert weights, the Zipf-skewed F16 prefill's GEMMs, the grouped sigmoid
+routing on the fine-grained prefill, and one first-order training step there.
 
 --impl reference times the CPU oracle (the only reference this path has) on
-bounded samples of the same workload.
+bounded samples of the headline workload.
 """
 from __future__ import annotations
 
@@ -53,8 +52,10 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "MoE fwd tokens/s + grouped-GEMM TFLOP/s vs bf16 peak; decode HBM GB/s"
-PREFILL = workloads.CONFIGS[2]
-DECODE = workloads.CONFIGS[4]
+HEADLINE = workloads.CONFIGS[2]  # coarse BF16 prefill
+FINE = workloads.CONFIGS[1]      # fine-grained BF16 prefill
+DECODE = workloads.CONFIGS[3]
+ZIPF = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 6  # route, dispatch count + scatter + gather, gate/up + down GEMMs (one launch), combine
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -87,7 +88,8 @@ def workload_config(cfg, n_gpus):
     return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
             "renormalize": cfg.renormalize, "tokens_per_gpu": cfg.T,
             "global_batch_tokens": cfg.T * n_gpus,
-            "parallelism": f"dp{n_gpus} (tokens split across GPUs, experts replicated)",
+            "parallelism": f"dp{n_gpus}: each rank runs its own {cfg.T}-token shard of a {cfg.T * n_gpus}-token "
+                           "global batch (rank-seeded tokens), experts replicated, no collective on the data path",
             "l2": "flushed between timed steps (256 MiB write, then a 256 MiB read so the written lines "
                   "are written back before the step)"}
 
@@ -159,9 +161,9 @@ class ClockSampler:
 class Chain:
     """Pre-allocated buffers and the raw C-ABI calls of one forward step."""
 
-    def __init__(self, moe, cfg, dev):
+    def __init__(self, moe, cfg, dev, shard=0):
         self.moe, self.lib, self.cfg, self.dev = moe, moe.load_library(), cfg, dev
-        inp = workloads.generate(cfg)
+        inp = workloads.generate(cfg, shard=shard)
         self.host = inp
         d = {k: v.to(dev) for k, v in inp.items()}
         self.d = d
@@ -186,6 +188,11 @@ class Chain:
         self.fws = torch.empty(max(1, self.lib.moe_forward_workspace_size(self.ex.handle, T, k)),
                                dtype=torch.uint8, **e)
         self.sws = torch.empty(moe.STAGE_WORKSPACE_BYTES, dtype=torch.uint8, **e)
+        self.cws = torch.empty(max(1, self.lib.moe_experts_forward_combine_workspace_size(self.ex.handle, T, k)),
+                               dtype=torch.uint8, **e)
+        self.uws = torch.empty(max(1, self.lib.moe_experts_forward_dispatched_workspace_size(self.ex.handle, n)),
+                               dtype=torch.uint8, **e)
+        self.fused = False  # prefill staged run: True = the experts and the combine in one launch
         self.dt = moe._dt(d["x"])
         self.grouped = None  # (bias device tensor or None, GroupRoutingOptions) to route by sigmoid groups
 
@@ -198,9 +205,14 @@ class Chain:
         self.grouped = (None if bias is None else bias.to(self.dev), opts)
 
     def step(self, stream, ev=None):
-        """route | dispatch | gate/up GEMM | down GEMM | combine, events between:
-        the calls moe_forward makes (x rows gathered in the gate/up GEMM for
-        decode-sized batches, else through x_dispatched)."""
+        """route | dispatch | experts | combine, events between: the calls
+        moe_forward makes. Prefill: the chained gate/up + down launch over
+        x_dispatched (moe_experts_forward_dispatched, the kernel moe_forward
+        runs), then moe_combine; with self.fused, the experts and the
+        combine in one launch (moe_experts_forward_combine; the combine
+        stage is then empty). Decode-sized batches: x rows gathered in the
+        gate/up GEMM (moe_experts_gate_up_gather), then moe_experts_down and
+        moe_combine."""
         c, lib, P = self.cfg, self.lib, self.moe._ptr
         s = ctypes.c_void_p(stream.cuda_stream)
         T, k, E, H = c.T, c.top_k, c.E, c.H
@@ -221,19 +233,24 @@ class Chain:
             rec(2)
             rc |= lib.moe_experts_gate_up_gather(self.ex.handle, P(self.d["x"]), T, P(self.row_src), k,
                                                  P(self.offsets), T * k, P(self.h), P(self.sws), self.sws.numel(), s)
+            rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), P(self.sws),
+                                       self.sws.numel(), s)
         else:
             rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts),
                                    P(self.offsets), P(self.row_src), P(self.inv), P(self.xd), P(self.dws),
                                    self.dws.numel(), s)
             rec(2)
-            rc |= lib.moe_experts_gate_up(self.ex.handle, P(self.xd), P(self.offsets), T * k, P(self.h),
-                                          P(self.sws), self.sws.numel(), s)
+            if self.fused:
+                rc |= lib.moe_experts_forward_combine(self.ex.handle, P(self.xd), P(self.offsets), P(self.inv),
+                                                      P(self.w), self.dt, T, k, P(self.out), P(self.cws),
+                                                      self.cws.numel(), s)
+            else:
+                rc |= lib.moe_experts_forward_dispatched(self.ex.handle, P(self.xd), P(self.offsets), T * k,
+                                                         P(self.yd), P(self.uws), self.uws.numel(), s)
         rec(3)
-        rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), P(self.sws),
-                                   self.sws.numel(), s)
+        if self.gather or not self.fused:
+            rc |= lib.moe_combine(P(self.yd), self.dt, P(self.inv), P(self.w), self.dt, T, k, H, P(self.out), s)
         rec(4)
-        rc |= lib.moe_combine(P(self.yd), self.dt, P(self.inv), P(self.w), self.dt, T, k, H, P(self.out), s)
-        rec(5)
         if rc:
             raise RuntimeError("a C-ABI call failed: " + lib.moe_last_error().decode())
 
@@ -248,6 +265,16 @@ class Chain:
 
     def touched_experts(self) -> int:
         return int((self.counts.cpu() > 0).sum())
+
+    def free(self):
+        """Drop the device buffers (the next workload's chain needs the room)."""
+        for name in list(vars(self)):
+            if isinstance(getattr(self, name), torch.Tensor) or name in ("d", "ex", "host"):
+                setattr(self, name, None)
+        torch.cuda.empty_cache()
+
+
+N_STAGES = 4  # route | dispatch | experts | combine
 
 
 class L2Flush:
@@ -272,13 +299,14 @@ def timed_steps(chain, stream, flush, steps, warmup):
         flush()
         chain.step(stream)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(N_STAGES + 1)] for _ in range(steps)]
     for i in range(steps):
         flush()
         chain.step(stream, evs[i])
     torch.cuda.synchronize()
-    stages = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(steps)]) / 1e3
-    total = float(sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(steps))) / 1e3
+    stages = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(N_STAGES)]
+                       for i in range(steps)]) / 1e3
+    total = float(sum(evs[i][0].elapsed_time(evs[i][N_STAGES]) for i in range(steps))) / 1e3
     return stages.mean(axis=0), total
 
 
@@ -379,15 +407,17 @@ def e2e_pipelined(chain, steps):
     return max(start.elapsed_time(e) for e in ends) / 1e3 / steps
 
 
-def traffic_record(kernel_source: Path):
-    """ncu DRAM bytes per launch of the dominant kernel, if they were taken on
-    the current kernel source (else None)."""
+def traffic_record(kernel_source: Path, workload: str):
+    """ncu DRAM bytes per launch of the dominant kernel on one workload, if
+    they were taken on the current kernel source (else None)."""
     p = ROOT / "profiles" / "ncu_traffic.json"
     if not p.exists():
         return None
     rec = json.loads(p.read_text())
     sha = hashlib.sha256(kernel_source.read_bytes()).hexdigest()
-    return rec if rec.get("source_sha256") == sha else None
+    if rec.get("source_sha256") != sha:
+        return None
+    return rec.get("workloads", {}).get(workload)
 
 
 def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
@@ -483,27 +513,99 @@ def training_step_times(moe, cfg, dev, stream, flush, steps):
 def widened_weights(inp):
     """The expert weights as f64 CPU tensors: exact copies of the dtype values
     (the oracle computes the experts in f64), made once so that a timed oracle
-    call does not convert the 1.2 GB of weights again."""
+    call does not convert the expert weights again."""
     return {k: inp[k].to(torch.float64) for k in ("gate", "up", "down")}
 
 
-def cpu_baseline_prefill(inp, n_tokens=PREFILL.T):
-    """The oracle, as it stands, on the first n_tokens of the prefill batch
-    (by default the whole batch: a few seconds of CPU work on the host); the
-    weights are widened to f64 before the timed call."""
+def cpu_baseline(cfg, inp, target_s=15.0):
+    """The oracle, as it stands, on the first n tokens of the batch, n sized
+    from a 256-token probe (after a 32-token warm-up call) so that the timed
+    call takes about ``target_s`` seconds of CPU work; the weights are
+    widened to f64 before the timed calls."""
     from oracle import moe_oracle
 
-    c = PREFILL
     w64 = widened_weights(inp)
-    t0 = time.perf_counter()
-    moe_oracle.forward(inp["x"][:n_tokens], inp["logits"][:n_tokens], w64["gate"], w64["up"], w64["down"],
-                       c.top_k, c.renormalize)
-    dt = time.perf_counter() - t0
-    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+
+    def run(n):
+        t0 = time.perf_counter()
+        moe_oracle.forward(inp["x"][:n], inp["logits"][:n], w64["gate"], w64["up"], w64["down"],
+                           cfg.top_k, cfg.renormalize)
+        return time.perf_counter() - t0
+
+    run(min(32, cfg.T))
+    probe = min(256, cfg.T)
+    t_probe = run(probe)
+    n = int(min(cfg.T, max(probe, (target_s / max(t_probe, 1e-6)) * probe)))
+    n = max(probe, (n // 32) * 32) if n < cfg.T else cfg.T
+    dt = run(n)
+    return {"value": n / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": f"{n_tokens} of {c.T} tokens of {c.name} (one batch): FP32 routing, dispatch, "
-                      f"f64 SwiGLU experts and combine, {dt:.1f} s (expert weights widened to f64 once, "
-                      "before the timed call)"}
+            "sample": f"the first {n} of {cfg.T} tokens of {cfg.name} (one call, sized from a {probe}-token probe "
+                      f"of {t_probe:.2f} s): FP32 routing, dispatch, f64 SwiGLU experts and combine, {dt:.1f} s "
+                      "(expert weights widened to f64 once, before the timed call)"}
+
+
+def gemm_roofline(cfg, t_chain, touched, peaks, peaks_src, traffic, timing):
+    """Roofline of the chained gate/up + down launch on one workload.
+    Algorithmic work per launch (the method's, not the kernel's): flops
+    6*T*k*H*I; bytes = the touched experts' gate, up and down weights, x read
+    once and the output written once (T*H each)."""
+    es = 2
+    flops = cfg.expert_flops
+    nbytes = touched * 3 * cfg.I * cfg.H * es + 2 * cfg.T * cfg.H * es
+    tflops = flops / t_chain / 1e12
+    gbs = nbytes / t_chain / 1e9
+    bound = "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
+    dram = traffic["dram_bytes_per_launch"] if traffic else None
+    return {"kernel": "experts_tc_kernel, chained gate/up + SwiGLU and down (K3 + K4), one launch",
+            "workload": cfg.name, "bound": bound,
+            "achieved": round(gbs if bound == "hbm" else tflops, 2),
+            "peak": peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": round(gbs / peaks["hbm_gbs"] if bound == "hbm" else tflops / peaks["bf16_tflops"], 4),
+            "traffic": dram, "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "traffic_over_algorithmic": round(dram / nbytes, 4) if dram else None,
+            "us": round(t_chain * 1e6, 2), "tflops": round(tflops, 1),
+            "tensor_frac": round(tflops / peaks["bf16_tflops"], 4),
+            "tensor_frac_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peaks_src, "timing": timing}
+
+
+def forward_measure(moe, cfg, dev, stream, flush, steps, warmup, world, shard=0, stage_steps=None):
+    """The whole chain on one workload: CUDA-graph replays of one moe_forward
+    call (tokens/s, max over ranks), then the staged run (route | dispatch |
+    experts | combine with events between), and for prefill the same staged
+    run with the experts and the combine in one launch
+    (moe_experts_forward_combine: an A/B of the fused combine). Returns
+    (chain, result dict)."""
+    chain = Chain(moe, cfg, dev, shard=shard)
+    graph = capture_step(chain)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
+    total = timed_graph_steps(graph, stream, flush, steps, warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total = max_over_ranks(total, world, dev)
+    del graph
+    n_stage = stage_steps or min(steps, 200)
+    stages, stage_total = timed_steps(chain, stream, flush, n_stage, warmup)
+    stages = [float(x) for x in stages]
+    fused = None
+    if not chain.gather:
+        chain.fused = True
+        f_stages, f_total = timed_steps(chain, stream, flush, n_stage, warmup)
+        chain.fused = False
+        fused = {"fused_experts_combine_us": round(float(f_stages[2]) * 1e6, 2),
+                 "experts_us": round(stages[2] * 1e6, 2), "combine_us": round(stages[3] * 1e6, 2),
+                 "experts_plus_combine_us": round((stages[2] + stages[3]) * 1e6, 2),
+                 "fused_staged_step_us": round(f_total / n_stage * 1e6, 2),
+                 "staged_step_us": round(stage_total / n_stage * 1e6, 2)}
+    return chain, {"total_s": total, "steps": steps, "stages_s": stages, "stage_steps": n_stage,
+                   "stage_total_s": stage_total, "touched": chain.touched_experts(), "fused_ab": fused}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -524,135 +626,95 @@ def run_ours(args, rank, world, local_rank):
     peaks, peaks_src = load_peaks()
     stream = torch.cuda.current_stream()
     flush = L2Flush(dev)
-
-    chain = Chain(moe, PREFILL, dev)
-    decode = Chain(moe, DECODE, dev)
-    graph = capture_step(chain)
-    torch.cuda.synchronize()
-
+    kernel_src = ROOT / "moe_routing_swiglu_gb300" / "csrc" / "experts_tc.cu"
     clocks = ClockSampler(local_rank)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    total = timed_graph_steps(graph, stream, flush, args.steps, args.warmup)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    total = max_over_ranks(total, world, dev)
-    stage_steps = min(args.steps, 200)
-    stages, stage_total = timed_steps(chain, stream, flush, stage_steps, args.warmup)
+
+    # ---- headline: the coarse BF16 prefill, this rank's token shard
+    c = HEADLINE
+    chain, hr = forward_measure(moe, c, dev, stream, flush, args.steps, args.warmup, world, shard=rank)
+    t_exp = hr["stages_s"][2]
     e2e_serial_s, h2d, d2h = e2e_steps(chain, stream, flush, min(args.steps, 20))
     e2e_serial_s = max_over_ranks(e2e_serial_s, world, dev)
-    e2e_steps_n = min(args.steps, 200)
+    e2e_steps_n = min(args.steps, 100)
     if world > 1:
         dist.barrier()
     e2e_s = max_over_ranks(e2e_pipelined(chain, e2e_steps_n), world, dev)
-    dec_stages, dec_total = timed_steps(decode, stream, flush, min(args.steps, 50), args.warmup)
-    dec_graph = capture_step(decode)
-    dec_graph_total = timed_graph_steps(dec_graph, stream, flush, min(args.steps, 200), args.warmup)
+    host_inp = chain.host if rank == 0 and world == 1 else None
+    chain.free()
+    del chain
+    t_gu, t_dn, _ = gemm_stage_times(moe, c, dev, stream, flush, 5)
+
+    # ---- fine-grained BF16 prefill (E=128, top_k=8): step, GEMM roofline, grouped routing, training
+    f = FINE
+    fchain, fr = forward_measure(moe, f, dev, stream, flush, min(args.steps, 1000), args.warmup, world)
     grouped_cfg, grouped_routing = workloads.GROUPED["bf16_prefill_grouped"]
-    assert grouped_cfg is PREFILL
-    chain.use_grouped_routing(grouped_routing)
+    assert grouped_cfg is FINE
+    fchain.use_grouped_routing(grouped_routing)
     g_steps = min(args.steps, 200)
-    g_stages, g_total = timed_steps(chain, stream, flush, g_steps, args.warmup)
+    g_stages, g_total = timed_steps(fchain, stream, flush, g_steps, args.warmup)
     g_total = max_over_ranks(g_total, world, dev)
-    tr = training_step_times(moe, PREFILL, dev, stream, flush, 5)
-    bwd_flops = 2 * PREFILL.expert_flops  # dgrad + wgrad: twice the forward's 6*T*k*H*I
-    training = {"workload": PREFILL.name, "us_per_step": round(sum(tr) * 1e6, 1),
-                "tokens_per_s": round(world * PREFILL.T / sum(tr), 1),
+    fchain.free()
+    del fchain
+    f_gu, f_dn, _ = gemm_stage_times(moe, f, dev, stream, flush, 5)
+    tr = training_step_times(moe, f, dev, stream, flush, 5)
+
+    # ---- decode
+    dchain, dr = forward_measure(moe, DECODE, dev, stream, flush, min(args.steps, 1000), args.warmup, world,
+                                 stage_steps=min(args.steps, 50))
+    dchain.free()
+    del dchain
+
+    # ---- Zipf-skewed F16 prefill: the expert GEMMs
+    z_gu, z_dn, z_ch = gemm_stage_times(moe, ZIPF, dev, stream, flush, 5)
+    clk = clocks.stop()
+    assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
+
+    ms_per_step = hr["total_s"] / args.steps * 1e3
+    tokens_per_s = world * c.T * args.steps / hr["total_s"]
+    stage_note = ("the staged run's experts stage: the chained gate/up + down launch "
+                  "(moe_experts_forward_dispatched, the kernel moe_forward runs), CUDA events on the launching "
+                  "stream around it in each of {n} steps, L2 flushed before each step")
+    roof = gemm_roofline(c, t_exp, hr["touched"], peaks, peaks_src, traffic_record(kernel_src, c.name),
+                         stage_note.format(n=hr["stage_steps"]))
+    froof = gemm_roofline(f, fr["stages_s"][2], fr["touched"], peaks, peaks_src, traffic_record(kernel_src, f.name),
+                          stage_note.format(n=fr["stage_steps"]))
+    bwd_flops = 2 * f.expert_flops  # dgrad + wgrad: twice the forward's 6*T*k*H*I
+    training = {"workload": f.name, "us_per_step": round(sum(tr) * 1e6, 1),
+                "tokens_per_s": round(world * f.T / sum(tr), 1),
                 "forward_us": round(tr[0] * 1e6, 1), "combine_backward_us": round(tr[1] * 1e6, 1),
                 "experts_backward_us": round(tr[2] * 1e6, 1), "dispatch_backward_us": round(tr[3] * 1e6, 1),
                 "router_backward_us": round(tr[4] * 1e6, 1),
                 "experts_backward_tflops": round(bwd_flops / tr[2] / 1e12, 1),
                 "experts_backward_frac_bf16_peak": round(bwd_flops / tr[2] / 1e12 / peaks["bf16_tflops"], 4)}
-    # The chained gate/up + down launch on the prefill workload, on its own.
-    _, _, t_chain = gemm_stage_times(moe, PREFILL, dev, stream, flush, 20)
-    other_gemms = {}
-    for cid in (3, 5):
-        oc = workloads.CONFIGS[cid]
-        t_g, t_d, t_c = gemm_stage_times(moe, oc, dev, stream, flush, 5)
-        tf = oc.expert_flops / t_c / 1e12
-        peak = peaks["bf16_tflops"]  # F16 and BF16 share the dense tensor rate
-        other_gemms[oc.name] = {"tflops": round(tf, 1), "frac_peak": round(tf / peak, 4),
-                                "chained_us": round(t_c * 1e6, 1), "gate_up_us": round(t_g * 1e6, 1),
-                                "down_us": round(t_d * 1e6, 1), "flops": oc.expert_flops}
-    clk = clocks.stop()
-    assert moe.moe_device_status() == 0, "a device-side wait timed out during the benchmark"
-
-    c = PREFILL
-    ms_per_step = total / args.steps * 1e3
-    tokens_per_s = world * c.T * args.steps / total
-    t_route, t_disp, t_gu, t_down, t_comb = [float(x) for x in stages]
-    es = 2
-    gemm_flops = c.expert_flops
-    gemm_tflops = gemm_flops / t_chain / 1e12
-    touched = chain.touched_experts()
-    # Dominant kernel: the chained gate/up + down launch (K3 + K4). Its
-    # algorithmic work per launch: the touched gate, up and down weights, x
-    # rows read through x_dispatched, h written and read back, y written.
-    k_flops = gemm_flops
-    k3_bytes = touched * 2 * c.I * c.H * es + c.T * c.H * es + c.T * c.top_k * c.I * es
-    k4_bytes = touched * c.H * c.I * es + c.T * c.top_k * c.I * es + c.T * c.top_k * c.H * es
-    k_bytes = k3_bytes + k4_bytes
-    k_tflops = k_flops / t_chain / 1e12
-    k_gbs = k_bytes / t_chain / 1e9
-    t_floor_tensor = k_flops / (peaks["bf16_tflops"] * 1e12)
-    t_floor_hbm = k_bytes / (peaks["hbm_gbs"] * 1e9)
-    bound = "hbm" if t_floor_hbm >= t_floor_tensor else "tensor"
-    traffic = traffic_record(ROOT / "moe_routing_swiglu_gb300" / "csrc" / "experts_tc.cu")
-    roof = {"kernel": "experts_tc_kernel<bf16, chained gate/up + SwiGLU and down> (K3 + K4)", "bound": bound,
-            "achieved": round(k_gbs if bound == "hbm" else k_tflops, 2),
-            "peak": peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"],
-            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-            "frac": round((k_gbs / peaks["hbm_gbs"]) if bound == "hbm" else (k_tflops / peaks["bf16_tflops"]), 4),
-            "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-            "algorithmic_bytes": k_bytes, "algorithmic_flops": k_flops, "us": round(t_chain * 1e6, 2),
-            "tensor_frac": round(k_tflops / peaks["bf16_tflops"], 4),
-            "hbm_frac": round(k_gbs / peaks["hbm_gbs"], 4), "peak_source": peaks_src,
-            "timing": "mean of 20 launches of moe_experts_forward_dispatched (the chained kernel alone), "
-                      "CUDA events, L2 flushed before each"}
-
     d = DECODE
-    dec_touched = decode.touched_experts()
-    dec_bytes = dec_touched * 3 * d.I * d.H * es
-    dec_fwd = float(dec_graph_total) / min(args.steps, 200)
-    dec_exp = float(dec_stages[2] + dec_stages[3])
+    es = 2
+    dec_bytes = dr["touched"] * 3 * d.I * d.H * es
+    dec_fwd = dr["total_s"] / dr["steps"]
+    dec_exp = dr["stages_s"][2]
+    ztf = ZIPF.expert_flops / z_ch / 1e12
+
+    def route_dispatch(st):
+        return {"route": round(st[0] * 1e6, 2), "dispatch": round(st[1] * 1e6, 2),
+                "total": round((st[0] + st[1]) * 1e6, 2)}
+
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) logits and x, N(0, 1/sqrt(fan_in)) expert weights (random init)",
         "config": workload_config(c, world),
-        "grouped_gemm": {"tflops": round(gemm_tflops, 2), "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
-                         "frac_bf16_sustained": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
-                         "flops_per_step": gemm_flops, "chained_us": round(t_chain * 1e6, 2),
-                         "split_gate_up_us": round(t_gu * 1e6, 2), "split_down_us": round(t_down * 1e6, 2)},
-        "route_dispatch_us": {"route": round(t_route * 1e6, 2), "dispatch": round(t_disp * 1e6, 2),
-                              "total": round((t_route + t_disp) * 1e6, 2)},
-        "combine_us": round(t_comb * 1e6, 2),
+        "grouped_gemm": {"tflops": roof["tflops"], "frac_bf16_peak": roof["tensor_frac"],
+                         "frac_bf16_sustained": roof["tensor_frac_sustained"], "flops_per_step": c.expert_flops,
+                         "chained_us": roof["us"], "gate_up_alone_us": round(t_gu * 1e6, 2),
+                         "down_alone_us": round(t_dn * 1e6, 2)},
+        "route_dispatch_us": route_dispatch(hr["stages_s"]),
+        "combine_us": round(hr["stages_s"][3] * 1e6, 2),
+        "fused_combine_ab": hr["fused_ab"],
         "timing": {"value": f"{args.steps} CUDA-graph replays of one moe_forward call (its {KERNELS_PER_STEP} "
                             "kernels), one event pair around each replay",
-                   "stages": f"{stage_steps} steps launched directly with events between the stages "
-                             f"({stage_total / stage_steps * 1e6:.1f} us per step including the events)"},
-        "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
-                   "timing": "CUDA-graph replays of the decode step (forward, gate/up and down chained in one "
-                             "launch); experts_us from the staged run (the two GEMMs launched apart)",
-                   "frac_hbm_forward": round(dec_bytes / dec_fwd / 1e9 / peaks["hbm_gbs"], 4),
-                   "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dec_touched,
-                   "touched_weight_bytes": dec_bytes,
-                   "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),
-                   "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
-                   "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
-        "grouped_gemm_other_workloads": other_gemms,
-        "training_step": training,
-        "sigmoid_grouped": {
-            "workload": f"{c.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
-                        f"{grouped_routing.selected_groups} selected, top-two group scores, scale "
-                        f"{grouped_routing.scale}, FP32 bias N(0, {grouped_routing.bias_std}^2)",
-            "tokens_per_s": round(world * c.T * g_steps / g_total, 1),
-            "us_per_step": round(g_total / g_steps * 1e6, 2),
-            "route_us": round(float(g_stages[0]) * 1e6, 2),
-            "softmax_route_us": round(t_route * 1e6, 2)},
+                   "stages": f"{hr['stage_steps']} steps launched stage by stage with events between "
+                             f"({hr['stage_total_s'] / hr['stage_steps'] * 1e6:.1f} us per step including the "
+                             "events)"},
         "roofline": roof,
         "e2e": {"value": round(world * c.T / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "moe_forward_host (C ABI, pinned host buffers)",
@@ -661,14 +723,46 @@ def run_ours(args, rank, world, local_rank):
                           "batches; from an event before the first batch to the last batch's end",
                 "serial": {"value": round(world * c.T / e2e_serial_s, 1), "unit": "tokens/s",
                            "timing": "one batch at a time (copy in, chain, copy out, wait), L2 flushed before "
-                                     "each, outside the events"}},
+                                     "each, outside the events; the cost of one call"}},
+        "fine_prefill": {
+            "workload": f.name, "tokens_per_s": round(world * f.T * fr["steps"] / fr["total_s"], 1),
+            "us_per_step": round(fr["total_s"] / fr["steps"] * 1e6, 2),
+            "route_dispatch_us": route_dispatch(fr["stages_s"]),
+            "experts_us": round(fr["stages_s"][2] * 1e6, 2), "combine_us": round(fr["stages_s"][3] * 1e6, 2),
+            "fused_combine_ab": fr["fused_ab"],
+            "gate_up_alone_us": round(f_gu * 1e6, 2), "down_alone_us": round(f_dn * 1e6, 2),
+            "roofline": froof},
+        "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
+                   "timing": "CUDA-graph replays of the decode step (forward, gate/up and down chained in one "
+                             "launch); experts_us from the staged run (the two GEMMs launched apart)",
+                   "route_dispatch_us": route_dispatch(dr["stages_s"]),
+                   "frac_hbm_forward": round(dec_bytes / dec_fwd / 1e9 / peaks["hbm_gbs"], 4),
+                   "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dr["touched"],
+                   "touched_weight_bytes": dec_bytes,
+                   "gbs_over_forward": round(dec_bytes / dec_fwd / 1e9, 1),
+                   "gbs_over_experts": round(dec_bytes / dec_exp / 1e9, 1),
+                   "frac_hbm_experts": round(dec_bytes / dec_exp / 1e9 / peaks["hbm_gbs"], 4)},
+        "zipf_prefill_gemms": {"workload": ZIPF.name, "tflops": round(ztf, 1),
+                               "frac_peak": round(ztf / peaks["bf16_tflops"], 4),
+                               "chained_us": round(z_ch * 1e6, 1), "gate_up_alone_us": round(z_gu * 1e6, 1),
+                               "down_alone_us": round(z_dn * 1e6, 1), "flops": ZIPF.expert_flops,
+                               "note": "F16 and BF16 share the dense tensor rate"},
+        "training_step": training,
+        "sigmoid_grouped": {
+            "workload": f"{f.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
+                        f"{grouped_routing.selected_groups} selected, top-two group scores, scale "
+                        f"{grouped_routing.scale}, FP32 bias N(0, {grouped_routing.bias_std}^2)",
+            "tokens_per_s": round(world * f.T * g_steps / g_total, 1),
+            "us_per_step": round(g_total / g_steps * 1e6, 2),
+            "route_us": round(float(g_stages[0]) * 1e6, 2),
+            "softmax_route_us": round(fr["stages_s"][0] * 1e6, 2)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }
     if world > 1:
         dist.barrier()
-    if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline_prefill(chain.host)
+    if host_inp is not None:
+        line["cpu_baseline"] = cpu_baseline(c, host_inp)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -678,12 +772,12 @@ def run_ours(args, rank, world, local_rank):
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
-    """The CPU oracle on bounded samples of the prefill batch (rank 0 only)."""
+    """The CPU oracle on bounded samples of the headline batch (rank 0 only)."""
     if rank != 0:
         return
     from oracle import moe_oracle
 
-    c = PREFILL
+    c = HEADLINE
     n_tok = 32
     inp = workloads.generate(c)
     w64 = widened_weights(inp)

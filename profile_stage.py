@@ -1,12 +1,19 @@
 """Run one stage of the MoE chain a few times on one workload, for profilers.
 
-    python -m moe_routing_swiglu_gb300.profile_stage --workload cfg2 --stage gate_up --reps 3
+    python profile_stage.py --workload cfg1 --stage gate_up --reps 3
 
-The inputs are the seeded synthetic workloads of ``workloads.py``; routing and
+Workloads: cfg0..cfg4 (the five configurations, numbered from 0: F32
+routing contract, fine-grained BF16 prefill, coarse BF16 prefill, BF16
+decode, Zipf-skewed F16 prefill), a reduced workload's name, or
+coarse_E2 (the coarse prefill's expert shape, H=4096, I=14336 and 2048 rows
+per expert, on 2 experts and 2048 tokens: the same kernel on 0.9 GB instead
+of 3.7 GB, for captures that replay a launch many times). The inputs
+are the seeded synthetic workloads of ``workloads.py``; routing and
 dispatch run once to set up the stage's inputs, then the chosen stage runs
 ``--reps`` times back to back (stream-ordered) and the device is synchronised.
 Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
-row_src), down, experts (gate/up and down chained in one launch, as
+row_src), down, experts (gate/up and down chained in one launch),
+experts_combine (gate/up, down and the weighted combine in one launch, as
 moe_forward runs them), combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
 variant in ``workloads.GROUPED``), backward (the experts' backward of
@@ -21,7 +28,7 @@ from pathlib import Path
 
 import torch
 
-ROOT = Path(__file__).resolve().parents[1]
+ROOT = Path(__file__).resolve().parent
 if str(ROOT) not in sys.path:
     sys.path.insert(0, str(ROOT))
 
@@ -34,10 +41,11 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     names = {f"cfg{i}": c for i, c in workloads.CONFIGS.items()}
     names.update(workloads.SMALL_CONFIGS)
-    ap.add_argument("--workload", default="cfg2", choices=sorted(names))
+    names["coarse_E2"] = workloads.CONFIGS[2].scaled("bf16_prefill_T2048_H4096_I14336_E2_k2", T=2048, E=2)
+    ap.add_argument("--workload", default="cfg1", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "experts", "combine", "forward",
-                             "route_grouped", "backward", "combine_backward"])
+                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "experts", "experts_combine",
+                             "combine", "forward", "route_grouped", "backward", "combine_backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     cfg = names[args.workload]
@@ -66,6 +74,11 @@ def main(argv=None):
     if args.stage == "combine_backward":
         g = torch.Generator().manual_seed(7)
         grad_out = torch.randn(cfg.T, cfg.H, generator=g).to(cfg.torch_dtype).to(dev)
+    if args.stage == "experts_combine":
+        comb_out = torch.empty(cfg.T, cfg.H, dtype=cfg.torch_dtype, device=dev)
+        comb_ws = torch.empty(moe.load_library().moe_experts_forward_combine_workspace_size(ex.handle, cfg.T,
+                                                                                             cfg.top_k),
+                              dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         if args.stage == "route":
@@ -80,6 +93,9 @@ def main(argv=None):
             moe.moe_experts_down(ex, h, disp.offsets, out=y)
         elif args.stage == "experts":  # gate/up and down chained in one launch
             moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets, out=y)
+        elif args.stage == "experts_combine":  # gate/up, down and combine in one launch
+            moe.moe_experts_forward_combine(ex, disp.x_dispatched, disp.offsets, disp.inv, w, out=comb_out,
+                                            workspace=comb_ws)
         elif args.stage == "route_grouped":
             moe.moe_route_sigmoid_grouped(d["logits"], bias, opts, indices=idx, weights=w)
         elif args.stage == "backward":

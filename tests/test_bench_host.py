@@ -46,9 +46,33 @@ def test_single_rank_max_is_identity():
 
 
 def test_workload_config_is_weak_scaling():
-    cfg = bench.workload_config(bench.PREFILL, 4)
-    assert cfg["tokens_per_gpu"] == 4096 and cfg["global_batch_tokens"] == 4 * 4096
-    assert cfg["workload"] == bench.PREFILL.name and "l2" in cfg
+    cfg = bench.workload_config(bench.HEADLINE, 4)
+    assert cfg["tokens_per_gpu"] == 8192 and cfg["global_batch_tokens"] == 4 * 8192
+    assert cfg["workload"] == bench.HEADLINE.name and "l2" in cfg
+    assert cfg["parallelism"].startswith("dp4")
+
+
+def test_headline_is_the_coarse_prefill():
+    """The headline workload is the GEMM-bound coarse BF16 prefill (T=8192,
+    H=4096, I=14336, E=8, top_k=2), the largest configuration on one GPU."""
+    c = bench.HEADLINE
+    assert (c.dtype, c.T, c.H, c.I, c.E, c.top_k, c.renormalize) == ("bf16", 8192, 4096, 14336, 8, 2, True)
+    assert c.expert_flops == max(w.expert_flops for w in bench.workloads.CONFIGS.values())
+
+
+def test_roofline_counts_the_methods_bytes():
+    """Algorithmic bytes are the touched weights plus x in and out; the
+    fraction follows from them and the peak."""
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0}
+    c = bench.HEADLINE
+    r = bench.gemm_roofline(c, 3e-3, 8, peaks, "test", {"dram_bytes_per_launch": 4.0e9}, "t")
+    want_bytes = 8 * 3 * c.I * c.H * 2 + 2 * c.T * c.H * 2
+    assert r["algorithmic_bytes"] == want_bytes and r["bound"] == "tensor"
+    assert abs(r["frac"] - c.expert_flops / 3e-3 / 1e12 / 2000.0) < 1e-4
+    assert abs(r["traffic_over_algorithmic"] - 4.0e9 / want_bytes) < 1e-4
+    f = bench.FINE
+    r = bench.gemm_roofline(f, 300e-6, 128, peaks, "test", None, "t")
+    assert r["bound"] == "hbm" and r["traffic"] is None
 
 
 def test_warmup_below_three_is_rejected():

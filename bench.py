@@ -643,6 +643,7 @@ def run_ours(args, rank, world, local_rank):
     chain.free()
     del chain
     t_gu, t_dn, _ = gemm_stage_times(moe, c, dev, stream, flush, 5)
+    trc = training_step_times(moe, c, dev, stream, flush, 3)
 
     # ---- fine-grained BF16 prefill (E=128, top_k=8): step, GEMM roofline, grouped routing, training
     f = FINE
@@ -678,14 +679,19 @@ def run_ours(args, rank, world, local_rank):
                          stage_note.format(n=hr["stage_steps"]))
     froof = gemm_roofline(f, fr["stages_s"][2], fr["touched"], peaks, peaks_src, traffic_record(kernel_src, f.name),
                           stage_note.format(n=fr["stage_steps"]))
-    bwd_flops = 2 * f.expert_flops  # dgrad + wgrad: twice the forward's 6*T*k*H*I
-    training = {"workload": f.name, "us_per_step": round(sum(tr) * 1e6, 1),
-                "tokens_per_s": round(world * f.T / sum(tr), 1),
+    def training_line(cfg, tr):
+        bwd_flops = 2 * cfg.expert_flops  # dgrad + wgrad: twice the forward's 6*T*k*H*I
+        tf = bwd_flops / tr[2] / 1e12
+        return {"workload": cfg.name, "us_per_step": round(sum(tr) * 1e6, 1),
+                "tokens_per_s": round(world * cfg.T / sum(tr), 1),
                 "forward_us": round(tr[0] * 1e6, 1), "combine_backward_us": round(tr[1] * 1e6, 1),
                 "experts_backward_us": round(tr[2] * 1e6, 1), "dispatch_backward_us": round(tr[3] * 1e6, 1),
-                "router_backward_us": round(tr[4] * 1e6, 1),
-                "experts_backward_tflops": round(bwd_flops / tr[2] / 1e12, 1),
-                "experts_backward_frac_bf16_peak": round(bwd_flops / tr[2] / 1e12 / peaks["bf16_tflops"], 4)}
+                "router_backward_us": round(tr[4] * 1e6, 1), "experts_backward_tflops": round(tf, 1),
+                "experts_backward_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                "experts_backward_frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+
+    training = training_line(f, tr)
+    training_coarse = training_line(c, trc)
     d = DECODE
     es = 2
     dec_bytes = dr["touched"] * 3 * d.I * d.H * es
@@ -748,6 +754,7 @@ def run_ours(args, rank, world, local_rank):
                                "down_alone_us": round(z_dn * 1e6, 1), "flops": ZIPF.expert_flops,
                                "note": "F16 and BF16 share the dense tensor rate"},
         "training_step": training,
+        "training_step_coarse": training_coarse,
         "sigmoid_grouped": {
             "workload": f"{f.name} with grouped sigmoid routing: {grouped_routing.groups} groups, "
                         f"{grouped_routing.selected_groups} selected, top-two group scores, scale "

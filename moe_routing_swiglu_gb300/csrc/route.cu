@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(const TL* __res
     for (int q = 0; q < V; ++q) {
       const int j = q * 32 + lane;
       p[q] = 0.0f;
-      if (j < k) p[q] = __fdiv_rn(my_e[keep_id[q]], s);
+      if (q * 32 < k && j < k) p[q] = __fdiv_rn(my_e[keep_id[q]], s);  // registers holding slots only
     }
     float z = 0.0f;
     if (renormalize) {
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(const TL* __res
 #pragma unroll
     for (int q = 0; q < V; ++q) {
       const int j = q * 32 + lane;
-      if (j < k) {
+      if (q * 32 < k && j < k) {
         const float w = renormalize ? __fdiv_rn(p[q], z) : p[q];
         idx_row[j] = keep_id[q];
         weights[t * k + j] = from_f32<TL>(w);

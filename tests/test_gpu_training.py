@@ -113,6 +113,29 @@ def test_experts_training_forward_and_backward_parity(cuda_lib, name):
     assert moe.moe_device_status() == 0
 
 
+def test_experts_training_coarse_expert_shape(cuda_lib):
+    """The coarse prefill's expert shape (H = 4096, I = 14336) on two experts
+    with 300 and 300 rows (every token on both): the training forward's cache
+    and the tensor-core backward against the oracle, entry by entry."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[2].scaled("coarse_shape_T300_E2_k2", T=300, E=2, seed=5301)
+    inp = workloads.generate(cfg)
+    rt = moe_oracle.route(inp["logits"], cfg.top_k, cfg.renormalize)
+    dp = moe_oracle.dispatch(rt.indices, cfg.E)
+    xd = inp["x"][torch.from_numpy(dp.row_src.astype(np.int64) // cfg.top_k)]
+    g = torch.Generator().manual_seed(17)
+    dy = (torch.randn(cfg.T * cfg.top_k, cfg.H, generator=g) * 0.5).to(cfg.torch_dtype)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    offs = torch.from_numpy(dp.offsets.astype(np.int64)).to(torch.int32).to(DEV)
+    xdd = xd.to(DEV).contiguous()
+    y, cache = moe.moe_experts_forward_training(ex, xdd, offs)
+    gr = moe.moe_experts_backward(ex, cache, dy.to(DEV))
+    torch.cuda.synchronize()
+    check_experts_training(cache, gr, xd, inp["gate"], inp["up"], inp["down"], dp.offsets, dy, cfg.torch_dtype)
+    assert moe.moe_device_status() == 0
+
+
 @pytest.mark.parametrize("which", ["u_is_g", "h_is_u"])
 def test_planted_wrong_cache_entry_is_caught(cuda_lib, which):
     """A cache whose u holds the gate pre-activation (or whose h holds u),

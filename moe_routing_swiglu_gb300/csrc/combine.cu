@@ -5,9 +5,10 @@
 // out[t, :] = sum_{j=0..k-1} w[t, j] * y[inv[t*k + j], :], accumulated in FP32
 // in slot order j = 0, 1, ..., k-1, then rounded to the output dtype. One
 // block per token (grid-stride): the token's k row numbers and weights are
-// staged in shared memory, then each thread owns 16-byte vectors of the row
-// and keeps 4 slot-row loads in flight before their in-order FMAs. No
-// atomics, so the result does not depend on scheduling. A slot whose inv
+// staged in shared memory (the threads that stage them also ask L2 to fetch
+// each whole slot row in one bulk prefetch), then each thread owns 16-byte
+// vectors of the row and keeps 4 slot-row loads in flight before their
+// in-order FMAs. No atomics, so the result does not depend on scheduling. A slot whose inv
 // entry is INVALID_ROW (an index >= E at dispatch), or any entry >= T*k,
 // makes its token's row NaN instead of reading out of range.
 //
@@ -68,6 +69,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
       s_row[j] = r < rows ? r : 0u;           // an invalid entry reads row 0 ...
       s_w[j] = WEIGHTED ? to_f32(w[t * k + j]) : 1.0f;
       if (r >= rows) s_bad = 1;               // ... and the whole row becomes NaN
+      // The whole slot row into L2 in one request, ahead of the loads below.
+      else if (VEC) prefetch_l2_bulk(y + static_cast<int64_t>(r) * H, static_cast<uint32_t>(H * sizeof(T)));
     }
     __syncthreads();
     const bool bad = s_bad != 0;

@@ -271,6 +271,12 @@ __device__ __forceinline__ uint32_t counter_acq_rel_add(uint32_t* ctr) {
   return old;
 }
 
+// Asynchronous prefetch of `bytes` of global memory into L2 (one bulk request,
+// no registers, nothing to wait for). Address and size must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA (bulk tensor copies)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {

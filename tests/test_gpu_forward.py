@@ -233,3 +233,25 @@ def test_forward_host_rejects_bad_arguments(cuda_lib):
     with pytest.raises(moe.MoeError):
         moe.moe_forward_host(ex, d["x"], hl, cfg.top_k, True)      # a device tensor where host memory belongs
     assert lib.moe_forward_host_workspace_size(ex.handle, cfg.T, cfg.top_k, 7) == 0
+
+
+@pytest.mark.parametrize("cfg_id", [1, 2])
+def test_token_shards_equal_the_global_batch(cuda_lib, cfg_id):
+    """Data-parallel sharding on the GPU path: moe_forward on two token shards
+    (workloads.generate shard=0 and shard=1, the same experts) equals, row
+    for row and bit for bit, moe_forward on their concatenation. A row's
+    expert outputs do not depend on which other rows share its tiles."""
+    moe = cuda_lib
+    cfg = workloads.CONFIGS[cfg_id]
+    full = workloads.generate(cfg)
+    other = workloads.generate(cfg, weights=False, shard=1)
+    d = _device_inputs(full)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    x1, l1 = other["x"].to(DEV), other["logits"].to(DEV)
+    out0 = moe.moe_forward(ex, d["x"], d["logits"], cfg.top_k, cfg.renormalize)
+    out1 = moe.moe_forward(ex, x1, l1, cfg.top_k, cfg.renormalize)
+    both = moe.moe_forward(ex, torch.cat([d["x"], x1]), torch.cat([d["logits"], l1]), cfg.top_k,
+                           cfg.renormalize)
+    torch.cuda.synchronize()
+    assert torch.equal(both.view(torch.uint8), torch.cat([out0, out1]).view(torch.uint8))
+    assert moe.moe_device_status() == 0

@@ -57,7 +57,7 @@ FINE = workloads.CONFIGS[1]      # fine-grained BF16 prefill
 DECODE = workloads.CONFIGS[3]
 ZIPF = workloads.CONFIGS[4]
 FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 6  # route, dispatch count + scatter + gather, gate/up + down GEMMs (one launch), combine
+KERNELS_PER_STEP = 3  # route + dispatch (one launch), gate/up + down GEMMs (one launch), combine
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -192,7 +192,9 @@ class Chain:
                                dtype=torch.uint8, **e)
         self.uws = torch.empty(max(1, self.lib.moe_experts_forward_dispatched_workspace_size(self.ex.handle, n)),
                                dtype=torch.uint8, **e)
+        self.rdws = torch.empty(max(1, self.lib.moe_route_dispatch_workspace_size(T, E)), dtype=torch.uint8, **e)
         self.fused = False  # prefill staged run: True = the experts and the combine in one launch
+        self.split_route = False  # staged run: True = moe_route then moe_dispatch instead of the one launch
         self.dt = moe._dt(d["x"])
         self.grouped = None  # (bias device tensor or None, GroupRoutingOptions) to route by sigmoid groups
 
@@ -206,7 +208,10 @@ class Chain:
 
     def step(self, stream, ev=None):
         """route | dispatch | experts | combine, events between: the calls
-        moe_forward makes. Prefill: the chained gate/up + down launch over
+        moe_forward makes. Softmax routing: route and dispatch as the one
+        launch moe_forward runs (moe_route_dispatch; the dispatch stage is
+        then empty), or with self.split_route moe_route then moe_dispatch.
+        Prefill: the chained gate/up + down launch over
         x_dispatched (moe_experts_forward_dispatched, the kernel moe_forward
         runs), then moe_combine; with self.fused, the experts and the
         combine in one launch (moe_experts_forward_combine; the combine
@@ -219,7 +224,14 @@ class Chain:
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
         rc = 0
         rec(0)
-        if self.grouped is None:
+        fused_rd = self.grouped is None and not self.split_route
+        if fused_rd:
+            xd = None if self.gather else self.xd
+            rc |= lib.moe_route_dispatch(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx),
+                                         P(self.w), None, None if xd is None else P(self.d["x"]), self.dt, H,
+                                         P(self.counts), P(self.offsets), P(self.row_src), P(self.inv), P(xd),
+                                         P(self.rdws), self.rdws.numel(), s)
+        elif self.grouped is None:
             rc |= lib.moe_route(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx),
                                 P(self.w), None, s)
         else:
@@ -228,17 +240,19 @@ class Chain:
                                                 P(self.idx), P(self.w), None, s)
         rec(1)
         if self.gather:
-            rc |= lib.moe_dispatch(P(self.idx), T, E, k, None, self.dt, H, P(self.counts), P(self.offsets),
-                                   P(self.row_src), P(self.inv), None, P(self.dws), self.dws.numel(), s)
+            if not fused_rd:
+                rc |= lib.moe_dispatch(P(self.idx), T, E, k, None, self.dt, H, P(self.counts), P(self.offsets),
+                                       P(self.row_src), P(self.inv), None, P(self.dws), self.dws.numel(), s)
             rec(2)
             rc |= lib.moe_experts_gate_up_gather(self.ex.handle, P(self.d["x"]), T, P(self.row_src), k,
                                                  P(self.offsets), T * k, P(self.h), P(self.sws), self.sws.numel(), s)
             rc |= lib.moe_experts_down(self.ex.handle, P(self.h), P(self.offsets), T * k, P(self.yd), P(self.sws),
                                        self.sws.numel(), s)
         else:
-            rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts),
-                                   P(self.offsets), P(self.row_src), P(self.inv), P(self.xd), P(self.dws),
-                                   self.dws.numel(), s)
+            if not fused_rd:
+                rc |= lib.moe_dispatch(P(self.idx), T, E, k, P(self.d["x"]), self.dt, H, P(self.counts),
+                                       P(self.offsets), P(self.row_src), P(self.inv), P(self.xd), P(self.dws),
+                                       self.dws.numel(), s)
             rec(2)
             if self.fused:
                 rc |= lib.moe_experts_forward_combine(self.ex.handle, P(self.xd), P(self.offsets), P(self.inv),
@@ -598,6 +612,10 @@ def forward_measure(moe, cfg, dev, stream, flush, steps, warmup, world, shard=0,
     n_stage = stage_steps or min(steps, 200)
     stages, stage_total = timed_steps(chain, stream, flush, n_stage, warmup)
     stages = [float(x) for x in stages]
+    chain.split_route = True
+    split, _ = timed_steps(chain, stream, flush, n_stage, warmup)
+    chain.split_route = False
+    split = [float(x) for x in split]
     fused = None
     if not chain.gather:
         chain.fused = True
@@ -608,7 +626,8 @@ def forward_measure(moe, cfg, dev, stream, flush, steps, warmup, world, shard=0,
                  "experts_plus_combine_us": round((stages[2] + stages[3]) * 1e6, 2),
                  "fused_staged_step_us": round(f_total / n_stage * 1e6, 2),
                  "staged_step_us": round(stage_total / n_stage * 1e6, 2)}
-    return chain, {"total_s": total, "steps": steps, "stages_s": stages, "stage_steps": n_stage,
+    return chain, {"total_s": total, "steps": steps, "stages_s": stages, "split_stages_s": split,
+                   "stage_steps": n_stage,
                    "stage_total_s": stage_total, "touched": chain.touched_experts(), "fused_ab": fused}
 
 
@@ -703,9 +722,12 @@ def run_ours(args, rank, world, local_rank):
     dec_exp = dr["stages_s"][2]
     ztf = ZIPF.expert_flops / z_ch / 1e12
 
-    def route_dispatch(st):
-        return {"route": round(st[0] * 1e6, 2), "dispatch": round(st[1] * 1e6, 2),
-                "total": round((st[0] + st[1]) * 1e6, 2)}
+    def route_dispatch(r):
+        """The one route + dispatch launch moe_forward runs, and beside it
+        moe_route then moe_dispatch (the split API's kernels)."""
+        st, sp = r["stages_s"], r["split_stages_s"]
+        return {"total": round((st[0] + st[1]) * 1e6, 2), "split_route": round(sp[0] * 1e6, 2),
+                "split_dispatch": round(sp[1] * 1e6, 2), "split_total": round((sp[0] + sp[1]) * 1e6, 2)}
 
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
@@ -717,7 +739,7 @@ def run_ours(args, rank, world, local_rank):
                          "frac_bf16_sustained": roof["tensor_frac_sustained"], "flops_per_step": c.expert_flops,
                          "chained_us": roof["us"], "gate_up_alone_us": round(t_gu * 1e6, 2),
                          "down_alone_us": round(t_dn * 1e6, 2)},
-        "route_dispatch_us": route_dispatch(hr["stages_s"]),
+        "route_dispatch_us": route_dispatch(hr),
         "combine_us": round(hr["stages_s"][3] * 1e6, 2),
         "fused_combine_ab": hr["fused_ab"],
         "timing": {"value": f"{args.steps} CUDA-graph replays of one moe_forward call (its {KERNELS_PER_STEP} "
@@ -737,7 +759,7 @@ def run_ours(args, rank, world, local_rank):
         "fine_prefill": {
             "workload": f.name, "tokens_per_s": round(world * f.T * fr["steps"] / fr["total_s"], 1),
             "us_per_step": round(fr["total_s"] / fr["steps"] * 1e6, 2),
-            "route_dispatch_us": route_dispatch(fr["stages_s"]),
+            "route_dispatch_us": route_dispatch(fr),
             "experts_us": round(fr["stages_s"][2] * 1e6, 2), "combine_us": round(fr["stages_s"][3] * 1e6, 2),
             "fused_combine_ab": fr["fused_ab"],
             "gate_up_alone_us": round(f_gu * 1e6, 2), "down_alone_us": round(f_dn * 1e6, 2),
@@ -745,7 +767,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"workload": d.name, "us_per_step": round(dec_fwd * 1e6, 2),
                    "timing": "CUDA-graph replays of the decode step (forward, gate/up and down chained in one "
                              "launch); experts_us from the staged run (the two GEMMs launched apart)",
-                   "route_dispatch_us": route_dispatch(dr["stages_s"]),
+                   "route_dispatch_us": route_dispatch(dr),
                    "frac_hbm_forward": round(dec_bytes / dec_fwd / 1e9 / peaks["hbm_gbs"], 4),
                    "experts_us": round(dec_exp * 1e6, 2), "touched_experts": dr["touched"],
                    "touched_weight_bytes": dec_bytes,
@@ -766,7 +788,7 @@ def run_ours(args, rank, world, local_rank):
             "tokens_per_s": round(world * f.T * g_steps / g_total, 1),
             "us_per_step": round(g_total / g_steps * 1e6, 2),
             "route_us": round(float(g_stages[0]) * 1e6, 2),
-            "softmax_route_us": round(fr["stages_s"][0] * 1e6, 2)},
+            "softmax_route_us": round(fr["split_stages_s"][0] * 1e6, 2)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }

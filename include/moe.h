@@ -152,6 +152,34 @@ moe_status moe_dispatch_noalloc(const uint32_t* indices, int64_t T, int64_t E, i
                                 void* x_dispatched, void* stream);
 
 /*
+ * moe_route_dispatch - moe_route followed by moe_dispatch as one cooperative
+ * launch (ruDNN user guide sections 4 "Routing contract" and 5 "Expert
+ * weights and dispatch"): every output is the same, bit for bit, as those two
+ * calls give. moe_forward runs this launch for its routing and dispatch.
+ *
+ *   logits, logits_dtype, T, E, top_k, renormalize, indices, weights,
+ *   weights_fp32      as moe_route.
+ *   x, x_dtype, H, counts, offsets, row_src, inv, x_dispatched
+ *                     as moe_dispatch (x_dtype is x's dtype; x_dispatched
+ *                     NULL writes the maps only).
+ *   workspace         device scratch of moe_route_dispatch_workspace_size(T, E)
+ *                     bytes (256-byte aligned); contents need not be
+ *                     initialised (the call zeroes what it needs on the
+ *                     stream).
+ *
+ * The blocks of the launch meet once at a grid-wide barrier (all of them are
+ * resident: the launch is cooperative). Its wait is bounded (about one
+ * second); a wait that runs out records 0x1B in the device status word
+ * (moe_device_status) and the launch returns with its outputs incomplete.
+ */
+size_t moe_route_dispatch_workspace_size(int64_t T, int64_t E);
+moe_status moe_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int64_t E, int32_t top_k,
+                              int32_t renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                              const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                              uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * moe_experts_create - validate and wrap bias-free SwiGLU expert weights
  * (SwiGluExperts::new; ruDNN user guide section 5: gate and up [E, I, H],
  * down [E, H, I], one float dtype, one device).
@@ -554,7 +582,9 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
  * waiting for a finished accumulator, 0x15 / 0x16 teardown drains, 0x17 a
  * wait on the shared-memory tile ring of the tile scheduler, 0x18 a gather
  * loader waiting for a free stage, 0x19 a down tile of the chained gate/up +
- * down launch waiting for its expert's h rows, 0x100
+ * down launch waiting for its expert's h rows, 0x1A the combine of
+ * moe_experts_forward_combine waiting for the last down tile, 0x1B the grid
+ * barrier of moe_route_dispatch (and of moe_forward's routing), 0x100
  * moe_selftest_bounded_wait. Synchronises the current device; *code = 0 when
  * no wait has timed out.
  */

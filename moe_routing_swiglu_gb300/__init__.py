@@ -68,6 +68,9 @@ SIGNATURES = {
                                     _P, _SZ, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, ctypes.c_int, _I64, _P, _P, _P, _P, _P,
                                             _P]),
+    "moe_route_dispatch_workspace_size": (_SZ, [_I64, _I64]),
+    "moe_route_dispatch": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _I32, _P, _P, _P, _P, ctypes.c_int,
+                                          _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_experts_create": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                           ctypes.POINTER(ctypes.c_void_p)]),
     "moe_experts_destroy": (None, [_P]),
@@ -213,6 +216,36 @@ def moe_dispatch(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None
                             _ptr(offsets), _ptr(row_src), _ptr(inv), _ptr(xd), _ptr(ws),
                             ws.numel(), _stream(stream)))
     return DispatchedTokens(counts, offsets, row_src, inv, xd)
+
+
+def moe_route_dispatch(logits: torch.Tensor, top_k: int, renormalize: bool, x: torch.Tensor | None = None,
+                       *, weights_fp32=False, workspace=None, stream=None):
+    """moe_route then moe_dispatch as one launch (the same outputs, bit for
+    bit): returns (indices, weights[, FP32 weights], DispatchedTokens)."""
+    lib = load_library()
+    _dev_tensor(logits, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    indices = torch.empty(T, top_k, dtype=torch.int32, device=dev)
+    weights = torch.empty(T, top_k, dtype=logits.dtype, device=dev)
+    w32 = torch.empty(T, top_k, dtype=torch.float32, device=dev) if weights_fp32 else None
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_src = torch.empty(T * top_k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * top_k, dtype=torch.int32, device=dev)
+    xd = None
+    H, xdt = 0, MOE_F32
+    if x is not None:
+        _dev_tensor(x, "x")
+        H, xdt = x.shape[1], _dt(x)
+        xd = torch.empty(T * top_k, H, dtype=x.dtype, device=dev)
+    need = lib.moe_route_dispatch_workspace_size(T, E)
+    ws = _workspace(need, dev, workspace)
+    _check(lib.moe_route_dispatch(_ptr(logits), _dt(logits), T, E, top_k, int(bool(renormalize)), _ptr(indices),
+                                  _ptr(weights), _ptr(w32), _ptr(x), xdt, H, _ptr(counts), _ptr(offsets),
+                                  _ptr(row_src), _ptr(inv), _ptr(xd), _ptr(ws), ws.numel(), _stream(stream)))
+    disp = DispatchedTokens(counts, offsets, row_src, inv, xd)
+    return (indices, weights, w32, disp) if w32 is not None else (indices, weights, disp)
 
 
 def moe_dispatch_noalloc(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None = None,

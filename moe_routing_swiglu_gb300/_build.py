@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libmoe_gb300.so"
 
-SOURCES = ["api.cu", "route.cu", "route_grouped.cu", "dispatch.cu", "combine.cu", "experts_simt.cu", "experts_tc.cu",
+SOURCES = ["api.cu", "route.cu", "route_dispatch.cu", "route_grouped.cu", "dispatch.cu", "combine.cu", "experts_simt.cu", "experts_tc.cu",
            "train_router.cu", "train_experts.cu", "experts_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -4,6 +4,7 @@
 // the device (moe_device_status excepted, which exists to read a result).
 #include <stdio.h>
 
+#include <algorithm>
 #include <limits>
 #include <string>
 
@@ -124,7 +125,7 @@ ForwardLayout forward_layout(const moe_experts* ex, int64_t T, int top_k) {
   L.offsets = take(static_cast<size_t>(ex->E + 1) * 4);
   L.row_src = take(n * 4);
   L.inv = take(n * 4);
-  L.scratch = take(moe::dispatch_scratch_bytes(T, ex->E, top_k));
+  L.scratch = take(std::max(moe::dispatch_scratch_bytes(T, ex->E, top_k), moe::route_dispatch_scratch_bytes(T, ex->E)));
   // Tile counters, then (from word 64) one ready counter per expert for the
   // chained gate/up + down kernel; the dispatch zeroes them.
   L.sched = take(moe::TC_SCHED_BYTES + static_cast<size_t>(ex->E) * 4);
@@ -186,13 +187,22 @@ moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t
   return check_current_device(ex);
 }
 
+// Softmax routing arguments of moe_forward: route and dispatch then run as
+// one cooperative launch.
+struct SoftmaxRouting {
+  const void* logits;
+  bool renormalize;
+};
+
 // Route (by the given launch), dispatch, experts, combine: the body of
 // moe_forward and moe_forward_sigmoid_grouped once the routing arguments
-// are checked.
+// are checked. With `softmax` set, route and dispatch are the one fused
+// launch (the same bits) and `route` is not called.
 template <typename RouteLaunch>
 moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_dtype, int64_t T, int top_k,
                          void* out, uint32_t* indices_opt, void* weights_opt, void* workspace,
-                         size_t workspace_bytes, cudaStream_t s, RouteLaunch route) {
+                         size_t workspace_bytes, cudaStream_t s, RouteLaunch route,
+                         const SoftmaxRouting* softmax = nullptr) {
   if (T > 0 && (x == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "x and out must be non-NULL");
   const ForwardLayout L = forward_layout(ex, T, top_k);
   if (workspace == nullptr || workspace_bytes < L.total)
@@ -221,19 +231,29 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   // GEMM streams with 128-row TMA boxes (a row gather costs about as much
   // TMA time as a whole box, so gathering every weight tile's 256 rows is
   // slower there than the extra copy).
-  // The dispatch's scatter kernel zeroes the GEMMs' tile counter and the
-  // per-expert ready counters, so the chain is kernels only (each launched
-  // as a dependent of the previous). F16/BF16: gate/up and down run as one
+  // The dispatch (the fused route + dispatch launch, or the scatter kernel)
+  // zeroes the GEMMs' tile counter and the per-expert ready counters, so the
+  // GEMMs need no memset (each kernel after the dispatch is launched as a
+  // dependent of the previous). F16/BF16: gate/up and down run as one
   // launch whose down tiles start on each expert as soon as its h rows are
   // stored; F32: two launches.
   uint32_t* sched = reinterpret_cast<uint32_t*>(ws + L.sched);
   uint32_t* ready = sched + moe::TC_SCHED_BYTES / 4;
-  cudaError_t err = route(indices, weights, s);
-  if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
-  err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
-                             ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched,
-                             static_cast<int64_t>(moe::TC_SCHED_BYTES / 4 + ex->E));
-  if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
+  const int64_t n_zero = static_cast<int64_t>(moe::TC_SCHED_BYTES / 4 + ex->E);
+  cudaError_t err;
+  if (softmax != nullptr) {
+    err = moe::launch_route_dispatch(softmax->logits, logits_dtype, T, static_cast<int>(ex->E), top_k,
+                                     softmax->renormalize, indices, weights, nullptr, gather_rows ? nullptr : x,
+                                     ex->dtype, ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch,
+                                     ex->num_sms, s, sched, n_zero);
+    if (err != cudaSuccess) return cuda_fail(err, "forward route + dispatch launch");
+  } else {
+    err = route(indices, weights, s);
+    if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
+    err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
+                               ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched, n_zero);
+    if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
+  }
   const moe::TcGather gather{x, row_src, top_k, T};
   if (ex->dtype == MOE_F32) {
     st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, sched, s, nullptr, true);
@@ -378,6 +398,48 @@ moe_status moe_dispatch_noalloc(const uint32_t* indices, int64_t T, int64_t E, i
   err = moe::launch_dispatch(indices, T, static_cast<int>(E), top_k, x, dtype, H, counts, offsets, row_src,
                              inv, x_dispatched, scratch, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch_noalloc launch");
+  return ok();
+}
+
+size_t moe_route_dispatch_workspace_size(int64_t T, int64_t E) {
+  if (T < 0 || E < 1 || E > moe::ROUTE_MAX_E) return 0;
+  return moe::route_dispatch_scratch_bytes(T, E);
+}
+
+moe_status moe_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int64_t E, int32_t top_k,
+                              int32_t renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                              const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                              uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  moe_status st = check_route_args(logits, logits_dtype, T, E, top_k, indices, weights);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "counts and offsets must be non-NULL");
+  if (T > 0 && (row_src == nullptr || inv == nullptr)) return fail(MOE_ERR_NULL, "row_src and inv must be non-NULL");
+  if (x_dispatched != nullptr) {
+    if (x == nullptr) return fail(MOE_ERR_NULL, "x_dispatched needs x");
+    if (!dtype_valid(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+    if (H < 1) return fail(MOE_ERR_SHAPE, "H must be >= 1");
+  }
+  const size_t need = moe::route_dispatch_scratch_bytes(T, E);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_route_dispatch_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // No slots: zero counts and offsets, as moe_dispatch writes them.
+    cudaError_t err = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch: zero counts and offsets");
+    return ok();
+  }
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch: device query");
+  err = moe::launch_route_dispatch(logits, logits_dtype, T, static_cast<int>(E), top_k, renormalize != 0, indices,
+                                   weights, weights_fp32, x, x_dtype, H, counts, offsets, row_src, inv, x_dispatched,
+                                   workspace, sms, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch launch");
   return ok();
 }
 
@@ -588,12 +650,10 @@ moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
   if (ex == nullptr) return fail(MOE_ERR_NULL, "experts must be non-NULL");
   moe_status st = check_route_args(logits, logits_dtype, T, ex->E, top_k, logits, logits);
   if (st != MOE_OK) return st;
-  auto route = [&](uint32_t* indices, void* weights, cudaStream_t s) {
-    return moe::launch_route(logits, logits_dtype, T, static_cast<int>(ex->E), top_k, renormalize != 0,
-                             indices, weights, nullptr, s);
-  };
+  auto route = [&](uint32_t*, void*, cudaStream_t) { return cudaSuccess; };
+  const SoftmaxRouting softmax{logits, renormalize != 0};
   return forward_chain(ex, x, logits_dtype, T, top_k, out, indices_opt, weights_opt, workspace,
-                       workspace_bytes, static_cast<cudaStream_t>(stream), route);
+                       workspace_bytes, static_cast<cudaStream_t>(stream), route, &softmax);
 }
 
 size_t moe_forward_host_workspace_size(const moe_experts* ex, int64_t T, int32_t top_k, moe_dtype logits_dtype) {
@@ -629,11 +689,9 @@ moe_status moe_forward_host(const moe_experts* ex, const void* x_host, const voi
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of x to the device");
   err = cudaMemcpyAsync(dl, logits_host, h.logits_bytes, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of the logits to the device");
-  auto route = [&](uint32_t* indices, void* weights, cudaStream_t rs) {
-    return moe::launch_route(dl, logits_dtype, T, static_cast<int>(ex->E), top_k, renormalize != 0, indices,
-                             weights, nullptr, rs);
-  };
-  st = forward_chain(ex, dx, logits_dtype, T, top_k, dout, indices_opt, weights_opt, ws, h.fwd, s, route);
+  auto route = [&](uint32_t*, void*, cudaStream_t) { return cudaSuccess; };
+  const SoftmaxRouting softmax{dl, renormalize != 0};
+  st = forward_chain(ex, dx, logits_dtype, T, top_k, dout, indices_opt, weights_opt, ws, h.fwd, s, route, &softmax);
   if (st != MOE_OK) return st;
   err = cudaMemcpyAsync(out_host, dout, h.out_bytes, cudaMemcpyDeviceToHost, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of out to the host");

@@ -69,6 +69,21 @@ cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
                             cudaStream_t stream, uint32_t* zero_words = nullptr, int64_t n_zero = 0);
 
+// ---- K1 + K2 in one cooperative launch (route_dispatch.cu): softmax routing,
+// then the dispatch maps and (x_dispatched != NULL) the x copy; the same bits
+// as launch_route followed by launch_dispatch. scratch: RD_BARRIER_BYTES for
+// the grid barrier (zeroed on the stream by the launcher), then the blocks'
+// expert histograms.
+constexpr int64_t RD_MAX_BLOCKS = 2048;
+constexpr size_t RD_BARRIER_BYTES = 256;
+size_t route_dispatch_scratch_bytes(int64_t T, int64_t E);
+cudaError_t launch_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int E, int top_k,
+                                  bool renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                                  const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                                  uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
+                                  int num_sms, cudaStream_t stream, uint32_t* zero_words = nullptr,
+                                  int64_t n_zero = 0);
+
 // ---- K5 combine (combine.cu)
 cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,
                            const void* weights, moe_dtype weights_dtype, int64_t T, int top_k,

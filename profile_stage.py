@@ -11,10 +11,11 @@ of 3.7 GB, for captures that replay a launch many times). The inputs
 are the seeded synthetic workloads of ``workloads.py``; routing and
 dispatch run once to set up the stage's inputs, then the chosen stage runs
 ``--reps`` times back to back (stream-ordered) and the device is synchronised.
-Stages: route, dispatch, gate_up, gate_up_gather (x rows read through
-row_src), down, experts (gate/up and down chained in one launch),
-experts_combine (gate/up, down and the weighted combine in one launch, as
-moe_forward runs them), combine, forward (moe_forward), and
+Stages: route, dispatch, route_dispatch (routing and dispatch in one
+launch, as moe_forward runs them), gate_up, gate_up_gather (x rows read
+through row_src), down, experts (gate/up and down chained in one launch),
+experts_combine (gate/up, down and the weighted combine in one launch:
+moe_experts_forward_combine), combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
 variant in ``workloads.GROUPED``), backward (the experts' backward of
 first-order training on a random output gradient) and combine_backward (the
@@ -44,7 +45,7 @@ def main(argv=None):
     names["coarse_E2"] = workloads.CONFIGS[2].scaled("bf16_prefill_T2048_H4096_I14336_E2_k2", T=2048, E=2)
     ap.add_argument("--workload", default="cfg1", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "gate_up", "gate_up_gather", "down", "experts", "experts_combine",
+                    choices=["route", "dispatch", "route_dispatch", "gate_up", "gate_up_gather", "down", "experts", "experts_combine",
                              "combine", "forward", "route_grouped", "backward", "combine_backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
@@ -85,6 +86,9 @@ def main(argv=None):
             moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize, indices=idx, weights=w)
         elif args.stage == "dispatch":
             moe.moe_dispatch(idx, cfg.E, d["x"])
+        elif args.stage == "route_dispatch":  # one launch, as moe_forward runs it
+            gather = cfg.T * cfg.top_k <= 8 * cfg.E
+            moe.moe_route_dispatch(d["logits"], cfg.top_k, cfg.renormalize, None if gather else d["x"])
         elif args.stage == "gate_up":
             moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets, out=h)
         elif args.stage == "gate_up_gather":

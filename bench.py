@@ -208,9 +208,10 @@ class Chain:
 
     def step(self, stream, ev=None):
         """route | dispatch | experts | combine, events between: the calls
-        moe_forward makes. Softmax routing: route and dispatch as the one
-        launch moe_forward runs (moe_route_dispatch; the dispatch stage is
-        then empty), or with self.split_route moe_route then moe_dispatch.
+        moe_forward makes. Route and dispatch as the one launch the forward
+        calls run (moe_route_dispatch, or moe_route_sigmoid_grouped_dispatch
+        with grouped routing; the dispatch stage is then empty), or with
+        self.split_route the routing call then moe_dispatch.
         Prefill: the chained gate/up + down launch over
         x_dispatched (moe_experts_forward_dispatched, the kernel moe_forward
         runs), then moe_combine; with self.fused, the experts and the
@@ -224,13 +225,20 @@ class Chain:
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
         rc = 0
         rec(0)
-        fused_rd = self.grouped is None and not self.split_route
-        if fused_rd:
-            xd = None if self.gather else self.xd
+        fused_rd = not self.split_route
+        xd = None if self.gather else self.xd
+        xp = None if xd is None else P(self.d["x"])
+        if fused_rd and self.grouped is None:
             rc |= lib.moe_route_dispatch(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx),
-                                         P(self.w), None, None if xd is None else P(self.d["x"]), self.dt, H,
-                                         P(self.counts), P(self.offsets), P(self.row_src), P(self.inv), P(xd),
-                                         P(self.rdws), self.rdws.numel(), s)
+                                         P(self.w), None, xp, self.dt, H, P(self.counts), P(self.offsets),
+                                         P(self.row_src), P(self.inv), P(xd), P(self.rdws), self.rdws.numel(), s)
+        elif fused_rd:
+            bias, opts = self.grouped
+            rc |= lib.moe_route_sigmoid_grouped_dispatch(P(self.d["logits"]), self.dt, T, E, P(bias),
+                                                         ctypes.byref(opts), P(self.idx), P(self.w), None, xp,
+                                                         self.dt, H, P(self.counts), P(self.offsets),
+                                                         P(self.row_src), P(self.inv), P(xd), P(self.rdws),
+                                                         self.rdws.numel(), s)
         elif self.grouped is None:
             rc |= lib.moe_route(P(self.d["logits"]), self.dt, T, E, k, int(c.renormalize), P(self.idx),
                                 P(self.w), None, s)
@@ -677,6 +685,9 @@ def run_ours(args, rank, world, local_rank):
     g_steps = min(args.steps, 200)
     g_stages, g_total = timed_steps(fchain, stream, flush, g_steps, args.warmup)
     g_total = max_over_ranks(g_total, world, dev)
+    fchain.split_route = True
+    g_split, _ = timed_steps(fchain, stream, flush, g_steps, args.warmup)
+    fchain.split_route = False
     fchain.free()
     del fchain
     f_gu, f_dn, _ = gemm_stage_times(moe, f, dev, stream, flush, 5)
@@ -787,8 +798,10 @@ def run_ours(args, rank, world, local_rank):
                         f"{grouped_routing.scale}, FP32 bias N(0, {grouped_routing.bias_std}^2)",
             "tokens_per_s": round(world * f.T * g_steps / g_total, 1),
             "us_per_step": round(g_total / g_steps * 1e6, 2),
-            "route_us": round(float(g_stages[0]) * 1e6, 2),
-            "softmax_route_us": round(fr["split_stages_s"][0] * 1e6, 2)},
+            "route_dispatch_us": round(float(g_stages[0] + g_stages[1]) * 1e6, 2),
+            "split_route_us": round(float(g_split[0]) * 1e6, 2),
+            "split_dispatch_us": round(float(g_split[1]) * 1e6, 2),
+            "softmax_split_route_us": round(fr["split_stages_s"][0] * 1e6, 2)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }

@@ -439,9 +439,27 @@ moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_
                                      uint32_t* indices, void* weights, float* weights_fp32, void* stream);
 
 /*
+ * moe_route_sigmoid_grouped_dispatch - moe_route_sigmoid_grouped followed by
+ * moe_dispatch as one cooperative launch, as moe_route_dispatch is for the
+ * softmax routing: every output is the same, bit for bit, as those two calls
+ * give. Routing arguments as moe_route_sigmoid_grouped; x, x_dtype, H, the
+ * maps and x_dispatched as moe_dispatch; the workspace is
+ * moe_route_dispatch_workspace_size(T, E) bytes (256-byte aligned, contents
+ * need not be initialised). The grid barrier's wait is bounded as in
+ * moe_route_dispatch (status 0x1B).
+ */
+moe_status moe_route_sigmoid_grouped_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int64_t E,
+                                              const float* bias, const moe_group_routing_options* options,
+                                              uint32_t* indices, void* weights, float* weights_fp32, const void* x,
+                                              moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                                              uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
+/*
  * moe_forward_sigmoid_grouped - the whole local chain with grouped sigmoid
  * routing (SwiGluExperts::forward_sigmoid_grouped, ruDNN user guide section
- * 10): moe_route_sigmoid_grouped, then dispatch, SwiGLU experts and combine
+ * 10): the grouped routing and the dispatch (one launch, as
+ * moe_route_sigmoid_grouped_dispatch), then SwiGLU experts and combine
  * exactly as moe_forward does. Arguments as in moe_forward, with `bias` and
  * `options` as in moe_route_sigmoid_grouped; the workspace is
  * moe_forward_workspace_size(experts, T, options->top_k) bytes.
@@ -584,7 +602,8 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
  * loader waiting for a free stage, 0x19 a down tile of the chained gate/up +
  * down launch waiting for its expert's h rows, 0x1A the combine of
  * moe_experts_forward_combine waiting for the last down tile, 0x1B the grid
- * barrier of moe_route_dispatch (and of moe_forward's routing), 0x100
+ * barrier of moe_route_dispatch and moe_route_sigmoid_grouped_dispatch (and
+ * of the forward calls' routing), 0x100
  * moe_selftest_bounded_wait. Synchronises the current device; *code = 0 when
  * no wait has timed out.
  */

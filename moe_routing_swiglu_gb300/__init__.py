@@ -88,6 +88,8 @@ SIGNATURES = {
     "moe_forward_host_workspace_size": (ctypes.c_size_t, [_P, _I64, _I32, ctypes.c_int]),
     "moe_forward_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_sigmoid_grouped": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _OPT, _P, _P, _P, _P]),
+    "moe_route_sigmoid_grouped_dispatch": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _OPT, _P, _P, _P, _P,
+                                                          ctypes.c_int, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_sigmoid_grouped": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _P, _OPT, _P, _P, _P, _P,
                                                    _SZ, _P]),
     "moe_router_weights": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_int, _I32, _ROPT, _P, _P]),
@@ -464,6 +466,44 @@ def moe_route_sigmoid_grouped(logits: torch.Tensor, bias: torch.Tensor | None, o
     _check(lib.moe_route_sigmoid_grouped(_ptr(logits), _dt(logits), T, E, _ptr(bias), ctypes.byref(o),
                                          _ptr(indices), _ptr(weights), _ptr(w32), _stream(stream)))
     return (indices, weights, w32) if w32 is not None else (indices, weights)
+
+
+def moe_route_sigmoid_grouped_dispatch(logits: torch.Tensor, bias: torch.Tensor | None, options,
+                                       x: torch.Tensor | None = None, *, weights_fp32=False, workspace=None,
+                                       stream=None):
+    """moe_route_sigmoid_grouped then moe_dispatch as one launch (the same
+    outputs, bit for bit): returns (indices, weights[, FP32 weights],
+    DispatchedTokens)."""
+    lib = load_library()
+    _dev_tensor(logits, "logits")
+    if bias is not None:
+        _dev_tensor(bias, "bias")
+        if bias.dtype != torch.float32:
+            raise MoeError(3, "bias must be float32")
+    o = _options(options)
+    T, E = logits.shape
+    k = o.top_k
+    dev = logits.device
+    indices = torch.empty(T, k, dtype=torch.int32, device=dev)
+    weights = torch.empty(T, k, dtype=logits.dtype, device=dev)
+    w32 = torch.empty(T, k, dtype=torch.float32, device=dev) if weights_fp32 else None
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_src = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    xd = None
+    H, xdt = 0, MOE_F32
+    if x is not None:
+        _dev_tensor(x, "x")
+        H, xdt = x.shape[1], _dt(x)
+        xd = torch.empty(T * k, H, dtype=x.dtype, device=dev)
+    ws = _workspace(lib.moe_route_dispatch_workspace_size(T, E), dev, workspace)
+    _check(lib.moe_route_sigmoid_grouped_dispatch(_ptr(logits), _dt(logits), T, E, _ptr(bias), ctypes.byref(o),
+                                                  _ptr(indices), _ptr(weights), _ptr(w32), _ptr(x), xdt, H,
+                                                  _ptr(counts), _ptr(offsets), _ptr(row_src), _ptr(inv), _ptr(xd),
+                                                  _ptr(ws), ws.numel(), _stream(stream)))
+    disp = DispatchedTokens(counts, offsets, row_src, inv, xd)
+    return (indices, weights, w32, disp) if w32 is not None else (indices, weights, disp)
 
 
 def moe_forward_sigmoid_grouped(experts: Experts, x: torch.Tensor, logits: torch.Tensor,

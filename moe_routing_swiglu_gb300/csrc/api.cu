@@ -187,22 +187,21 @@ moe_status check_stage_args(const moe_experts* ex, const void* a, const uint32_t
   return check_current_device(ex);
 }
 
-// Softmax routing arguments of moe_forward: route and dispatch then run as
-// one cooperative launch.
-struct SoftmaxRouting {
+// The routing of a forward call: softmax / top-k (grouped == NULL) or the
+// grouped, bias-corrected sigmoid routing. Either runs with the dispatch as
+// one launch.
+struct ForwardRouting {
   const void* logits;
-  bool renormalize;
+  bool renormalize;                      // softmax routing
+  const float* bias;                     // grouped routing: [E] or NULL
+  const moe::GroupRouteParams* grouped;  // NULL: softmax routing
 };
 
-// Route (by the given launch), dispatch, experts, combine: the body of
-// moe_forward and moe_forward_sigmoid_grouped once the routing arguments
-// are checked. With `softmax` set, route and dispatch are the one fused
-// launch (the same bits) and `route` is not called.
-template <typename RouteLaunch>
+// Route + dispatch (one launch), experts, combine: the body of moe_forward
+// and moe_forward_sigmoid_grouped once the routing arguments are checked.
 moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_dtype, int64_t T, int top_k,
                          void* out, uint32_t* indices_opt, void* weights_opt, void* workspace,
-                         size_t workspace_bytes, cudaStream_t s, RouteLaunch route,
-                         const SoftmaxRouting* softmax = nullptr) {
+                         size_t workspace_bytes, cudaStream_t s, const ForwardRouting& routing) {
   if (T > 0 && (x == nullptr || out == nullptr)) return fail(MOE_ERR_NULL, "x and out must be non-NULL");
   const ForwardLayout L = forward_layout(ex, T, top_k);
   if (workspace == nullptr || workspace_bytes < L.total)
@@ -240,20 +239,17 @@ moe_status forward_chain(const moe_experts* ex, const void* x, moe_dtype logits_
   uint32_t* sched = reinterpret_cast<uint32_t*>(ws + L.sched);
   uint32_t* ready = sched + moe::TC_SCHED_BYTES / 4;
   const int64_t n_zero = static_cast<int64_t>(moe::TC_SCHED_BYTES / 4 + ex->E);
-  cudaError_t err;
-  if (softmax != nullptr) {
-    err = moe::launch_route_dispatch(softmax->logits, logits_dtype, T, static_cast<int>(ex->E), top_k,
-                                     softmax->renormalize, indices, weights, nullptr, gather_rows ? nullptr : x,
-                                     ex->dtype, ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch,
-                                     ex->num_sms, s, sched, n_zero);
-    if (err != cudaSuccess) return cuda_fail(err, "forward route + dispatch launch");
-  } else {
-    err = route(indices, weights, s);
-    if (err != cudaSuccess) return cuda_fail(err, "forward route launch");
-    err = moe::launch_dispatch(indices, T, static_cast<int>(ex->E), top_k, gather_rows ? nullptr : x, ex->dtype,
-                               ex->H, counts, offsets, row_src, inv, xd, ws + L.scratch, s, sched, n_zero);
-    if (err != cudaSuccess) return cuda_fail(err, "forward dispatch launch");
-  }
+  const void* xg = gather_rows ? nullptr : x;
+  cudaError_t err =
+      routing.grouped != nullptr
+          ? moe::launch_route_dispatch_grouped(routing.logits, logits_dtype, T, static_cast<int>(ex->E), routing.bias,
+                                               *routing.grouped, indices, weights, nullptr, xg, ex->dtype, ex->H,
+                                               counts, offsets, row_src, inv, xd, ws + L.scratch, ex->num_sms, s,
+                                               sched, n_zero)
+          : moe::launch_route_dispatch(routing.logits, logits_dtype, T, static_cast<int>(ex->E), top_k,
+                                       routing.renormalize, indices, weights, nullptr, xg, ex->dtype, ex->H, counts,
+                                       offsets, row_src, inv, xd, ws + L.scratch, ex->num_sms, s, sched, n_zero);
+  if (err != cudaSuccess) return cuda_fail(err, "forward route + dispatch launch");
   const moe::TcGather gather{x, row_src, top_k, T};
   if (ex->dtype == MOE_F32) {
     st = run_stage(ex, true, xd, gather_rows ? &gather : nullptr, offsets, rows, h, sched, s, nullptr, true);
@@ -401,6 +397,43 @@ moe_status moe_dispatch_noalloc(const uint32_t* indices, int64_t T, int64_t E, i
   return ok();
 }
 
+// The checks moe_route_dispatch and moe_route_sigmoid_grouped_dispatch share
+// beyond the routing's own: maps, x copy, workspace.
+static moe_status check_route_dispatch_maps(int64_t T, int64_t E, const void* x, moe_dtype x_dtype, int64_t H,
+                                            const uint32_t* counts, const uint32_t* offsets,
+                                            const uint32_t* row_src, const uint32_t* inv,
+                                            const void* x_dispatched, const void* workspace,
+                                            size_t workspace_bytes) {
+  if (counts == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "counts and offsets must be non-NULL");
+  if (T > 0 && (row_src == nullptr || inv == nullptr)) return fail(MOE_ERR_NULL, "row_src and inv must be non-NULL");
+  if (x_dispatched != nullptr) {
+    if (x == nullptr) return fail(MOE_ERR_NULL, "x_dispatched needs x");
+    if (!dtype_valid(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+    if (H < 1) return fail(MOE_ERR_SHAPE, "H must be >= 1");
+  }
+  const size_t need = moe::route_dispatch_scratch_bytes(T, E);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_route_dispatch_workspace_size()");
+  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  return MOE_OK;
+}
+
+// No slots: zero counts and offsets, as moe_dispatch writes them.
+static moe_status zero_maps(int64_t E, uint32_t* counts, uint32_t* offsets, cudaStream_t s, const char* what) {
+  cudaError_t err = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, s);
+  if (err != cudaSuccess) return cuda_fail(err, what);
+  return ok();
+}
+
+static moe_status current_sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return cuda_fail(err, "device query");
+  return MOE_OK;
+}
+
 size_t moe_route_dispatch_workspace_size(int64_t T, int64_t E) {
   if (T < 0 || E < 1 || E > moe::ROUTE_MAX_E) return 0;
   return moe::route_dispatch_scratch_bytes(T, E);
@@ -413,32 +446,17 @@ moe_status moe_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_
                               size_t workspace_bytes, void* stream) {
   moe_status st = check_route_args(logits, logits_dtype, T, E, top_k, indices, weights);
   if (st != MOE_OK) return st;
-  if (counts == nullptr || offsets == nullptr) return fail(MOE_ERR_NULL, "counts and offsets must be non-NULL");
-  if (T > 0 && (row_src == nullptr || inv == nullptr)) return fail(MOE_ERR_NULL, "row_src and inv must be non-NULL");
-  if (x_dispatched != nullptr) {
-    if (x == nullptr) return fail(MOE_ERR_NULL, "x_dispatched needs x");
-    if (!dtype_valid(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be MOE_F32, MOE_F16 or MOE_BF16");
-    if (H < 1) return fail(MOE_ERR_SHAPE, "H must be >= 1");
-  }
-  const size_t need = moe::route_dispatch_scratch_bytes(T, E);
-  if (workspace == nullptr || workspace_bytes < need)
-    return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_route_dispatch_workspace_size()");
-  if (!aligned256(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  st = check_route_dispatch_maps(T, E, x, x_dtype, H, counts, offsets, row_src, inv, x_dispatched, workspace,
+                                 workspace_bytes);
+  if (st != MOE_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (T == 0) {
-    // No slots: zero counts and offsets, as moe_dispatch writes them.
-    cudaError_t err = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, s);
-    if (err == cudaSuccess) err = cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, s);
-    if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch: zero counts and offsets");
-    return ok();
-  }
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch: device query");
-  err = moe::launch_route_dispatch(logits, logits_dtype, T, static_cast<int>(E), top_k, renormalize != 0, indices,
-                                   weights, weights_fp32, x, x_dtype, H, counts, offsets, row_src, inv, x_dispatched,
-                                   workspace, sms, s);
+  if (T == 0) return zero_maps(E, counts, offsets, s, "moe_route_dispatch: zero counts and offsets");
+  int sms = 0;
+  st = current_sm_count(&sms);
+  if (st != MOE_OK) return st;
+  cudaError_t err = moe::launch_route_dispatch(logits, logits_dtype, T, static_cast<int>(E), top_k, renormalize != 0,
+                                               indices, weights, weights_fp32, x, x_dtype, H, counts, offsets, row_src,
+                                               inv, x_dispatched, workspace, sms, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_route_dispatch launch");
   return ok();
 }
@@ -650,10 +668,9 @@ moe_status moe_forward(const moe_experts* ex, const void* x, const void* logits,
   if (ex == nullptr) return fail(MOE_ERR_NULL, "experts must be non-NULL");
   moe_status st = check_route_args(logits, logits_dtype, T, ex->E, top_k, logits, logits);
   if (st != MOE_OK) return st;
-  auto route = [&](uint32_t*, void*, cudaStream_t) { return cudaSuccess; };
-  const SoftmaxRouting softmax{logits, renormalize != 0};
+  const ForwardRouting routing{logits, renormalize != 0, nullptr, nullptr};
   return forward_chain(ex, x, logits_dtype, T, top_k, out, indices_opt, weights_opt, workspace,
-                       workspace_bytes, static_cast<cudaStream_t>(stream), route, &softmax);
+                       workspace_bytes, static_cast<cudaStream_t>(stream), routing);
 }
 
 size_t moe_forward_host_workspace_size(const moe_experts* ex, int64_t T, int32_t top_k, moe_dtype logits_dtype) {
@@ -689,9 +706,8 @@ moe_status moe_forward_host(const moe_experts* ex, const void* x_host, const voi
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of x to the device");
   err = cudaMemcpyAsync(dl, logits_host, h.logits_bytes, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of the logits to the device");
-  auto route = [&](uint32_t*, void*, cudaStream_t) { return cudaSuccess; };
-  const SoftmaxRouting softmax{dl, renormalize != 0};
-  st = forward_chain(ex, dx, logits_dtype, T, top_k, dout, indices_opt, weights_opt, ws, h.fwd, s, route, &softmax);
+  const ForwardRouting routing{dl, renormalize != 0, nullptr, nullptr};
+  st = forward_chain(ex, dx, logits_dtype, T, top_k, dout, indices_opt, weights_opt, ws, h.fwd, s, routing);
   if (st != MOE_OK) return st;
   err = cudaMemcpyAsync(out_host, dout, h.out_bytes, cudaMemcpyDeviceToHost, s);
   if (err != cudaSuccess) return cuda_fail(err, "moe_forward_host: copy of out to the host");
@@ -718,6 +734,37 @@ moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype dtype, int64_
   return ok();
 }
 
+moe_status moe_route_sigmoid_grouped_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int64_t E,
+                                              const float* bias, const moe_group_routing_options* options,
+                                              uint32_t* indices, void* weights, float* weights_fp32, const void* x,
+                                              moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                                              uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
+  if (!dtype_valid(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be MOE_F32, MOE_F16 or MOE_BF16");
+  if (E < 1 || E > moe::ROUTE_MAX_E) return fail(MOE_ERR_SHAPE, "E must satisfy 1 <= E <= 1024");
+  moe::GroupRouteParams p{};
+  moe_status st = check_group_options(options, E, &p);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !slots_fit(T, p.k)) return fail(MOE_ERR_SHAPE, "T must be >= 0 and T*top_k < 2^32-1");
+  if (T > 0 && (logits == nullptr || indices == nullptr || weights == nullptr))
+    return fail(MOE_ERR_NULL, "logits, indices and weights must be non-NULL");
+  st = check_bias(bias);
+  if (st != MOE_OK) return st;
+  st = check_route_dispatch_maps(T, E, x, x_dtype, H, counts, offsets, row_src, inv, x_dispatched, workspace,
+                                 workspace_bytes);
+  if (st != MOE_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return zero_maps(E, counts, offsets, s, "moe_route_sigmoid_grouped_dispatch: zero counts and offsets");
+  int sms = 0;
+  st = current_sm_count(&sms);
+  if (st != MOE_OK) return st;
+  cudaError_t err = moe::launch_route_dispatch_grouped(logits, logits_dtype, T, static_cast<int>(E), bias, p, indices,
+                                                       weights, weights_fp32, x, x_dtype, H, counts, offsets, row_src,
+                                                       inv, x_dispatched, workspace, sms, s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_route_sigmoid_grouped_dispatch launch");
+  return ok();
+}
+
 moe_status moe_forward_sigmoid_grouped(const moe_experts* ex, const void* x, const void* logits,
                                        moe_dtype logits_dtype, int64_t T, const float* bias,
                                        const moe_group_routing_options* options, void* out,
@@ -733,12 +780,9 @@ moe_status moe_forward_sigmoid_grouped(const moe_experts* ex, const void* x, con
   if (T > 0 && logits == nullptr) return fail(MOE_ERR_NULL, "logits must be non-NULL");
   st = check_bias(bias);
   if (st != MOE_OK) return st;
-  auto route = [&](uint32_t* indices, void* weights, cudaStream_t s) {
-    return moe::launch_route_sigmoid_grouped(logits, logits_dtype, T, static_cast<int>(ex->E), bias, p,
-                                             indices, weights, nullptr, s);
-  };
+  const ForwardRouting routing{logits, false, bias, &p};
   return forward_chain(ex, x, logits_dtype, T, p.k, out, indices_opt, weights_opt, workspace,
-                       workspace_bytes, static_cast<cudaStream_t>(stream), route);
+                       workspace_bytes, static_cast<cudaStream_t>(stream), routing);
 }
 
 // ---------------------------------------------------------------- first-order training

@@ -83,6 +83,14 @@ cudaError_t launch_route_dispatch(const void* logits, moe_dtype logits_dtype, in
                                   uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
                                   int num_sms, cudaStream_t stream, uint32_t* zero_words = nullptr,
                                   int64_t n_zero = 0);
+// The same with the grouped, bias-corrected sigmoid routing (the same bits as
+// launch_route_sigmoid_grouped followed by launch_dispatch).
+cudaError_t launch_route_dispatch_grouped(const void* logits, moe_dtype logits_dtype, int64_t T, int E,
+                                          const float* bias, const GroupRouteParams& p, uint32_t* indices,
+                                          void* weights, float* weights_fp32, const void* x, moe_dtype x_dtype,
+                                          int64_t H, uint32_t* counts, uint32_t* offsets, uint32_t* row_src,
+                                          uint32_t* inv, void* x_dispatched, void* scratch, int num_sms,
+                                          cudaStream_t stream, uint32_t* zero_words = nullptr, int64_t n_zero = 0);
 
 // ---- K5 combine (combine.cu)
 cudaError_t launch_combine(const void* y_dispatched, moe_dtype dtype, const uint32_t* inv,

@@ -1,16 +1,17 @@
-// K1 + K2 in one cooperative launch: softmax / top-k routing, then the
-// compact per-expert dispatch (ruDNN user guide, section 4 "Routing
-// contract" and section 5 "Expert weights and dispatch": no capacity
-// dropping; a saved mapping restores token order), with the same outputs,
-// bit for bit, as the routing kernel followed by the dispatch kernels.
+// K1 + K2 in one cooperative launch: softmax / top-k routing (ruDNN user
+// guide, section 4 "Routing contract") or the grouped, bias-corrected sigmoid
+// routing (section 10), then the compact per-expert dispatch (section 5
+// "Expert weights and dispatch": no capacity dropping; a saved mapping
+// restores token order), with the same outputs, bit for bit, as the routing
+// kernel followed by the dispatch kernels.
 //
 // Block b owns the contiguous tokens [b*tpb, (b+1)*tpb), so the blocks'
 // slots f = t*k + j come in block order, and the stable layout (rows of an
 // expert in ascending f) is:
 //   row(f) = offsets[e] + (slots of expert e in blocks before b)
 //            + (slots of expert e in block b before f).
-//   1. Route: warp w routes token b*tpb + r*W + w in round r (route_softmax.cuh,
-//      the routing kernel's own code). The top-k experts of one token are
+//   1. Route: warp w routes token b*tpb + r*W + w in round r (route_softmax.cuh
+//      or route_grouped.cuh, the routing kernels' own code). The top-k experts of one token are
 //      distinct, so each warp marks one bit per chosen expert in a 32-bit
 //      per-expert mask; a chosen slot's rank inside the block is the block's
 //      running count of the expert plus the marks of the lower warps. The
@@ -30,6 +31,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "route_grouped.cuh"
 #include "route_softmax.cuh"
 
 namespace moe {
@@ -41,7 +43,7 @@ constexpr uint64_t RD_WAIT_LIMIT_NS = 1000000000ull;  // about a second
 // Warps per block: one token each per round; fewer for large E, whose
 // per-lane logits and keys take more registers (a 32-warp block leaves 64
 // registers a thread).
-template <int V> struct RdWarps { static constexpr int value = V <= 4 ? 32 : (V == 8 ? 16 : 8); };
+template <typename R, int V> struct RdWarps { static constexpr int value = V <= 4 ? 32 : (V == 8 ? 16 : 8); };
 // Batches of at most this many tokens run as one block of this many warps:
 // no grid barrier, and twice the registers of a 32-warp block for the
 // routing chain of each token.
@@ -51,6 +53,8 @@ struct RdArgs {
   const void* logits;
   int64_t T;
   int E, k, renorm;
+  const float* bias;    // grouped routing: [E] or NULL
+  GroupRouteParams gp;  // grouped routing
   uint32_t* indices;
   void* weights;
   float* weights32;
@@ -70,14 +74,57 @@ struct RdArgs {
   uint32_t* status;
 };
 
+// Routing policies: the per-token routing of phase 1, the number of slot
+// registers per lane it returns the chosen experts in (slot j on lane j % 32,
+// register j / 32), and what the block loads once before routing.
+template <typename TL_, int V>
+struct SoftmaxRouter {
+  using TL = TL_;
+  static constexpr int S = V;  // top_k <= E <= 32 * V
+  struct Shared {};
+  __device__ static bool prepare(const RdArgs&, Shared&) { return false; }
+  __device__ static void route(const RdArgs& a, const Shared&, bool, int64_t t, int lane, float* buf,
+                               uint32_t (&sid)[S]) {
+    route_token<TL, V>(static_cast<const TL*>(a.logits), t, a.E, a.k, a.renorm, lane, buf, a.indices,
+                       static_cast<TL*>(a.weights), a.weights32, sid);
+  }
+};
+
+template <typename TL_, int V>
+struct GroupedRouter {
+  using TL = TL_;
+  static constexpr int S = 2;  // top_k <= 64
+  struct Shared {
+    float bias[ROUTE_MAX_E];
+    uint8_t grp[ROUTE_MAX_E];
+  };
+  // The bias (0 without one) and every expert's group id in shared memory;
+  // returns whether any bias is NaN. Called by the whole block.
+  __device__ static bool prepare(const RdArgs& a, Shared& sh) {
+    bool nan = false;
+    for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+      const float b = a.bias != nullptr ? a.bias[i] : 0.0f;
+      sh.bias[i] = b;
+      nan |= isnan(b);
+      sh.grp[i] = static_cast<uint8_t>(i / a.gp.group_size);
+    }
+    return __syncthreads_or(nan) != 0;
+  }
+  __device__ static void route(const RdArgs& a, const Shared& sh, bool bias_nan, int64_t t, int lane, float* buf,
+                               uint32_t (&sid)[S]) {
+    route_token_grouped<TL, V>(static_cast<const TL*>(a.logits), t, a.E, a.gp, sh.bias, sh.grp, bias_nan, lane, buf,
+                               a.indices, static_cast<TL*>(a.weights), a.weights32, sid);
+  }
+};
+
 // Copies x[t] into the dispatched rows of its k slots (slot j's row held on
 // lane j % 32, register j / 32): U units per lane in flight, then k stores.
 // (Stores do not hold registers once issued, so the loads in flight are the
 // only register cost; eight per lane spilled under the 64-register limit of
 // a 32-warp block.)
-template <typename U_T, int V>
+template <typename U_T, int S>
 __device__ __forceinline__ void copy_token(const U_T* __restrict__ x, U_T* __restrict__ xd, int64_t units,
-                                           int64_t t, int k, int lane, const uint32_t (&row)[V]) {
+                                           int64_t t, int k, int lane, const uint32_t (&row)[S]) {
   constexpr int U = 4;
   const U_T* src = x + t * units;
   for (int64_t c0 = 0; c0 < units; c0 += 32 * U) {
@@ -90,7 +137,7 @@ __device__ __forceinline__ void copy_token(const U_T* __restrict__ x, U_T* __res
     for (int j = 0; j < k; ++j) {
       uint32_t rj = 0;
 #pragma unroll
-      for (int q = 0; q < V; ++q)
+      for (int q = 0; q < S; ++q)
         if (q == (j >> 5)) rj = row[q];
       rj = __shfl_sync(FULL_MASK, rj, j & 31);
       U_T* dst = xd + static_cast<int64_t>(rj) * units;
@@ -103,21 +150,21 @@ __device__ __forceinline__ void copy_token(const U_T* __restrict__ x, U_T* __res
   }
 }
 
-template <typename TL, int V, int W>
+template <typename R, int V, int W>
 __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs a) {
+  constexpr int S = R::S;
   __shared__ __align__(16) float e_sm[W * 32 * V];   // phase 1: the warps' exp buffers
   __shared__ uint32_t cnt[ROUTE_MAX_E];              // the block's running count per expert
   __shared__ uint32_t mark[ROUTE_MAX_E];             // phase 1: this round's warp marks; phase 3: first rows
   __shared__ uint32_t warp_sums[32];
   __shared__ int s_abort;
+  __shared__ typename R::Shared router_sm;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = a.E, k = a.k;
   const int nthreads = blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * a.tpb;
   const int64_t t1 = min(a.T, t0 + a.tpb);
   const int rounds = static_cast<int>((a.tpb + W - 1) / W);  // the same in every block
-  const TL* logits = static_cast<const TL*>(a.logits);
-  TL* weights = static_cast<TL*>(a.weights);
 
   // A one-block grid is launched as a programmatic dependent of the previous
   // kernel in the stream: wait for it before touching memory it may use.
@@ -136,6 +183,7 @@ __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs 
       z4[i] = make_uint4(0u, 0u, 0u, 0u);
     if (blockIdx.x == 0 && threadIdx.x < (a.n_zero & 3)) a.zero_words[(n4 << 2) + threadIdx.x] = 0u;
   }
+  const bool router_flag = R::prepare(a, router_sm);  // syncs the block if it loads anything
   __syncthreads();
 
   // ---- 1. route; ranks inside the block
@@ -144,17 +192,17 @@ __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs 
   for (int r = 0; r < rounds; ++r) {
     const int64_t t = t0 + static_cast<int64_t>(r) * W + warp;
     const bool active = t < t1;
-    uint32_t sid[V];
+    uint32_t sid[S];
     if (active) {
-      route_token<TL, V>(logits, t, E, k, a.renorm, lane, my_e, a.indices, weights, a.weights32, sid);
+      R::route(a, router_sm, router_flag, t, lane, my_e, sid);
 #pragma unroll
-      for (int q = 0; q < V; ++q)
+      for (int q = 0; q < S; ++q)
         if (q * 32 + lane < k) atomicOr(&mark[sid[q]], 1u << warp);
     }
     __syncthreads();
     if (active) {
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
+      for (int q = 0; q < S; ++q) {
         const int j = q * 32 + lane;
         if (j < k) a.inv[t * k + j] = cnt[sid[q]] + __popc(mark[sid[q]] & lower_warps);
       }
@@ -258,9 +306,9 @@ __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs 
   for (int r = 0; r < rounds; ++r) {
     const int64_t t = t0 + static_cast<int64_t>(r) * W + warp;
     if (t >= t1) break;
-    uint32_t row[V];
+    uint32_t row[S];
 #pragma unroll
-    for (int q = 0; q < V; ++q) {
+    for (int q = 0; q < S; ++q) {
       const int j = q * 32 + lane;
       row[q] = 0;
       if (j < k) {
@@ -272,17 +320,17 @@ __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs 
     }
     if (a.x != nullptr) {
       if (a.vec16)
-        copy_token<uint4, V>(static_cast<const uint4*>(a.x), static_cast<uint4*>(a.xd), a.row_units, t, k, lane, row);
+        copy_token<uint4, S>(static_cast<const uint4*>(a.x), static_cast<uint4*>(a.xd), a.row_units, t, k, lane, row);
       else
-        copy_token<uint16_t, V>(static_cast<const uint16_t*>(a.x), static_cast<uint16_t*>(a.xd), a.row_units, t, k,
+        copy_token<uint16_t, S>(static_cast<const uint16_t*>(a.x), static_cast<uint16_t*>(a.xd), a.row_units, t, k,
                                 lane, row);
     }
   }
 }
 
-template <typename TL, int V, int W>
+template <typename R, int V, int W>
 cudaError_t launch_rd_v(RdArgs a, int num_sms, cudaStream_t stream) {
-  auto kern = route_dispatch_kernel<TL, V, W>;
+  auto kern = route_dispatch_kernel<R, V, W>;
   static std::atomic<int> occ_cache{0};  // resident blocks per SM (per kernel; one GPU architecture)
   int occ = occ_cache.load(std::memory_order_relaxed);
   if (occ == 0) {
@@ -313,48 +361,46 @@ cudaError_t launch_rd_v(RdArgs a, int num_sms, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <typename TL, int V>
+template <template <typename, int> class Router, typename TL, int V>
 cudaError_t launch_rd_w(const RdArgs& a, int num_sms, cudaStream_t stream) {
-  constexpr int W = RdWarps<V>::value;
+  using R = Router<TL, V>;
+  constexpr int W = RdWarps<R, V>::value;
   if constexpr (W > RD_SMALL_T) {
-    if (a.T <= RD_SMALL_T) return launch_rd_v<TL, V, RD_SMALL_T>(a, num_sms, stream);
+    if (a.T <= RD_SMALL_T) return launch_rd_v<R, V, RD_SMALL_T>(a, num_sms, stream);
   }
-  return launch_rd_v<TL, V, W>(a, num_sms, stream);
+  return launch_rd_v<R, V, W>(a, num_sms, stream);
 }
 
-template <typename TL>
+template <template <typename, int> class Router, typename TL>
 cudaError_t launch_rd_t(const RdArgs& a, int num_sms, cudaStream_t stream) {
-  if (a.E <= 32) return launch_rd_w<TL, 1>(a, num_sms, stream);
-  if (a.E <= 64) return launch_rd_w<TL, 2>(a, num_sms, stream);
-  if (a.E <= 128) return launch_rd_w<TL, 4>(a, num_sms, stream);
-  if (a.E <= 256) return launch_rd_w<TL, 8>(a, num_sms, stream);
-  if (a.E <= 512) return launch_rd_w<TL, 16>(a, num_sms, stream);
-  return launch_rd_w<TL, 32>(a, num_sms, stream);
+  if (a.E <= 32) return launch_rd_w<Router, TL, 1>(a, num_sms, stream);
+  if (a.E <= 64) return launch_rd_w<Router, TL, 2>(a, num_sms, stream);
+  if (a.E <= 128) return launch_rd_w<Router, TL, 4>(a, num_sms, stream);
+  if (a.E <= 256) return launch_rd_w<Router, TL, 8>(a, num_sms, stream);
+  if (a.E <= 512) return launch_rd_w<Router, TL, 16>(a, num_sms, stream);
+  return launch_rd_w<Router, TL, 32>(a, num_sms, stream);
 }
 
-}  // namespace
-
-size_t route_dispatch_scratch_bytes(int64_t T, int64_t E) {
-  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(T, RD_MAX_BLOCKS));
-  return RD_BARRIER_BYTES + align_up(static_cast<size_t>(blocks) * static_cast<size_t>(E) * 4, 256);
+template <template <typename, int> class Router>
+cudaError_t launch_rd_dtype(const RdArgs& a, moe_dtype logits_dtype, int num_sms, cudaStream_t stream) {
+  switch (logits_dtype) {
+    case MOE_F32: return launch_rd_t<Router, float>(a, num_sms, stream);
+    case MOE_F16: return launch_rd_t<Router, __half>(a, num_sms, stream);
+    default: return launch_rd_t<Router, __nv_bfloat16>(a, num_sms, stream);
+  }
 }
 
-cudaError_t launch_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int E, int top_k,
-                                  bool renormalize, uint32_t* indices, void* weights, float* weights_fp32,
-                                  const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
-                                  uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
-                                  int num_sms, cudaStream_t stream, uint32_t* zero_words, int64_t n_zero) {
-  if (T == 0) return cudaSuccess;
+// The arguments both routings share: outputs, x copy, scratch, counters.
+cudaError_t fill_common(RdArgs& a, int64_t T, int E, int top_k, uint32_t* indices, void* weights,
+                        float* weights_fp32, const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts,
+                        uint32_t* offsets, uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
+                        uint32_t* zero_words, int64_t n_zero) {
   uint32_t* status = nullptr;
   cudaError_t err = device_status_ptr(&status);
   if (err != cudaSuccess) return err;
-  uint32_t* barrier = static_cast<uint32_t*>(scratch);
-  RdArgs a{};
-  a.logits = logits;
   a.T = T;
   a.E = E;
   a.k = top_k;
-  a.renorm = renormalize ? 1 : 0;
   a.indices = indices;
   a.weights = weights;
   a.weights32 = weights_fp32;
@@ -372,15 +418,50 @@ cudaError_t launch_route_dispatch(const void* logits, moe_dtype logits_dtype, in
   a.row_src = row_src;
   a.inv = inv;
   a.hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + RD_BARRIER_BYTES);
-  a.barrier = barrier;
+  a.barrier = static_cast<uint32_t*>(scratch);
   a.zero_words = zero_words;
   a.n_zero = n_zero;
   a.status = status;
-  switch (logits_dtype) {
-    case MOE_F32: return launch_rd_t<float>(a, num_sms, stream);
-    case MOE_F16: return launch_rd_t<__half>(a, num_sms, stream);
-    default: return launch_rd_t<__nv_bfloat16>(a, num_sms, stream);
-  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t route_dispatch_scratch_bytes(int64_t T, int64_t E) {
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(T, RD_MAX_BLOCKS));
+  return RD_BARRIER_BYTES + align_up(static_cast<size_t>(blocks) * static_cast<size_t>(E) * 4, 256);
+}
+
+cudaError_t launch_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_t T, int E, int top_k,
+                                  bool renormalize, uint32_t* indices, void* weights, float* weights_fp32,
+                                  const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
+                                  uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
+                                  int num_sms, cudaStream_t stream, uint32_t* zero_words, int64_t n_zero) {
+  if (T == 0) return cudaSuccess;
+  RdArgs a{};
+  cudaError_t err = fill_common(a, T, E, top_k, indices, weights, weights_fp32, x, x_dtype, H, counts, offsets,
+                                row_src, inv, x_dispatched, scratch, zero_words, n_zero);
+  if (err != cudaSuccess) return err;
+  a.logits = logits;
+  a.renorm = renormalize ? 1 : 0;
+  return launch_rd_dtype<SoftmaxRouter>(a, logits_dtype, num_sms, stream);
+}
+
+cudaError_t launch_route_dispatch_grouped(const void* logits, moe_dtype logits_dtype, int64_t T, int E,
+                                          const float* bias, const GroupRouteParams& p, uint32_t* indices,
+                                          void* weights, float* weights_fp32, const void* x, moe_dtype x_dtype,
+                                          int64_t H, uint32_t* counts, uint32_t* offsets, uint32_t* row_src,
+                                          uint32_t* inv, void* x_dispatched, void* scratch, int num_sms,
+                                          cudaStream_t stream, uint32_t* zero_words, int64_t n_zero) {
+  if (T == 0) return cudaSuccess;
+  RdArgs a{};
+  cudaError_t err = fill_common(a, T, E, p.k, indices, weights, weights_fp32, x, x_dtype, H, counts, offsets,
+                                row_src, inv, x_dispatched, scratch, zero_words, n_zero);
+  if (err != cudaSuccess) return err;
+  a.logits = logits;
+  a.bias = bias;
+  a.gp = p;
+  return launch_rd_dtype<GroupedRouter>(a, logits_dtype, num_sms, stream);
 }
 
 }  // namespace moe

@@ -173,3 +173,95 @@ def test_forward_in_a_cuda_graph(cuda_lib, name):
         torch.cuda.synchronize()
         assert _same(out, ref)
     assert moe.moe_device_status() == 0
+
+
+# ---- the grouped, bias-corrected sigmoid routing in the same launch
+
+GOpt = moe_oracle.GroupRoutingOptions
+
+
+def _gopts(r):
+    return GOpt(r.top_k, r.groups, r.selected_groups, r.group_top_two, r.renormalize, r.scale)
+
+
+def _compare_grouped(moe, logits, bias, o, x, E):
+    """moe_route_sigmoid_grouped_dispatch vs moe_route_sigmoid_grouped then
+    moe_dispatch (bit for bit), then vs the oracle."""
+    b = None if bias is None else bias.to(DEV)
+    idx_s, w_s, w32_s = moe.moe_route_sigmoid_grouped(logits, b, o, weights_fp32=True)
+    disp_s = moe.moe_dispatch(idx_s, E, x)
+    idx_f, w_f, w32_f, disp_f = moe.moe_route_sigmoid_grouped_dispatch(logits, b, o, x, weights_fp32=True)
+    torch.cuda.synchronize()
+    n = int(disp_s.offsets[-1])
+    assert _same(idx_f, idx_s) and _same(w_f, w_s) and _same(w32_f, w32_s), "routing outputs differ"
+    assert _same(disp_f.counts, disp_s.counts) and _same(disp_f.offsets, disp_s.offsets)
+    assert _same(disp_f.row_src[:n], disp_s.row_src[:n]) and _same(disp_f.inv, disp_s.inv)
+    assert _same(disp_f.x_dispatched, disp_s.x_dispatched), "x_dispatched differs"
+    ref = moe_oracle.route_sigmoid_grouped(logits.cpu(), bias, o)
+    assert_route_matches(idx_f, w_f, w32_f, ref, logits.dtype)
+    rd = moe_oracle.dispatch(ref.indices, E)
+    assert np.array_equal(u32(disp_f.counts), rd.counts)
+    assert np.array_equal(u32(disp_f.row_src)[:n], rd.row_src)
+    assert np.array_equal(u32(disp_f.inv), rd.inv)
+    assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("name", sorted(workloads.GROUPED))
+def test_grouped_workloads(cuda_lib, name):
+    cfg, r = workloads.GROUPED[name]
+    inp = workloads.generate(cfg, weights=False)
+    x = None if cfg.T * r.top_k <= 8 * cfg.E else inp["x"].to(DEV)
+    _compare_grouped(cuda_lib, inp["logits"].to(DEV), workloads.grouped_bias(cfg.E, r), _gopts(r), x, cfg.E)
+
+
+# (T, E, groups, selected, top_k, top_two): one block, one token per block,
+# a full round and one token more, many rounds; top_k past 32 (the second
+# slot register); the largest E.
+GSHAPES = [(1, 16, 4, 2, 4, True), (33, 64, 8, 3, 6, True), (4865, 128, 8, 4, 8, True), (70000, 8, 2, 1, 2, False),
+           (600, 256, 8, 4, 40, True), (300, 1024, 128, 128, 64, True), (157, 1024, 1, 1, 64, False)]
+
+
+@pytest.mark.parametrize("T,E,groups,sel,k,top_two", GSHAPES)
+def test_grouped_block_shapes(cuda_lib, T, E, groups, sel, k, top_two):
+    g = torch.Generator().manual_seed(T + E * 3 + k)
+    logits = torch.randn(T, E, generator=g).to(torch.bfloat16)
+    bias = (torch.randn(E, generator=g) * 0.02).float()
+    H = 64 if T * k <= 400000 else 16
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    _compare_grouped(cuda_lib, logits.to(DEV), bias, GOpt(k, groups, sel, top_two, True, 2.5), x.to(DEV), E)
+
+
+def test_grouped_contract_rows(cuda_lib):
+    """Quantised ties, +-inf logits, a NaN row; then a NaN bias (every row NaN)."""
+    g = torch.Generator().manual_seed(13)
+    T, E = 157, 96
+    l = torch.round(torch.randn(T, E, generator=g) * 4) / 4
+    l[torch.rand(T, E, generator=g) < 0.05] = float("-inf")
+    l[torch.rand(T, E, generator=g) < 0.02] = float("inf")
+    l[5, 40] = float("nan")
+    b = torch.round(torch.randn(E, generator=g) * 4) / 256
+    x = torch.randn(T, 24, generator=g).to(torch.float32)
+    _compare_grouped(cuda_lib, l.to(DEV), b.float(), GOpt(10, 32, 5, True, False, 1.0), x.to(DEV), E)
+    b[3] = float("nan")
+    _compare_grouped(cuda_lib, l.to(DEV), b.float(), GOpt(10, 32, 5, True, True, 1.0), x.to(DEV), E)
+
+
+@pytest.mark.parametrize("name", ["bf16_fine_grouped", "f16_zipf_grouped", "bf16_decode_grouped"])
+def test_grouped_forward_equals_split_calls(cuda_lib, name):
+    """moe_forward_sigmoid_grouped (routing and dispatch in one launch) gives
+    the bits of the split calls: grouped routing, dispatch, experts, combine."""
+    moe = cuda_lib
+    cfg, r = workloads.GROUPED[name]
+    d = {k: v.to(DEV) for k, v in workloads.generate(cfg).items()}
+    bias = workloads.grouped_bias(cfg.E, r)
+    b = None if bias is None else bias.to(DEV)
+    ex = moe.Experts(d["gate"], d["up"], d["down"])
+    o = _gopts(r)
+    out = moe.moe_forward_sigmoid_grouped(ex, d["x"], d["logits"], b, o)
+    idx, w = moe.moe_route_sigmoid_grouped(d["logits"], b, o)
+    disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+    y = moe.moe_experts_forward_dispatched(ex, disp.x_dispatched, disp.offsets)
+    ref = moe.moe_combine(y, disp.inv, w)
+    torch.cuda.synchronize()
+    assert _same(out, ref)
+    assert moe.moe_device_status() == 0

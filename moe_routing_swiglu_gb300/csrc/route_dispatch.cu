@@ -11,11 +11,12 @@
 //   row(f) = offsets[e] + (slots of expert e in blocks before b)
 //            + (slots of expert e in block b before f).
 //   1. Route: warp w routes token b*tpb + r*W + w in round r (route_softmax.cuh
-//      or route_grouped.cuh, the routing kernels' own code). The top-k experts of one token are
-//      distinct, so each warp marks one bit per chosen expert in a 32-bit
-//      per-expert mask; a chosen slot's rank inside the block is the block's
-//      running count of the expert plus the marks of the lower warps. The
-//      rank goes to inv[f] for now; the block's histogram goes to hist[b].
+//      or route_grouped.cuh, the routing kernels' own code). The top-k
+//      experts of one token are distinct, so each warp marks one bit per
+//      chosen expert in a 32-bit per-expert mask; a chosen slot's rank inside
+//      the block is the block's running count of the expert plus the marks
+//      of the lower warps. The rank goes to inv[f] for now; the block's
+//      histogram goes to hist[b].
 //   2. Grid barrier (one arrival counter, zeroed on the stream before the
 //      launch; the wait is bounded like the GEMMs' waits and records 0x1B).
 //      A grid of one block (batches of up to one block's warps) skips it.
@@ -43,7 +44,7 @@ constexpr uint64_t RD_WAIT_LIMIT_NS = 1000000000ull;  // about a second
 // Warps per block: one token each per round; fewer for large E, whose
 // per-lane logits and keys take more registers (a 32-warp block leaves 64
 // registers a thread).
-template <typename R, int V> struct RdWarps { static constexpr int value = V <= 4 ? 32 : (V == 8 ? 16 : 8); };
+template <int V> struct RdWarps { static constexpr int value = V <= 4 ? 32 : (V == 8 ? 16 : 8); };
 // Batches of at most this many tokens run as one block of this many warps:
 // no grid barrier, and twice the registers of a 32-warp block for the
 // routing chain of each token.
@@ -364,7 +365,7 @@ cudaError_t launch_rd_v(RdArgs a, int num_sms, cudaStream_t stream) {
 template <template <typename, int> class Router, typename TL, int V>
 cudaError_t launch_rd_w(const RdArgs& a, int num_sms, cudaStream_t stream) {
   using R = Router<TL, V>;
-  constexpr int W = RdWarps<R, V>::value;
+  constexpr int W = RdWarps<V>::value;
   if constexpr (W > RD_SMALL_T) {
     if (a.T <= RD_SMALL_T) return launch_rd_v<R, V, RD_SMALL_T>(a, num_sms, stream);
   }

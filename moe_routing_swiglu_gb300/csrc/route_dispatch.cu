@@ -244,6 +244,42 @@ __global__ void __launch_bounds__(W * 32, 1) route_dispatch_kernel(const RdArgs 
   __syncthreads();
   if (gridDim.x == 1) {
     for (int e = threadIdx.x; e < E; e += nthreads) tot[e] = cnt[e];
+  } else if ((E & 3) == 0 && nthreads % (E >> 2) == 0) {
+    // 16-byte vectors of four experts: consecutive threads read consecutive
+    // vectors of a histogram row (coalesced), each thread every
+    // (nthreads / (E/4))-th row, all its loads in flight at once; the sums
+    // meet in shared memory.
+    const int G = gridDim.x, b = blockIdx.x, E4 = E >> 2;
+    const uint4* hist4 = reinterpret_cast<const uint4*>(a.hist);
+    const int e4 = threadIdx.x % E4, rstep = nthreads / E4;
+    constexpr int U = 8;
+    uint32_t all[4] = {0u, 0u, 0u, 0u}, bef[4] = {0u, 0u, 0u, 0u};
+    for (int c = threadIdx.x / E4; c < G; c += U * rstep) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        v[u] = c + u * rstep < G ? __ldcg(hist4 + static_cast<int64_t>(c + u * rstep) * E4 + e4)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool early = c + u * rstep < b;
+        all[0] += v[u].x;
+        all[1] += v[u].y;
+        all[2] += v[u].z;
+        all[3] += v[u].w;
+        bef[0] += early ? v[u].x : 0u;
+        bef[1] += early ? v[u].y : 0u;
+        bef[2] += early ? v[u].z : 0u;
+        bef[3] += early ? v[u].w : 0u;
+      }
+    }
+    if (threadIdx.x / E4 < G) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        atomicAdd(&tot[4 * e4 + i], all[i]);
+        atomicAdd(&before[4 * e4 + i], bef[i]);
+      }
+    }
   } else {
     const int G = gridDim.x, b = blockIdx.x;
     const int S = nthreads >= 2 * E ? nthreads / E : 1;  // segments of the histogram rows per expert

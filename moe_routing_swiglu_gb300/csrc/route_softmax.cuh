@@ -155,10 +155,11 @@ __device__ __forceinline__ void route_token(const TL* __restrict__ logits, int64
       kl[v] = real ? 0xFFFFu - id : 0u;
     }
   }
-  // k rounds of arg-max; slot j's id ends on lane j % 32, register j / 32.
+  // k rounds of arg-max; slot j's id ends on lane j % 32, register j / 32
+  // (while k <= 32, the usual case, every slot sits in register 0).
 #pragma unroll
   for (int q = 0; q < V; ++q) slot_id[q] = 0;
-  for (int j = 0; j < k; ++j) {
+  auto arg_max_round = [&]() -> uint32_t {
     uint32_t bh = kh[0];
 #pragma unroll
     for (int v = 1; v < V; ++v) bh = max(bh, kh[v]);
@@ -179,10 +180,21 @@ __device__ __forceinline__ void route_token(const TL* __restrict__ logits, int64
       for (int v = 0; v < V; ++v)
         if (v == slot) kh[v] = 0u;
     }
-    if (lane == (j & 31)) {
+    return id;
+  };
+  if (k <= 32) {
+    for (int j = 0; j < k; ++j) {
+      const uint32_t id = arg_max_round();
+      if (lane == j) slot_id[0] = id;
+    }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const uint32_t id = arg_max_round();
+      if (lane == (j & 31)) {
 #pragma unroll
-      for (int q = 0; q < V; ++q)
-        if (q == (j >> 5)) slot_id[q] = id;
+        for (int q = 0; q < V; ++q)
+          if (q == (j >> 5)) slot_id[q] = id;
+      }
     }
   }
 
@@ -195,7 +207,10 @@ __device__ __forceinline__ void route_token(const TL* __restrict__ logits, int64
     if (q * 32 < k && j < k) p[q] = __fdiv_rn(my_e[slot_id[q]], s);  // registers holding slots only
   }
   float z = 0.0f;
-  if (renormalize) {
+  if (renormalize && k <= 32) {
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) z = __fadd_rn(z, __shfl_sync(FULL_MASK, p[0], j));
+  } else if (renormalize) {
     for (int j = 0; j < k; ++j) {
       float pj = 0.0f;
 #pragma unroll

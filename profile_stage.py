@@ -17,7 +17,8 @@ through row_src), down, experts (gate/up and down chained in one launch),
 experts_combine (gate/up, down and the weighted combine in one launch:
 moe_experts_forward_combine), combine, forward (moe_forward), and
 route_grouped (the grouped sigmoid routing, on workloads that have a grouped
-variant in ``workloads.GROUPED``), backward (the experts' backward of
+variant in ``workloads.GROUPED``), route_grouped_dispatch (the same routing
+with the dispatch in one launch), backward (the experts' backward of
 first-order training on a random output gradient) and combine_backward (the
 combine's backward on a random output gradient).
 """
@@ -45,7 +46,7 @@ def main(argv=None):
     names["coarse_E2"] = workloads.CONFIGS[2].scaled("bf16_prefill_T2048_H4096_I14336_E2_k2", T=2048, E=2)
     ap.add_argument("--workload", default="cfg1", choices=sorted(names))
     ap.add_argument("--stage", default="gate_up",
-                    choices=["route", "dispatch", "route_dispatch", "gate_up", "gate_up_gather", "down", "experts", "experts_combine",
+                    choices=["route", "dispatch", "route_dispatch", "route_grouped_dispatch", "gate_up", "gate_up_gather", "down", "experts", "experts_combine",
                              "combine", "forward", "route_grouped", "backward", "combine_backward"])
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
@@ -60,7 +61,7 @@ def main(argv=None):
     h = moe.moe_experts_gate_up(ex, disp.x_dispatched, disp.offsets)
     y = moe.moe_experts_down(ex, h, disp.offsets)
     grouped = [r for c, r in workloads.GROUPED.values() if c is cfg]
-    if args.stage == "route_grouped":
+    if args.stage in ("route_grouped", "route_grouped_dispatch"):
         if not grouped:
             ap.error(f"{args.workload} has no grouped-routing variant")
         r = grouped[0]
@@ -102,6 +103,9 @@ def main(argv=None):
                                             workspace=comb_ws)
         elif args.stage == "route_grouped":
             moe.moe_route_sigmoid_grouped(d["logits"], bias, opts, indices=idx, weights=w)
+        elif args.stage == "route_grouped_dispatch":  # one launch, as moe_forward_sigmoid_grouped runs it
+            gather = cfg.T * cfg.top_k <= 8 * cfg.E
+            moe.moe_route_sigmoid_grouped_dispatch(d["logits"], bias, opts, None if gather else d["x"])
         elif args.stage == "backward":
             moe.moe_experts_backward(ex, cache, dy)
         elif args.stage == "combine":

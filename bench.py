@@ -12,8 +12,9 @@ one replay bracketed by CUDA events on the launching stream, and L2 is
 flushed between steps outside the events (a 256 MiB write, then a 256 MiB
 read so the flush's dirty lines are written back before the step). The
 per-stage times come from a second run that launches the C-ABI stage calls
-(route, dispatch, the experts' GEMMs, combine) directly with events between
-the stages. Under torchrun each rank runs its own T-token shard of an
+(route + dispatch as one launch, the experts' GEMMs, combine: the kernels
+moe_forward runs) directly with events between the stages, and a third with
+the routing and the dispatch as separate calls. Under torchrun each rank runs its own T-token shard of an
 N*T-token global batch (weak scaling, replicated experts, no collective on
 the data path); the time is the maximum over ranks.
 
@@ -25,7 +26,8 @@ oracle baseline, kernel launches and the SM clocks seen during the run; then,
 as extra keys, the fine-grained BF16 prefill (T=4096, E=128, top_k=8) step
 with its GEMM roofline, the decode workload's HBM GB/s over the touched
 expert weights, the Zipf-skewed F16 prefill's GEMMs, the grouped sigmoid
-routing on the fine-grained prefill, and one first-order training step there.
+routing on the fine-grained prefill, and one first-order training step on the
+fine-grained and on the coarse prefill.
 
 --impl reference times the CPU oracle (the only reference this path has) on
 bounded samples of the headline workload.

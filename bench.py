@@ -278,6 +278,17 @@ class Chain:
         if rc:
             raise RuntimeError("a C-ABI call failed: " + lib.moe_last_error().decode())
 
+    def route_dispatch_maps(self, stream):
+        """The one route + dispatch launch without the x copy (indices,
+        weights and the dispatch maps only)."""
+        c, lib, P = self.cfg, self.lib, self.moe._ptr
+        rc = lib.moe_route_dispatch(P(self.d["logits"]), self.dt, c.T, c.E, c.top_k, int(c.renormalize),
+                                    P(self.idx), P(self.w), None, None, self.dt, c.H, P(self.counts),
+                                    P(self.offsets), P(self.row_src), P(self.inv), None, P(self.rdws),
+                                    self.rdws.numel(), ctypes.c_void_p(stream.cuda_stream))
+        if rc:
+            raise RuntimeError("moe_route_dispatch failed: " + lib.moe_last_error().decode())
+
     def forward(self, stream):
         """The whole chain as one moe_forward call (what a user runs)."""
         c, lib, P = self.cfg, self.lib, self.moe._ptr
@@ -332,6 +343,22 @@ def timed_steps(chain, stream, flush, steps, warmup):
                        for i in range(steps)]) / 1e3
     total = float(sum(evs[i][0].elapsed_time(evs[i][N_STAGES]) for i in range(steps))) / 1e3
     return stages.mean(axis=0), total
+
+
+def timed_calls(fn, stream, flush, steps, warmup):
+    """Mean seconds of fn(stream) between CUDA events, L2 flushed before each."""
+    for _ in range(warmup):
+        flush()
+        fn(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
 
 
 def capture_step(chain):
@@ -626,6 +653,7 @@ def forward_measure(moe, cfg, dev, stream, flush, steps, warmup, world, shard=0,
     split, _ = timed_steps(chain, stream, flush, n_stage, warmup)
     chain.split_route = False
     split = [float(x) for x in split]
+    maps_only = timed_calls(chain.route_dispatch_maps, stream, flush, n_stage, warmup)
     fused = None
     if not chain.gather:
         chain.fused = True
@@ -637,6 +665,7 @@ def forward_measure(moe, cfg, dev, stream, flush, steps, warmup, world, shard=0,
                  "fused_staged_step_us": round(f_total / n_stage * 1e6, 2),
                  "staged_step_us": round(stage_total / n_stage * 1e6, 2)}
     return chain, {"total_s": total, "steps": steps, "stages_s": stages, "split_stages_s": split,
+                   "maps_only_s": maps_only,
                    "stage_steps": n_stage,
                    "stage_total_s": stage_total, "touched": chain.touched_experts(), "fused_ab": fused}
 
@@ -739,7 +768,9 @@ def run_ours(args, rank, world, local_rank):
         """The one route + dispatch launch moe_forward runs, and beside it
         moe_route then moe_dispatch (the split API's kernels)."""
         st, sp = r["stages_s"], r["split_stages_s"]
-        return {"total": round((st[0] + st[1]) * 1e6, 2), "split_route": round(sp[0] * 1e6, 2),
+        return {"total": round((st[0] + st[1]) * 1e6, 2),
+                "maps_only": round(r["maps_only_s"] * 1e6, 2),  # the same launch without the x copy
+                "split_route": round(sp[0] * 1e6, 2),
                 "split_dispatch": round(sp[1] * 1e6, 2), "split_total": round((sp[0] + sp[1]) * 1e6, 2)}
 
     line = {

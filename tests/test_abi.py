@@ -96,6 +96,58 @@ def test_dispatch_workspace_size(lib):
     assert lib.moe_dispatch_workspace_size(0, 8, 2) % 256 == 0
 
 
+def _route_dispatch(lib, logits=FAKE, ldt=2, T=4, E=8, k=2, idx=FAKE, w=FAKE, x=None, xdt=2, H=0, counts=FAKE,
+                    offsets=FAKE, row_src=FAKE, inv=FAKE, xd=None, ws=P(0x200000), ws_bytes=1 << 20):
+    return lib.moe_route_dispatch(logits, ldt, T, E, k, 1, idx, w, None, x, xdt, H, counts, offsets, row_src, inv,
+                                  xd, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(w=None), 1), (dict(counts=None), 1),
+    (dict(offsets=None), 1), (dict(row_src=None), 1), (dict(inv=None), 1),
+    (dict(xd=FAKE), 1),                                   # x_dispatched without x
+    (dict(xd=FAKE, x=FAKE, H=16, xdt=7), 3), (dict(xd=FAKE, x=FAKE, H=0), 2),
+    (dict(ldt=5), 3), (dict(E=0, k=1), 2), (dict(E=1025), 2), (dict(T=-1), 2),
+    (dict(k=0), 4), (dict(k=9), 4),
+    (dict(ws=None), 6), (dict(ws_bytes=256), 6),          # the histograms need more than the barrier word
+    (dict(ws=P(0x200010)), 5),
+])
+def test_route_dispatch_rejects_bad_arguments(lib, kwargs, status):
+    """Every check runs on the host before anything is enqueued."""
+    assert _route_dispatch(lib, **kwargs) == status
+    assert lib.moe_last_error().decode() != ""
+
+
+def test_route_dispatch_workspace_size(lib):
+    """256 bytes for the barrier word, then one E-word histogram per block
+    (at most one block per token, at most 2048 blocks)."""
+    assert lib.moe_route_dispatch_workspace_size(-1, 8) == 0
+    assert lib.moe_route_dispatch_workspace_size(4, 0) == 0
+    assert lib.moe_route_dispatch_workspace_size(4, 1025) == 0
+    for T, E in [(0, 8), (1, 1), (16, 128), (4096, 128), (70000, 8), (300, 1024)]:
+        n = lib.moe_route_dispatch_workspace_size(T, E)
+        assert n % 256 == 0 and n >= 256 + min(max(T, 1), 2048) * E * 4
+    assert lib.moe_route_dispatch_workspace_size(10 ** 6, 128) == lib.moe_route_dispatch_workspace_size(2048, 128)
+
+
+def test_grouped_route_dispatch_rejects_bad_arguments(lib):
+    o = moe.GroupRoutingOptions(2, 4, 2, True, True, 1.0)
+    bad = moe.GroupRoutingOptions(0, 4, 2, True, True, 1.0)
+
+    def call(opts=o, E=8, counts=FAKE, ws=P(0x200000), ws_bytes=1 << 20, bias=None):
+        return lib.moe_route_sigmoid_grouped_dispatch(FAKE, 2, 4, E, bias, None if opts is None else ctypes.byref(opts),
+                                                      FAKE, FAKE, None, None, 2, 0, counts, FAKE, FAKE, FAKE, None,
+                                                      ws, ws_bytes, None)
+
+    assert call(opts=None) == 1
+    assert call(opts=bad) == 4
+    assert call(E=0) == 2
+    assert call(counts=None) == 1
+    assert call(ws=None) == 6
+    assert call(ws=P(0x200010)) == 5
+    assert call(bias=P(0x100002)) == 5
+
+
 def _create(lib, gate=FAKE, up=FAKE, down=FAKE, dtype=2, E=8, H=64, I=128, out=True):
     h = ctypes.c_void_p()
     return lib.moe_experts_create(gate, up, down, dtype, E, H, I, ctypes.byref(h) if out else None)

@@ -174,18 +174,17 @@ __device__ __forceinline__ void route_token(const TL* __restrict__ logits, int64
       bl = __reduce_max_sync(FULL_MASK, bl);
       id = 0xFFFFu - bl;
     }
-    if (lane == static_cast<int>(id / V)) {
-      const int slot = static_cast<int>(id % V);
+    // The owner lane zeroes the taken key (selects, no divergent branch).
+    const bool mine = lane == static_cast<int>(id / V);
+    const uint32_t slot = id % V;
 #pragma unroll
-      for (int v = 0; v < V; ++v)
-        if (v == slot) kh[v] = 0u;
-    }
+    for (int v = 0; v < V; ++v) kh[v] = (mine && static_cast<uint32_t>(v) == slot) ? 0u : kh[v];
     return id;
   };
   if (k <= 32) {
     for (int j = 0; j < k; ++j) {
       const uint32_t id = arg_max_round();
-      if (lane == j) slot_id[0] = id;
+      slot_id[0] = lane == j ? id : slot_id[0];
     }
   } else {
     for (int j = 0; j < k; ++j) {

@@ -64,7 +64,10 @@ const char* moe_status_string(int status);
 /* Detail of the last failed call on this host thread (empty if none). */
 const char* moe_last_error(void);
 
-/* ABI version of this library (major * 10000 + minor * 100 + patch). */
+/* ABI version of this library (major * 10000 + minor * 100 + patch): 1.1.0
+ * adds moe_experts_forward_combine, moe_route_dispatch and
+ * moe_route_sigmoid_grouped_dispatch to 1.0.0; nothing was removed or
+ * changed. */
 int moe_version(void);
 
 /*

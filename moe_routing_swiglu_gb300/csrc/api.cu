@@ -324,7 +324,7 @@ const char* moe_status_string(int status) {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-int moe_version(void) { return 10000; }
+int moe_version(void) { return 10100; }
 
 moe_status moe_route(const void* logits, moe_dtype dtype, int64_t T, int64_t E, int32_t top_k,
                      int32_t renormalize, uint32_t* indices, void* weights, float* weights_fp32,

@@ -44,7 +44,7 @@ def test_status_strings(lib):
     for code, name in moe.STATUS_NAMES.items():
         assert lib.moe_status_string(code).decode() == name
     assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"
-    assert lib.moe_version() == 10000
+    assert lib.moe_version() == 10100
 
 
 P = ctypes.c_void_p

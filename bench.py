@@ -514,7 +514,8 @@ def gemm_stage_times(moe, cfg, dev, stream, flush, steps):
 
 def training_step_times(moe, cfg, dev, stream, flush, steps):
     """One first-order training step on a workload (ruDNN user guide, section
-    12): forward (route, dispatch, training forward of the experts, combine)
+    12): forward (route + dispatch in one launch, training forward of the
+    experts, combine)
     then backward (combine backward, experts backward, dispatch backward,
     router backward of the softmax weights). Returns mean seconds per stage
     (forward, combine_backward, experts_backward, dispatch_backward,
@@ -530,8 +531,7 @@ def training_step_times(moe, cfg, dev, stream, flush, steps):
     def step(ev=None):
         rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
         rec(0)
-        idx, w = moe.moe_route(d["logits"], cfg.top_k, cfg.renormalize)
-        disp = moe.moe_dispatch(idx, cfg.E, d["x"])
+        idx, w, disp = moe.moe_route_dispatch(d["logits"], cfg.top_k, cfg.renormalize, d["x"])
         y, cache = moe.moe_experts_forward_training(ex, disp.x_dispatched, disp.offsets)
         moe.moe_combine(y, disp.inv, w)
         rec(1)

@@ -79,6 +79,16 @@ def test_block_shapes(cuda_lib, T, E, k):
     _compare(cuda_lib, logits.to(DEV), k, True, x.to(DEV), E)
 
 
+def test_many_rounds_per_block(cuda_lib):
+    """T = 131072 (862 tokens a block, 27 rounds of 32 warps), E = 128, top_k
+    = 8: a million slots, block histograms in the thousands."""
+    g = torch.Generator().manual_seed(77)
+    T, E, k = 131072, 128, 8
+    logits = torch.randn(T, E, generator=g).to(torch.bfloat16)
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    _compare(cuda_lib, logits.to(DEV), k, True, x.to(DEV), E)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("E,k,renorm", [(1, 1, True), (3, 3, False), (33, 5, True), (64, 64, True),
                                         (1000, 7, False), (1024, 1, True)])

@@ -65,9 +65,9 @@ const char* moe_status_string(int status);
 const char* moe_last_error(void);
 
 /* ABI version of this library (major * 10000 + minor * 100 + patch): 1.1.0
- * adds moe_experts_forward_combine, moe_route_dispatch and
- * moe_route_sigmoid_grouped_dispatch to 1.0.0; nothing was removed or
- * changed. */
+ * adds moe_experts_forward_combine, moe_route_dispatch,
+ * moe_route_sigmoid_grouped_dispatch and moe_permute_rows to 1.0.0; nothing
+ * was removed or changed. */
 int moe_version(void);
 
 /*
@@ -181,6 +181,29 @@ moe_status moe_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_
                               const void* x, moe_dtype x_dtype, int64_t H, uint32_t* counts, uint32_t* offsets,
                               uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* workspace,
                               size_t workspace_bytes, void* stream);
+
+/*
+ * moe_permute_rows - move whole rows by an index: the reorders of the
+ * expert-parallel exchange (the received rows into expert-major order, the
+ * experts' outputs back into the received order); the exchange itself is the
+ * caller's collective. Not on the pages: they run every expert on one device.
+ *
+ *   src           device, [src_rows, row_bytes] (rows contiguous).
+ *   dst           device, [dst_rows, row_bytes]; must not overlap src.
+ *   index         device, [rows] int64.
+ *   scatter       zero: gather, dst[r] = src[index[r]] for r < rows
+ *                 (rows <= dst_rows); a row whose index is outside
+ *                 0..src_rows-1 is written as zeros. Nonzero: scatter,
+ *                 dst[index[r]] = src[r] for r < rows (rows <= src_rows); a
+ *                 row whose index is outside 0..dst_rows-1 is skipped, and
+ *                 repeated indexes leave one of their rows (unspecified).
+ *   row_bytes     > 0; 16-byte rows and pointers move as 16-byte vectors.
+ *
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE (negative sizes, row_bytes < 1, rows
+ * beyond the written or read side). Enqueued on the stream, no host sync.
+ */
+moe_status moe_permute_rows(const void* src, int64_t src_rows, void* dst, int64_t dst_rows, const int64_t* index,
+                            int64_t rows, int64_t row_bytes, int32_t scatter, void* stream);
 
 /*
  * moe_experts_create - validate and wrap bias-free SwiGLU expert weights

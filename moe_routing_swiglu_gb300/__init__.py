@@ -71,6 +71,7 @@ SIGNATURES = {
     "moe_route_dispatch_workspace_size": (_SZ, [_I64, _I64]),
     "moe_route_dispatch": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I32, _I32, _P, _P, _P, _P, ctypes.c_int,
                                           _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_rows": (ctypes.c_int, [_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _P]),
     "moe_experts_create": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                           ctypes.POINTER(ctypes.c_void_p)]),
     "moe_experts_destroy": (None, [_P]),
@@ -248,6 +249,27 @@ def moe_route_dispatch(logits: torch.Tensor, top_k: int, renormalize: bool, x: t
                                   _ptr(row_src), _ptr(inv), _ptr(xd), _ptr(ws), ws.numel(), _stream(stream)))
     disp = DispatchedTokens(counts, offsets, row_src, inv, xd)
     return (indices, weights, w32, disp) if w32 is not None else (indices, weights, disp)
+
+
+def moe_permute_rows(src: torch.Tensor, index: torch.Tensor, *, scatter: bool = False, out=None,
+                     out_rows: int | None = None, stream=None) -> torch.Tensor:
+    """Row moves by an int64 index on the device: gather out[r] = src[index[r]]
+    (out has index.numel() rows), or with scatter out[index[r]] = src[r] (out
+    has out_rows rows, default src's)."""
+    lib = load_library()
+    _dev_tensor(src, "src")
+    _dev_tensor(index, "index")
+    if index.dtype != torch.int64:
+        raise MoeError(3, "index must be int64")
+    rows = index.numel()
+    row_shape = tuple(src.shape[1:])
+    if out is None:
+        n_out = (out_rows if out_rows is not None else src.shape[0]) if scatter else rows
+        out = torch.empty((n_out,) + row_shape, dtype=src.dtype, device=src.device)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 1
+    _check(lib.moe_permute_rows(_ptr(src), src.shape[0], _ptr(out), out.shape[0], _ptr(index), rows, row_bytes,
+                                int(bool(scatter)), _stream(stream)))
+    return out
 
 
 def moe_dispatch_noalloc(indices: torch.Tensor, num_experts: int, x: torch.Tensor | None = None,

@@ -461,6 +461,21 @@ moe_status moe_route_dispatch(const void* logits, moe_dtype logits_dtype, int64_
   return ok();
 }
 
+moe_status moe_permute_rows(const void* src, int64_t src_rows, void* dst, int64_t dst_rows, const int64_t* index,
+                            int64_t rows, int64_t row_bytes, int32_t scatter, void* stream) {
+  if (src_rows < 0 || dst_rows < 0 || rows < 0 || row_bytes < 1)
+    return fail(MOE_ERR_SHAPE, "row counts must be >= 0 and row_bytes >= 1");
+  if (rows > (scatter != 0 ? src_rows : dst_rows))
+    return fail(MOE_ERR_SHAPE, "rows exceeds the rows of the side read or written in order");
+  if (rows == 0) return ok();
+  if (src == nullptr || dst == nullptr || index == nullptr)
+    return fail(MOE_ERR_NULL, "src, dst and index must be non-NULL");
+  cudaError_t err = moe::launch_permute_rows(src, src_rows, dst, dst_rows, index, rows, row_bytes, scatter != 0,
+                                             static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_permute_rows launch");
+  return ok();
+}
+
 moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dtype,
                               int64_t E, int64_t H, int64_t I, moe_experts** out) {
   if (out == nullptr) return fail(MOE_ERR_NULL, "out must be non-NULL");

@@ -218,6 +218,51 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const VecT* __rest
   }
 }
 
+// Row moves by an index, warp per row: gather dst[r] = src[index[r]]
+// (a row whose index is outside src is written as zeros), or scatter
+// dst[index[r]] = src[r] (a row whose index is outside dst is skipped).
+template <typename VecT, bool SCATTER>
+__global__ void __launch_bounds__(256) permute_rows_kernel(const VecT* __restrict__ src, int64_t src_rows,
+                                                           VecT* __restrict__ dst, int64_t dst_rows,
+                                                           const int64_t* __restrict__ index, int64_t rows,
+                                                           int64_t vec_per_row) {
+  grid_dependency_wait();
+  launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = warp0; r < rows; r += nwarps) {
+    const int64_t i = index[r];
+    if constexpr (SCATTER) {
+      if (i < 0 || i >= dst_rows) continue;
+      const VecT* s = src + r * vec_per_row;
+      VecT* d = dst + i * vec_per_row;
+      for (int64_t c = lane; c < vec_per_row; c += 32) d[c] = s[c];
+    } else {
+      VecT* d = dst + r * vec_per_row;
+      if (i < 0 || i >= src_rows) {
+        for (int64_t c = lane; c < vec_per_row; c += 32) d[c] = VecT{};
+        continue;
+      }
+      const VecT* s = src + i * vec_per_row;
+      for (int64_t c = lane; c < vec_per_row; c += 32) d[c] = s[c];
+    }
+  }
+}
+
+template <typename VecT>
+cudaError_t launch_permute_t(const void* src, int64_t src_rows, void* dst, int64_t dst_rows, const int64_t* index,
+                             int64_t rows, int64_t vec_per_row, bool scatter, cudaStream_t stream) {
+  const int64_t blocks64 = (rows + 7) / 8;
+  const int blocks = static_cast<int>(blocks64 < 16384 ? blocks64 : 16384);
+  const VecT* s = static_cast<const VecT*>(src);
+  VecT* d = static_cast<VecT*>(dst);
+  return scatter ? launch_dependent(permute_rows_kernel<VecT, true>, dim3(blocks), dim3(256), 0, stream, s, src_rows,
+                                    d, dst_rows, index, rows, vec_per_row)
+                 : launch_dependent(permute_rows_kernel<VecT, false>, dim3(blocks), dim3(256), 0, stream, s, src_rows,
+                                    d, dst_rows, index, rows, vec_per_row);
+}
+
 // Fixed scratch of moe_dispatch_noalloc. Every GPU that loads this library
 // holds this array (1 MiB) in its device image until the process exits; all
 // calls on a device share it.
@@ -233,6 +278,19 @@ cudaError_t noalloc_dispatch_scratch(void** ptr) {
   // stale after cudaDeviceReset, which unloads the module and drops the array.
   *ptr = nullptr;
   return cudaGetSymbolAddress(ptr, g_noalloc_dispatch_scratch);
+}
+
+cudaError_t launch_permute_rows(const void* src, int64_t src_rows, void* dst, int64_t dst_rows,
+                                const int64_t* index, int64_t rows, int64_t row_bytes, bool scatter,
+                                cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const bool v16 = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dst) % 16 == 0;
+  const bool v4 = row_bytes % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 4 == 0 &&
+                  reinterpret_cast<uintptr_t>(dst) % 4 == 0;
+  if (v16) return launch_permute_t<uint4>(src, src_rows, dst, dst_rows, index, rows, row_bytes / 16, scatter, stream);
+  if (v4) return launch_permute_t<uint32_t>(src, src_rows, dst, dst_rows, index, rows, row_bytes / 4, scatter, stream);
+  return launch_permute_t<uint8_t>(src, src_rows, dst, dst_rows, index, rows, row_bytes, scatter, stream);
 }
 
 size_t dispatch_scratch_bytes(int64_t T, int64_t E, int top_k) {

@@ -69,6 +69,13 @@ cudaError_t launch_dispatch(const uint32_t* indices, int64_t T, int E, int top_k
                             uint32_t* row_src, uint32_t* inv, void* x_dispatched, void* scratch,
                             cudaStream_t stream, uint32_t* zero_words = nullptr, int64_t n_zero = 0);
 
+// Row moves by an int64 index (the expert-parallel exchange's reorders):
+// gather dst[r] = src[index[r]] (out-of-range index: zero row) or scatter
+// dst[index[r]] = src[r] (out-of-range index: skipped).
+cudaError_t launch_permute_rows(const void* src, int64_t src_rows, void* dst, int64_t dst_rows,
+                                const int64_t* index, int64_t rows, int64_t row_bytes, bool scatter,
+                                cudaStream_t stream);
+
 // ---- K1 + K2 in one cooperative launch (route_dispatch.cu): softmax routing,
 // then the dispatch maps and (x_dispatched != NULL) the x copy; the same bits
 // as launch_route followed by launch_dispatch. scratch: RD_BARRIER_BYTES for

@@ -23,8 +23,10 @@ The pages describe the local chain only; this sharding is the expert-parallel
 extension of its dispatch and combine contract (ruDNN user guide, section 5
 "Expert weights and dispatch" and section 6 "Call MoE"). The plan and the
 exchanges here use torch.distributed collectives (NCCL on GPUs, gloo on the
-CPU) and torch index operations; the experts and the combine are the
-library's kernels.
+CPU); on CUDA tensors the two reorders (steps 3 and 4) run the library's
+row-move kernel (moe_permute_rows), and the experts and the combine are the
+library's kernels too. On CPU tensors (the plan's gloo tests) the reorders
+are torch indexing.
 """
 from __future__ import annotations
 
@@ -33,6 +35,14 @@ from typing import Callable
 
 import torch
 import torch.distributed as dist
+
+
+def _moe():
+    """The library's Python binding (imported on first use: the plan itself
+    needs no GPU)."""
+    import moe_routing_swiglu_gb300 as moe
+
+    return moe
 
 
 def expert_range(E: int, world: int, rank: int) -> tuple[int, int]:
@@ -101,6 +111,8 @@ def ep_dispatch_rows(x_dispatched: torch.Tensor, plan: EpPlan, group=None) -> to
     H = x_dispatched.shape[1]
     recv = x_dispatched.new_empty(sum(plan.recv_splits), H)
     dist.all_to_all_single(recv, x_dispatched.contiguous(), plan.recv_splits, plan.send_splits, group=group)
+    if recv.is_cuda:  # the library's row-move kernel
+        return _moe().moe_permute_rows(recv, plan.perm, scatter=True)
     local = torch.empty_like(recv)
     local[plan.perm] = recv
     return local
@@ -110,7 +122,10 @@ def ep_return_rows(y_local: torch.Tensor, plan: EpPlan, group=None) -> torch.Ten
     """Send the owned experts' outputs [n_recv, H] (expert-major) back to
     their sources; returns this rank's expert outputs in its own dispatched
     order [rows, H]."""
-    back = y_local[plan.perm].contiguous()
+    if y_local.is_cuda:  # the library's row-move kernel
+        back = _moe().moe_permute_rows(y_local.contiguous(), plan.perm)
+    else:
+        back = y_local[plan.perm].contiguous()
     out = y_local.new_empty(sum(plan.send_splits), y_local.shape[1])
     dist.all_to_all_single(out, back, plan.send_splits, plan.recv_splits, group=group)
     return out

@@ -148,6 +148,20 @@ def test_grouped_route_dispatch_rejects_bad_arguments(lib):
     assert call(bias=P(0x100002)) == 5
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, 4, FAKE, 4, FAKE, 4, 16, 0), 1), ((FAKE, 4, None, 4, FAKE, 4, 16, 0), 1),
+    ((FAKE, 4, FAKE, 4, None, 4, 16, 0), 1), ((FAKE, -1, FAKE, 4, FAKE, 4, 16, 0), 2),
+    ((FAKE, 4, FAKE, 4, FAKE, 4, 0, 0), 2), ((FAKE, 4, FAKE, 3, FAKE, 4, 16, 0), 2),  # gather writes 4 rows into 3
+    ((FAKE, 3, FAKE, 4, FAKE, 4, 16, 1), 2),                                          # scatter reads 4 rows of 3
+])
+def test_permute_rows_rejects_bad_arguments(lib, args, status):
+    assert lib.moe_permute_rows(*args, None) == status
+
+
+def test_permute_rows_zero_rows_is_a_no_op(lib):
+    assert lib.moe_permute_rows(None, 0, None, 0, None, 0, 16, 0, None) == 0
+
+
 def _create(lib, gate=FAKE, up=FAKE, down=FAKE, dtype=2, E=8, H=64, I=128, out=True):
     h = ctypes.c_void_p()
     return lib.moe_experts_create(gate, up, down, dtype, E, H, I, ctypes.byref(h) if out else None)
